@@ -1,0 +1,94 @@
+"""Plant plausible mistakes in copies of the oracle source and check that the
+pins catch every one.  The mistakes live only in temporary copies on the CPU;
+the real oracle is untouched.  CPU only."""
+import os
+import shutil
+import subprocess
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+MUTANTS = [
+    ("accept ratio inverted", "ratio = p / q;", "ratio = q / p;"),
+    ("residual sign flipped", "double r = w_out[v] - q[v];", "double r = q[v] - w_out[v];"),
+    ("accept test not strict", "(double)u_accept[di] < ratio", "(double)u_accept[di] <= ratio"),
+    ("target rows lose the per-request bonus offset",
+     "return (int64_t)cu[i] + i + j;", "return (int64_t)cu[i] + j;"),
+    ("argmax ties go to the highest index", "if (l > best) {", "if (l >= best) {"),
+    ("temperature multiplies instead of divides", "s += exp((l - m) / T);",
+     "s += exp((l - m) * T);"),
+    ("inverse CDF boundary not strict", "if (C > target)", "if (C >= target)"),
+    ("D-cut ties prefer the higher request", "return a->i < b->i ? -1 : 1;",
+     "return a->i > b->i ? -1 : 1;"),
+    ("D-cut ignores min_gain", "int64_t keep = eligible < budget ? eligible : budget;",
+     "int64_t keep = budget < n ? budget : n;"),
+    ("last rejection instead of first", "if (!accept && a == k)", "if (!accept)"),
+    ("residual fallback removed", "if (any) {", "if (1) {"),
+    ("D-cut prefix product off by one",
+     "P = P * conf[(int64_t)i * Kmax + (d - 1)];\n            cand[c].P = P;",
+     "cand[c].P = P;\n            P = P * conf[(int64_t)i * Kmax + (d - 1)];"),
+    ("q read from the target row",
+     "err = softmax_at(draft, dtype, di, V, T, x, &q);",
+     "err = softmax_at(target, dtype, target_row(cu, i, j), V, T, x, &q);"),
+    ("final draw from the previous target row",
+     "err = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a), drow,",
+     "err = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a > 0 ? a - 1 : a), drow,"),
+    ("greedy compares every draft against row 0",
+     "err = oracle_argmax_row(target, dtype, target_row(cu, i, j), V, &g);",
+     "err = oracle_argmax_row(target, dtype, target_row(cu, i, 0), V, &g);"),
+    ("padded draft stride ignored",
+     "return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)cu[i] + j;",
+     "return (int64_t)cu[i] + j;"),
+    ("softmax numerator drops the max shift",
+     "p_out[v] = exp((logit_at(logits, dtype, row, V, v) - m) / T) / s;",
+     "p_out[v] = exp(logit_at(logits, dtype, row, V, v) / T) / s;"),
+    ("inverse CDF forgets to scale u by S", "double target = u * S;", "double target = u;"),
+]
+
+
+def _pins_in_cost_order():
+    cheap = [p for p in P.ALL_PINS if p is not P.pin_lossless_chi_square]
+
+    def chi(lib):
+        P.pin_lossless_chi_square(lib, n=200_000, batch=200_000)
+    return cheap + [chi]
+
+
+@pytest.fixture(scope="module")
+def mutant_dir(tmp_path_factory):
+    d = tmp_path_factory.mktemp("oracle_mutants")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(mutant_dir, name, old, new):
+    src = open(oracle.SRC).read()
+    assert src.count(old) >= 1, f"mutation site for '{name}' not found in oracle.c"
+    mutated = src.replace(old, new)
+    tag = "".join(c if c.isalnum() else "_" for c in name)
+    c_path = os.path.join(mutant_dir, f"{tag}.c")
+    so_path = os.path.join(mutant_dir, f"lib{tag}.so")
+    with open(c_path, "w") as f:
+        f.write(mutated)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-w", "-o", so_path, c_path, "-lm"], check=True)
+    lib = oracle.load(so_path)
+    for pin in _pins_in_cost_order():
+        try:
+            pin(lib)
+        except AssertionError:
+            return  # caught
+    pytest.fail(f"no pin caught the planted mistake '{name}'")
+
+
+def test_unmutated_copy_passes(mutant_dir):
+    """The harness itself: an unmodified copy passes every pin."""
+    c_path = os.path.join(mutant_dir, "clean.c")
+    so_path = os.path.join(mutant_dir, "libclean.so")
+    shutil.copy(oracle.SRC, c_path)
+    subprocess.run(["gcc", *oracle.CFLAGS, "-o", so_path, c_path, "-lm"], check=True)
+    lib = oracle.load(so_path)
+    for pin in _pins_in_cost_order():
+        pin(lib)
