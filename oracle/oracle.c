@@ -265,6 +265,8 @@ static void emit(const int32_t *cu, int32_t i, int32_t draft_stride, const int32
 
 /*
  * Greedy verification (T = 0).  Target row j's choice g_j is its argmax.
+ * Every row of a request is read, so a non-finite value in any of them is an
+ * error even past the first mismatch.
  * Draft j is accepted iff x_j == g_j; a = first mismatch (or K).  Emitted:
  * x_0..x_{a-1}, then g_a (the bonus row's argmax when a = K).
  * Returns the first error met; a failing request gets -1 outputs.
@@ -290,17 +292,16 @@ int oracle_verify_greedy(const void *target, int dtype, const int32_t *tokens,
             if (x < 0 || x >= V)
                 err = ORC_ERR_INVALID_ARG;
         }
+        /* every row of the request is read: g_0..g_K first, then the match */
+        int32_t g[ORC_MAX_DRAFT + 1];
+        for (int32_t j = 0; j <= k && err == ORC_OK; ++j)
+            err = oracle_argmax_row(target, dtype, target_row(cu, i, j), V, &g[j]);
         int32_t a = k, y = -1;
-        for (int32_t j = 0; j <= k && err == ORC_OK; ++j) {
-            int32_t g;
-            err = oracle_argmax_row(target, dtype, target_row(cu, i, j), V, &g);
-            if (err != ORC_OK)
-                break;
-            if (j == k || tokens[draft_index(cu, i, j, draft_stride)] != g) {
-                a = j;
-                y = g;
-                break;
-            }
+        if (err == ORC_OK) {
+            a = 0;
+            while (a < k && tokens[draft_index(cu, i, a, draft_stride)] == g[a])
+                ++a;
+            y = g[a];
         }
         if (err != ORC_OK) {
             poison_request(cu, i, out_tokens, out_accept_len);
@@ -368,6 +369,8 @@ int oracle_final_weights(const void *target, const void *draft, int dtype, int64
  * out_p/out_q (draft index, float) hold p_j and q_j for every j < K.
  * Optional diagnostics: out_ratio[draft index] = p_j/q_j (+inf when q_j = 0
  * and p_j > 0); out_final[4*i..] = {u*S, S, C(y-1), C(y)} of the final draw.
+ * Every row of a request (including the bonus row after an early rejection)
+ * is read: a non-finite value in any of them is an error.
  * T == 0 runs the greedy verification.  Returns the first error met.
  */
 int oracle_verify_sample(const void *target, const void *draft, int dtype,
@@ -423,6 +426,10 @@ int oracle_verify_sample(const void *target, const void *draft, int dtype,
                 out_ratio[di] = ratio;
             if (!accept && a == k)
                 a = j;
+        }
+        if (err == ORC_OK) { /* the bonus row is read even when a < K */
+            double mb, sb;
+            err = oracle_softmax_stats(target, dtype, target_row(cu, i, k), V, T, &mb, &sb);
         }
         int32_t y = -1;
         if (err == ORC_OK) {

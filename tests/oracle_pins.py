@@ -258,6 +258,11 @@ def pin_greedy_errors(lib):
     res = O.verify_greedy(target, np.array([1], np.int32), np.array([1, 1, 1], np.int32),
                           lib=lib)
     assert res.status == O.ERR_INVALID_ARG
+    # a NaN past the first mismatch is still an error (every row is read)
+    t4 = target.copy()
+    t4[1, 3] = np.nan
+    res = O.verify_greedy(t4, np.array([0], np.int32), cu, lib=lib)  # mismatch at 0
+    assert res.status == O.ERR_NONFINITE and res.accept_len.tolist() == [-1, 0]
 
 
 # ---------------------------------------------------------------------------
@@ -486,6 +491,14 @@ def pin_sample_errors(lib):
     assert res.status == O.ERR_NONFINITE and res.accept_len[0] == -1
     res = O.verify_sample(t, d, np.array([1], np.int32), cu, -1.0, u1, u2, lib=lib)
     assert res.status == O.ERR_INVALID_ARG
+    # every row of a request is read: a NaN in the bonus row is an error even
+    # when position 0 rejects (p(x) = 0 forces the rejection here)
+    t3 = np.zeros((3, 4), np.float32)
+    t3[0, 1] = -np.inf
+    t3[1, 2] = np.nan
+    res = O.verify_sample(t3, d, np.array([1], np.int32), cu, 1.0, np.zeros(1, np.float32),
+                          u2, lib=lib)
+    assert res.status == O.ERR_NONFINITE and res.accept_len.tolist() == [-1, 0]
 
 
 # ---------------------------------------------------------------------------

@@ -36,8 +36,10 @@ MUTANTS = [
      "err = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a), drow,",
      "err = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a > 0 ? a - 1 : a), drow,"),
     ("greedy compares every draft against row 0",
-     "err = oracle_argmax_row(target, dtype, target_row(cu, i, j), V, &g);",
-     "err = oracle_argmax_row(target, dtype, target_row(cu, i, 0), V, &g);"),
+     "while (a < k && tokens[draft_index(cu, i, a, draft_stride)] == g[a])",
+     "while (a < k && tokens[draft_index(cu, i, a, draft_stride)] == g[0])"),
+    ("greedy final token from the row before the mismatch", "y = g[a];",
+     "y = g[a > 0 ? a - 1 : 0];"),
     ("padded draft stride ignored",
      "return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)cu[i] + j;",
      "return (int64_t)cu[i] + j;"),
