@@ -1,0 +1,629 @@
+#!/usr/bin/env python3
+"""Benchmark of batched draft verification (+ D-cut) on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mtp|block|block_greedy|dcut|tiny]
+    python bench.py --impl reference ...     (the CPU oracle, timed on the host cores)
+
+One step = one pass of the whole verification path over one batch whose
+inputs are already in HBM: spec_verify_sample (row statistics + accept test +
+first-rejection scan, then the residual / bonus draw), preceded by
+dcut_allocate for the D-cut workload.  The timed region replays CUDA graphs
+of those C-ABI calls (the calls themselves are what is captured), bracketed
+by a barrier and a device synchronise, timed with CUDA events; inputs rotate
+through enough independent sets that their total exceeds twice the L2 size.
+Rank 0 prints one JSON line.  Under torchrun every rank verifies its own
+independent batches (weak scaling, no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from draft_verification_02_b300 import workloads as W  # noqa: E402
+
+METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of peak) at 1 B300"
+UNIT = "positions/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6400.0
+WORKLOADS = {  # name -> (workload, temperature)
+    "mtp": (W.MTP, 1.0),
+    "block": (W.BLOCK, 0.7),
+    "block_greedy": (W.BLOCK, 0.0),
+    "dcut": (W.DCUT, 1.0),
+    "tiny": (W.TINY, 1.0),
+}
+KERNEL_SOURCES = ["draft_verification_02_b300/csrc/verify.cu",
+                  "draft_verification_02_b300/csrc/common.cuh",
+                  "draft_verification_02_b300/csrc/dcut.cu"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mtp")
+    ap.add_argument("--graph-steps", type=int, default=200,
+                    help="verify steps captured per CUDA graph")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU-oracle baseline sample length")
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="time budget of the whole reference run")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host-side only)
+# ---------------------------------------------------------------------------
+
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float, device) -> float:
+        if self.pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float, device) -> float:
+        if self.pg is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def rank_seed_offset(rank: int) -> int:
+    """Independent input sets per rank (weak scaling)."""
+    return 1000 * rank
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str):
+    """DRAM bytes per launch from a committed ncu summary line
+    '<workload> <kernel> <source hash> <bytes>' in profiles/ncu_traffic.txt,
+    valid only while the kernel sources still hash the same."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    try:
+        want = kernel_source_hash()
+        with open(path) as f:
+            for line in f:
+                p = line.split()
+                if len(p) >= 4 and p[0] == workload and p[1] == kernel and p[2] == want:
+                    return float(p[3])
+    except FileNotFoundError:
+        pass
+    return None
+
+
+def workload_desc(w, T):
+    return f"{W.describe(w)}, T={T}"
+
+
+def l2_bytes(device) -> int:
+    try:
+        return int(torch.cuda.get_device_properties(device).L2_cache_size)
+    except Exception:
+        return 126 * 1024 * 1024
+
+
+def pci_bus_id(device) -> str:
+    try:
+        p = torch.cuda.get_device_properties(device)
+        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+    except Exception:
+        return ""
+
+
+class ClockSampler:
+    def __init__(self, device, enabled=True):
+        self.proc = None
+        self.path = None
+        if not enabled:
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".txt")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                [sys.executable, "-m", "draft_verification_02_b300.clocks", "--pci",
+                 pci_bus_id(device), "--interval-ms", "5", "--out", self.path],
+                cwd=ROOT, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def wait_first_sample(self, timeout=5.0):
+        t_end = time.time() + timeout
+        while self.proc is not None and time.time() < t_end:
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                pass
+            time.sleep(0.02)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if self.path is None:
+            return {"samples": 0, "error": "clock sampling disabled"}
+        from draft_verification_02_b300 import clocks
+        s = clocks.summarize(self.path, t0, t1)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
+        return s
+
+
+# ---------------------------------------------------------------------------
+# host-side oracle sampling (CPU baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+
+def host_arrays(batch):
+    def arr(t):
+        t = t.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            return t.view(torch.int16).numpy().view(np.uint16)
+        return t.numpy()
+    return {"k": arr(batch.k), "cu": arr(batch.cu_draft), "target": arr(batch.target_logits),
+            "draft": arr(batch.draft_logits), "tokens": arr(batch.draft_tokens),
+            "u_accept": arr(batch.u_accept), "u_final": arr(batch.u_final),
+            "stride": batch.draft_stride, "T": batch.temperature}
+
+
+def oracle_request(orc, h, i):
+    """Run the oracle on request i alone; returns its number of verified positions."""
+    K = int(h["k"][i])
+    t0 = int(h["cu"][i]) + i
+    d0 = i * h["stride"] if h["stride"] else int(h["cu"][i])
+    cu = np.array([0, K], np.int32)
+    tgt = h["target"][t0:t0 + K + 1]
+    if h["T"] == 0:
+        r = orc.verify_greedy(tgt, h["tokens"][d0:d0 + K], cu)
+    else:
+        r = orc.verify_sample(tgt, h["draft"][d0:d0 + K], h["tokens"][d0:d0 + K], cu, h["T"],
+                              h["u_accept"][d0:d0 + K], h["u_final"][i:i + 1])
+    if r.status != orc.OK:
+        raise RuntimeError(f"oracle status {r.status}")
+    return K
+
+
+def oracle_sample_rate(h, seconds, threads, max_requests=None):
+    """Positions/s of the oracle over whole requests, round-robin, on `threads`
+    host threads (the C oracle releases the GIL), for about `seconds`."""
+    import oracle as orc
+    orc.load()
+    B = len(h["k"])
+    order = list(range(B))
+    done_pos = 0
+    done_req = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        i = 0
+        while True:
+            chunk = [order[(i + j) % B] for j in range(threads)]
+            i += threads
+            done_pos += sum(ex.map(lambda r: oracle_request(orc, h, r), chunk))
+            done_req += len(chunk)
+            el = time.perf_counter() - t0
+            if el >= seconds or (max_requests and done_req >= max_requests):
+                break
+    el = time.perf_counter() - t0
+    return done_pos / el, done_req, el
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+
+def run_ours(args, dist):
+    from draft_verification_02_b300 import specverify as sv
+    from draft_verification_02_b300.verifier import Verifier
+
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    dist.init("nccl")
+    w, T = WORKLOADS[args.workload]
+    rows = W.max_target_rows(w)
+    is_dcut = bool(w.kmax)
+    v = Verifier(w.B, rows, w.V, device=device)
+
+    # ---- input sets, resident in HBM
+    def make_set(rep):
+        s = {}
+        if is_dcut:
+            prob = W.make_dcut_problem(w, device, rep=rep)
+            d = v.dcut(prob.conf, prob.kmax, prob.budget)
+            depth = d["depth"].cpu()
+            b = W.make_verify_batch(w, T, device, rep=rep, depths=depth, draft_stride=w.kmax)
+            if b.target_logits.shape[0] < rows:  # pad to the host bound
+                t = torch.zeros((rows, w.V), dtype=b.target_logits.dtype, device=device)
+                t[:b.target_logits.shape[0]] = b.target_logits
+                b.target_logits = t
+            s["prob"] = prob
+            s["dcut_out"] = {"depth": torch.empty(w.B, dtype=torch.int32, device=device),
+                             "cu": torch.empty(w.B + 1, dtype=torch.int32, device=device),
+                             "expected": torch.empty(w.B, dtype=torch.float32, device=device)}
+        else:
+            b = W.make_verify_batch(w, T, device, rep=rep)
+        s["batch"] = b
+        s["out"] = v.outputs(b, rows)
+        return s
+
+    first = make_set(rank_seed_offset(dist.rank))
+    set_bytes = sum(t.numel() * t.element_size() for t in
+                    (first["batch"].target_logits, first["batch"].draft_logits))
+    n_sets = max(2, min(64, math.ceil(2.2 * l2_bytes(device) / max(set_bytes, 1))))
+    sets = [first] + [make_set(rank_seed_offset(dist.rank) + r) for r in range(1, n_sets)]
+    batch0 = first["batch"]
+    positions = batch0.n_draft          # verified draft positions per step
+    alg_bytes = batch0.algorithmic_bytes()
+
+    def step(s, trace_dcut=None, trace_verify=None):
+        b = s["batch"]
+        cu = b.cu_draft
+        if is_dcut:
+            if trace_dcut is not None:
+                sv.spec_set_trace(trace_dcut)
+            d = s["dcut_out"]
+            sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax, s["prob"].budget, 0.0,
+                             d["depth"], d["cu"], d["expected"], v.workspace)
+            cu = d["cu"]
+        if trace_verify is not None:
+            sv.spec_set_trace(trace_verify)
+        o = s["out"]
+        if T == 0:
+            st = sv.spec_verify_greedy(b.target_logits, b.draft_tokens, cu, b.B, b.V, rows,
+                                       b.draft_stride, o["tokens"], o["accept_len"], v.workspace)
+        else:
+            st = sv.spec_verify_sample(b.target_logits, b.draft_logits, b.draft_tokens, cu, b.B,
+                                       b.V, rows, b.draft_stride, T, b.u_accept, b.u_final,
+                                       o["tokens"], o["accept_len"], o["p"], o["q"],
+                                       v.workspace)
+        if trace_dcut is not None or trace_verify is not None:
+            sv.spec_set_trace(None)
+        return st
+
+    # ---- warm-up (eager), launch count, correctness of statuses
+    n0 = sv.spec_kernel_launch_count()
+    for k in range(max(1, args.warmup)):
+        sv.check(step(sets[k % n_sets]), "warm-up step")
+    torch.cuda.synchronize(device)
+    launches_per_step = (sv.spec_kernel_launch_count() - n0) // max(1, args.warmup)
+    sv.check(v.device_status(), "device status after warm-up")
+
+    # ---- CUDA graphs of G steps with per-kernel trace events
+    K = args.steps
+    G = max(1, min(K, args.graph_steps))
+    n_verify_ev = 3 if T > 0 else 2
+    stream = torch.cuda.Stream(device)
+
+    def make_events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    def capture(n_steps, offset):
+        evs = [(make_events(2) if is_dcut else None, make_events(n_verify_ev))
+               for _ in range(n_steps)]
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n_steps):
+                step(sets[(offset + k) % n_sets], evs[k][0], evs[k][1])
+        return g, evs
+
+    g_main, ev_main = capture(G, 0)
+    n_rep, rem = divmod(K, G)
+    g_rem = capture(rem, n_rep * G)[0] if rem else None
+    # one untimed replay so that the graphs' first-launch cost is not timed
+    g_main.replay()
+    torch.cuda.synchronize(device)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(device, enabled=not args.no_clocks)
+    sampler.wait_first_sample()
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n_rep):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    dist.barrier()
+    sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms_max = dist.max(elapsed_ms, device)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    st_after = v.device_status()
+    if st_after != sv.SPEC_OK:
+        raise RuntimeError(f"device status after the timed region: {st_after}")
+
+    # per-kernel durations from the last replay of the main graph
+    rows_us = [ev_main[k][1][0].elapsed_time(ev_main[k][1][1]) * 1e3 for k in range(G)]
+    final_us = ([ev_main[k][1][1].elapsed_time(ev_main[k][1][2]) * 1e3 for k in range(G)]
+                if T > 0 else [])
+    dcut_us = ([ev_main[k][0][0].elapsed_time(ev_main[k][0][1]) * 1e3 for k in range(G)]
+               if is_dcut else [])
+    rows_mean = statistics.mean(rows_us)
+
+    total_positions = dist.sum(positions * K, device)
+    value = total_positions / (elapsed_ms_max / 1e3)
+    ms_per_step = elapsed_ms_max / K
+    peak, peak_kind = measured_hbm_peak()
+    step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+    achieved = alg_bytes / (rows_mean / 1e6) / 1e9
+
+    # acceptance statistics of the last outputs (the quantities the pages report)
+    acc = {}
+    if T >= 0:
+        a = first["out"]["accept_len"].cpu().numpy().astype(np.int64)
+        k_arr = batch0.k.cpu().numpy()
+        rates = []
+        for j in range(int(k_arr.max()) if k_arr.size else 0):
+            elig = k_arr > j
+            reach = (a >= j) & elig
+            if reach.sum():
+                rates.append(round(float(((a > j) & reach).sum() / reach.sum()), 4))
+        acc = {"mean_accepted_len": round(float(a.mean()), 4), "per_position_rate": rates}
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist)
+
+    # ---- CPU oracle baseline (rank 0, N = 1)
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, nreq, el = oracle_sample_rate(host_arrays(batch0), args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{nreq} whole requests of input set 0 ({workload_desc(w, T)}), "
+                         f"one oracle call per request on {threads} host threads, {el:.1f} s"}
+
+    traffic = recorded_traffic(args.workload, "rows_kernel")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": workload_desc(w, T), "B": w.B, "V": w.V, "logits_dtype": w.dtype,
+            "temperature": T, "verified_positions_per_step": positions,
+            "target_rows_per_step": batch0.n_target_rows,
+            "l2": f"inputs rotate through {n_sets} independent sets "
+                  f"({n_sets * set_bytes / 1e6:.0f} MB > 2x L2 of {l2_bytes(device) / 1e6:.0f} MB)",
+            "timing": f"CUDA graphs of {G} steps replayed, CUDA events on the launching stream",
+            "parallelism": f"{dist.world} GPU(s), independent batches per GPU",
+        },
+        "requests_per_s": dist.sum(w.B * K, device) / (elapsed_ms_max / 1e3),
+        "hbm_gbs_step": step_gbs,
+        "hbm_frac_step": step_gbs / peak,
+        "hbm_frac_step_of_nominal_8000": step_gbs / NOMINAL_HBM_GBS,
+        "roofline": {"bound": "hbm", "kernel": "rows_kernel", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"of {peak_kind}", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "launch_us_mean": rows_mean},
+        "kernels_us": {"rows_kernel": rows_mean,
+                       "final_kernel": statistics.mean(final_us) if final_us else None,
+                       "dcut_kernel": statistics.mean(dcut_us) if dcut_us else None},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "acceptance": acc,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist):
+    """Same metric through the public C-ABI calls, with every step's inputs
+    copied from pinned host memory and its results read back."""
+    from draft_verification_02_b300 import specverify as sv
+    steps = max(1, min(args.e2e_steps, args.steps))
+    names = ["target_logits", "draft_logits", "draft_tokens", "cu_draft", "u_accept", "u_final"]
+    host = []
+    for s in sets[:min(n_sets, 3)]:
+        b = s["batch"]
+        hs = {n: getattr(b, n).cpu().pin_memory() for n in names}
+        if is_dcut:
+            hs["conf"] = s["prob"].conf.cpu().pin_memory()
+            hs["kmax"] = s["prob"].kmax.cpu().pin_memory()
+        host.append(hs)
+    out_host = torch.empty(rows + w.B, dtype=torch.int32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = out_host.numel() * out_host.element_size()
+    stream = torch.cuda.current_stream(device)
+
+    def one(k):
+        s = sets[k % len(host)]
+        hs = host[k % len(host)]
+        b = s["batch"]
+        for n in names:
+            getattr(b, n).copy_(hs[n], non_blocking=True)
+        cu = b.cu_draft
+        if is_dcut:
+            s["prob"].conf.copy_(hs["conf"], non_blocking=True)
+            s["prob"].kmax.copy_(hs["kmax"], non_blocking=True)
+            d = s["dcut_out"]
+            sv.check(sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax,
+                                      s["prob"].budget, 0.0, d["depth"], d["cu"],
+                                      d["expected"], v.workspace), "dcut")
+            cu = d["cu"]
+        o = s["out"]
+        if T == 0:
+            st = sv.spec_verify_greedy(b.target_logits, b.draft_tokens, cu, b.B, b.V, rows,
+                                       b.draft_stride, o["tokens"], o["accept_len"], v.workspace)
+        else:
+            st = sv.spec_verify_sample(b.target_logits, b.draft_logits, b.draft_tokens, cu, b.B,
+                                       b.V, rows, b.draft_stride, T, b.u_accept, b.u_final,
+                                       o["tokens"], o["accept_len"], o["p"], o["q"],
+                                       v.workspace)
+        sv.check(st, "verify")
+        out_host[:rows].copy_(o["tokens"][:rows], non_blocking=True)
+        out_host[rows:].copy_(o["accept_len"], non_blocking=True)
+
+    for k in range(3):
+        one(k)
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        one(k)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    dist.barrier()
+    ms = dist.max(e0.elapsed_time(e1), device)
+    value = dist.sum(positions * steps, device) / (ms / 1e3)
+    return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": steps, "ms_per_step": ms / steps}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return  # the other ranks exit without work
+    import oracle as orc
+    orc.load()
+    w, T = WORKLOADS[args.workload]
+    if w.kmax:
+        prob = W.make_dcut_problem(w, "cpu")
+        o = orc.dcut_allocate(prob.conf.numpy(), prob.kmax.numpy(), prob.budget)
+        batch = W.make_verify_batch(w, T, "cpu", depths=torch.from_numpy(o.depth),
+                                    draft_stride=w.kmax)
+    else:
+        batch = W.make_verify_batch(w, T, "cpu")
+    h = host_arrays(batch)
+    threads = os.cpu_count() or 1
+    # size each step's sample of whole requests to the time budget
+    t0 = time.perf_counter()
+    oracle_request(orc, h, 0)
+    t_req = max(time.perf_counter() - t0, 1e-4)
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
+    n_req = int(max(1, min(w.B, per_step * threads / t_req)))
+    ex = ThreadPoolExecutor(threads)
+
+    def one(k):
+        reqs = [(k * n_req + j) % w.B for j in range(n_req)]
+        return sum(ex.map(lambda r: oracle_request(orc, h, r), reqs))
+
+    for k in range(args.warmup):
+        one(k)
+    pos = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        pos += one(k)
+    el = time.perf_counter() - t0
+    ex.shutdown()
+    value = pos / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(w, T), "B": w.B, "V": w.V,
+                   "logits_dtype": w.dtype, "temperature": T,
+                   "sample_per_step": f"{n_req} of {w.B} requests"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n_req} whole requests per step of {workload_desc(w, T)}, "
+                                   f"one oracle call per request on {threads} host threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_ours(args, dist)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,258 @@
+// api.cu - the C ABI (include/specverify.h): argument checks, workspace
+// sizing, launches on the caller's stream, device status, trace hook.
+// Nothing here allocates device memory or synchronises, except
+// spec_get_device_status, whose job is to synchronise and read.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "common.cuh"
+#include "launch.h"
+#include "specverify.h"
+
+namespace {
+
+constexpr int kMaxTraceEvents = 16;
+thread_local cudaEvent_t g_trace[kMaxTraceEvents];
+thread_local int g_trace_n = 0;
+thread_local int64_t g_launches = 0;
+
+sv::Tracer make_tracer()
+{
+    sv::Tracer t;
+    t.events = g_trace_n > 0 ? g_trace : nullptr;
+    t.n = g_trace_n;
+    return t;
+}
+
+int cuda_status(cudaError_t e)
+{
+    return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+bool valid_dtype(int dtype) { return dtype == SPEC_F32 || dtype == SPEC_BF16; }
+
+// Checks shared by both verification calls; SPEC_OK when the sizes are usable.
+int check_verify_sizes(int32_t B, int32_t V, int64_t max_target_rows, int32_t draft_stride)
+{
+    if (B < 0 || B > SPEC_MAX_BATCH || V < 1 || draft_stride < 0 || draft_stride > (1 << 20))
+        return SPEC_ERR_INVALID_ARG;
+    if (max_target_rows < B || max_target_rows > (int64_t)B * (SPEC_MAX_DRAFT + 1))
+        return SPEC_ERR_INVALID_ARG;
+    if (sv::chunking(V, 4).nchunks > sv::kMaxChunks)
+        return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+namespace sv {
+
+void Tracer::begin(cudaStream_t s)
+{
+    next = 0;
+    if (next < n)
+        cudaEventRecord(events[next++], s);
+}
+
+void Tracer::after_kernel(cudaStream_t s)
+{
+    ++g_launches;
+    if (next < n)
+        cudaEventRecord(events[next++], s);
+}
+
+}  // namespace sv
+
+extern "C" {
+
+size_t spec_workspace_size(int32_t B, int64_t max_target_rows, int32_t V)
+{
+    if (B < 0 || max_target_rows < 0 || V < 0)
+        return 0;
+    if (V > 0 && sv::chunking(V, 4).nchunks > sv::kMaxChunks)
+        return 0;
+    return sv::ws_layout(B, max_target_rows, V).total;
+}
+
+int spec_workspace_init(void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (!workspace || ws_bytes == 0)
+        return SPEC_ERR_WORKSPACE;
+    return cuda_status(cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draft_tokens,
+                       const int32_t *cu_draft, int32_t B, int32_t V, int64_t max_target_rows,
+                       int32_t draft_stride, int32_t *out_tokens, int32_t *out_accept_len,
+                       void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (!valid_dtype(dtype))
+        return SPEC_ERR_INVALID_ARG;
+    int st = check_verify_sizes(B, V, max_target_rows, draft_stride);
+    if (st != SPEC_OK)
+        return st;
+    if (B == 0)
+        return SPEC_OK;
+    if (!target_logits || !cu_draft || !out_tokens || !out_accept_len ||
+        (!draft_tokens && max_target_rows > B))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(B, max_target_rows, V))
+        return SPEC_ERR_WORKSPACE;
+    sv::VerifyArgs a{};
+    a.target = target_logits;
+    a.draft = nullptr;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.cu = cu_draft;
+    a.B = B;
+    a.V = V;
+    a.max_rows = max_target_rows;
+    a.draft_stride = draft_stride;
+    a.temperature = 0.0;
+    a.out_tokens = out_tokens;
+    a.out_len = out_accept_len;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_verify(a, (cudaStream_t)stream, tr));
+}
+
+int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
+                       const int32_t *draft_tokens, const int32_t *cu_draft, int32_t B,
+                       int32_t V, int64_t max_target_rows, int32_t draft_stride,
+                       float temperature, const float *u_accept, const float *u_final,
+                       int32_t *out_tokens, int32_t *out_accept_len, float *out_p,
+                       float *out_q, void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (!(temperature >= 0.f) || std::isinf(temperature))
+        return SPEC_ERR_INVALID_ARG;
+    if (temperature == 0.f)
+        return spec_verify_greedy(target_logits, dtype, draft_tokens, cu_draft, B, V,
+                                  max_target_rows, draft_stride, out_tokens, out_accept_len,
+                                  workspace, ws_bytes, stream);
+    if (!valid_dtype(dtype))
+        return SPEC_ERR_INVALID_ARG;
+    int st = check_verify_sizes(B, V, max_target_rows, draft_stride);
+    if (st != SPEC_OK)
+        return st;
+    if (B == 0)
+        return SPEC_OK;
+    const bool drafts = max_target_rows > B;
+    if (!target_logits || !cu_draft || !out_tokens || !out_accept_len || !u_final ||
+        (drafts && (!draft_logits || !draft_tokens || !u_accept)))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(B, max_target_rows, V))
+        return SPEC_ERR_WORKSPACE;
+    sv::VerifyArgs a{};
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.cu = cu_draft;
+    a.B = B;
+    a.V = V;
+    a.max_rows = max_target_rows;
+    a.draft_stride = draft_stride;
+    a.temperature = (double)temperature;
+    a.u_accept = u_accept;
+    a.u_final = u_final;
+    a.out_tokens = out_tokens;
+    a.out_len = out_accept_len;
+    a.out_p = out_p;
+    a.out_q = out_q;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_verify(a, (cudaStream_t)stream, tr));
+}
+
+int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kmax,
+                  int32_t budget, float min_gain, int32_t *out_depth, int32_t *out_cu,
+                  float *out_expected_len, void *workspace, size_t ws_bytes,
+                  spec_stream_t stream)
+{
+    if (B < 0 || B > SPEC_MAX_BATCH || Kmax < 0 || Kmax > SPEC_MAX_DRAFT || budget < 0 ||
+        std::isnan(min_gain))
+        return SPEC_ERR_INVALID_ARG;
+    int bp = 1, kp = 1;
+    while (bp < B)
+        bp <<= 1;
+    while (kp < Kmax)
+        kp <<= 1;
+    if ((int64_t)bp * kp > SPEC_DCUT_MAX_CANDIDATES)
+        return SPEC_ERR_INVALID_ARG;
+    if (!out_cu || (B > 0 && (!kmax || !out_depth || (Kmax > 0 && !conf))))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(0, 0, 0))
+        return SPEC_ERR_WORKSPACE;
+    sv::DcutArgs a{};
+    a.conf = conf;
+    a.kmax = kmax;
+    a.B = B;
+    a.Kmax = Kmax;
+    a.budget = budget;
+    a.min_gain = min_gain;
+    a.out_depth = out_depth;
+    a.out_cu = out_cu;
+    a.out_expected = out_expected_len;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_dcut(a, (cudaStream_t)stream, tr));
+}
+
+int spec_get_device_status(void *workspace, spec_stream_t stream)
+{
+    if (!workspace)
+        return SPEC_ERR_WORKSPACE;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t word = 0;
+    unsigned char *status = static_cast<unsigned char *>(workspace) + sv::ws_layout(0, 0, 0).status;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaMemcpyAsync(&word, status, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaMemsetAsync(status, 0, sizeof word, s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (word & sv::ST_TIMEOUT)
+        return SPEC_ERR_TIMEOUT;
+    if (word & sv::ST_INVALID)
+        return SPEC_ERR_INVALID_ARG;
+    if (word & sv::ST_NONFINITE)
+        return SPEC_ERR_NONFINITE;
+    return SPEC_OK;
+}
+
+const char *spec_status_string(int status)
+{
+    switch (status) {
+    case SPEC_OK:
+        return "ok";
+    case SPEC_ERR_INVALID_ARG:
+        return "invalid argument (or malformed offsets / token id on the device)";
+    case SPEC_ERR_WORKSPACE:
+        return "workspace missing or too small";
+    case SPEC_ERR_CUDA:
+        return "CUDA runtime error";
+    case SPEC_ERR_NONFINITE:
+        return "NaN or +inf logit, or a row with every entry masked";
+    case SPEC_ERR_TIMEOUT:
+        return "a bounded wait for an asynchronous copy expired";
+    default:
+        return "unknown status";
+    }
+}
+
+int spec_set_trace(void *const *events, int n_events)
+{
+    if (n_events < 0 || n_events > kMaxTraceEvents || (n_events > 0 && !events))
+        return SPEC_ERR_INVALID_ARG;
+    for (int k = 0; k < n_events; ++k)
+        g_trace[k] = static_cast<cudaEvent_t>(events[k]);
+    g_trace_n = n_events;
+    return SPEC_OK;
+}
+
+int64_t spec_kernel_launch_count(void) { return g_launches; }
+
+}  // extern "C"

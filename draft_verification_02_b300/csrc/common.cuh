@@ -1,0 +1,284 @@
+// common.cuh - device helpers shared by the verification and D-cut kernels:
+// inline-PTX wrappers for mbarriers and 1-D TMA bulk copies (sm_90+ forms,
+// compiled for sm_103a), a bounded mbarrier wait, NaN-propagating max and
+// warp/block reductions, and the workspace layout.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+constexpr int kThreads = 256;  // threads per CTA of the row kernels
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxDraft = 32;  // drafted tokens per request (one warp ballot)
+constexpr int kMaxBatch = 4096;
+constexpr int kDcutMaxCand = 8192;
+
+#ifndef SV_CHUNK_BYTES
+#define SV_CHUNK_BYTES 32768  // bytes of one row chunk staged in shared memory
+#endif
+constexpr int kChunkBytes = SV_CHUNK_BYTES;
+constexpr int kMaxChunks = 1024;  // chunks per row (bounds V)
+
+// Device status bits (the workspace status word).
+enum : uint32_t { ST_INVALID = 1u, ST_NONFINITE = 2u, ST_TIMEOUT = 4u };
+
+// Bounded waits give up after this many nanoseconds of %globaltimer.
+#ifndef SV_WAIT_NS
+#define SV_WAIT_NS 2000000000ull
+#endif
+
+// -------------------------------------------------------------------------
+// workspace layout
+// -------------------------------------------------------------------------
+
+// One chunk partial: softmax (m, s) or argmax (m = value, idx = index).
+struct __align__(16) Partial {
+    float m;
+    int32_t idx;
+    double s;
+};
+
+// Per-request result of the accept stage, consumed by the final-draw kernel.
+struct __align__(16) Handoff {
+    int32_t a;      // accepted length; -1 = request poisoned / nothing to draw
+    int32_t pad;
+    int64_t trow;   // target row of the final draw
+    int64_t drow;   // draft row of a rejection, -1 for the bonus draw
+    float m_t, m_d; // row maxima
+    double s_t, s_d;// row sums of exp((l - m) / T)
+};
+
+struct Chunking {
+    int nchunks;
+    int chunk_elems;
+};
+
+// Rows are cut into nearly equal chunks of at most kChunkBytes, each a
+// multiple of 16 bytes long (the TMA bulk-copy granule).
+inline Chunking chunking(int V, int elem_bytes)
+{
+    Chunking c{0, 0};
+    if (V <= 0)
+        return c;
+    const int64_t row_bytes = (int64_t)V * elem_bytes;
+    int n = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
+    const int per16 = 16 / elem_bytes;
+    int64_t ce = ((int64_t)V + n - 1) / n;
+    ce = (ce + per16 - 1) / per16 * per16;
+    c.chunk_elems = (int)ce;
+    c.nchunks = (int)(((int64_t)V + ce - 1) / ce);
+    return c;
+}
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t status, cnt1, cnt2, part1, hand, part2, total;
+};
+
+// Sized for the worst case over both dtypes (fp32 has the most chunks).
+inline WsLayout ws_layout(int B, int64_t max_rows, int V)
+{
+    WsLayout L{};
+    const int nch = V > 0 ? chunking(V, 4).nchunks : 0;
+    const int64_t slots = max_rows > 0 ? 2 * max_rows - B : 0;
+    size_t off = 0;
+    L.status = off;
+    off += 256;
+    L.cnt1 = off;
+    off = align_up(off + (size_t)B * 4, 256);
+    L.cnt2 = off;
+    off = align_up(off + (size_t)B * 4, 256);
+    L.part1 = off;
+    off = align_up(off + (size_t)(slots > 0 ? slots : 0) * nch * sizeof(Partial), 256);
+    L.hand = off;
+    off = align_up(off + (size_t)B * sizeof(Handoff), 256);
+    L.part2 = off;
+    off = align_up(off + (size_t)B * nch * sizeof(double), 256);
+    L.total = off;
+    return L;
+}
+
+// -------------------------------------------------------------------------
+// PTX wrappers
+// -------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make the initialised barrier visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion signalled on `bar` (tx bytes).
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t phase)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(smem_u32(bar)), "r"(phase)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `phase` of `bar` to complete, giving up after SV_WAIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase)
+{
+    if (mbar_try_wait(bar, phase))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, phase))
+            return true;
+        if (globaltimer_ns() - t0 > SV_WAIT_NS)
+            return false;
+    }
+}
+
+// max that returns NaN when either input is NaN.
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+__device__ __forceinline__ float warp_max_nan(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = max_nan(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ double warp_sum_d(double v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Block-wide NaN-propagating max (kThreads threads, all participate).
+__device__ __forceinline__ float block_max_nan(float v, float *scratch /* [kWarps] */)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max_nan(v);
+    __syncthreads();
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    float r = scratch[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w)
+        r = max_nan(r, scratch[w]);
+    return r;
+}
+
+// Block-wide fp64 sum in a fixed order (deterministic).
+__device__ __forceinline__ double block_sum_d(double v, double *scratch /* [kWarps] */)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_sum_d(v);
+    __syncthreads();
+    if (lane == 0)
+        scratch[warp] = v;
+    __syncthreads();
+    double r = 0.0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        r += scratch[w];
+    return r;
+}
+
+// Element access for the two logit dtypes.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static constexpr int kPerVec = 4;  // per 16-byte vector
+    __device__ __forceinline__ static float at(const float *p, int64_t k) { return p[k]; }
+    __device__ __forceinline__ static float ld_global(const float *p, int64_t k)
+    {
+        return __ldg(p + k);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 v, float (&f)[4])
+    {
+        f[0] = __uint_as_float(v.x);
+        f[1] = __uint_as_float(v.y);
+        f[2] = __uint_as_float(v.z);
+        f[3] = __uint_as_float(v.w);
+    }
+};
+template <> struct Elem<uint16_t> {  // bfloat16 bit patterns
+    static constexpr int kPerVec = 8;
+    __device__ __forceinline__ static float at(const uint16_t *p, int64_t k)
+    {
+        return __uint_as_float((uint32_t)p[k] << 16);
+    }
+    __device__ __forceinline__ static float ld_global(const uint16_t *p, int64_t k)
+    {
+        return __uint_as_float((uint32_t)__ldg(p + k) << 16);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 v, float (&f)[8])
+    {
+        f[0] = __uint_as_float(v.x << 16);
+        f[1] = __uint_as_float(v.x & 0xffff0000u);
+        f[2] = __uint_as_float(v.y << 16);
+        f[3] = __uint_as_float(v.y & 0xffff0000u);
+        f[4] = __uint_as_float(v.z << 16);
+        f[5] = __uint_as_float(v.z & 0xffff0000u);
+        f[6] = __uint_as_float(v.w << 16);
+        f[7] = __uint_as_float(v.w & 0xffff0000u);
+    }
+};
+
+__device__ __forceinline__ void set_status(uint32_t *status, uint32_t bits)
+{
+    atomicOr(status, bits);
+}
+
+__device__ __forceinline__ uint32_t read_status(const uint32_t *status)
+{
+    return *(volatile const uint32_t *)status;
+}
+
+}  // namespace sv

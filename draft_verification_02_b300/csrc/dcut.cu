@@ -1,0 +1,233 @@
+// dcut.cu - D-cut: batch-level allocation of verification depth, one CTA.
+//
+// D-cut treats target-verification capacity as a shared batch-level resource
+// and moves depth to high-confidence prefixes ("Tencent rilascia AngelSpec in
+// open source ...", "Come AngelSpec rende DFly piu selettivo"; "Tencent
+// Hunyuan Turns Speculative Decoding Into a Full Open-Source Stack", "What
+// problem does it solve", inference layer).  Reading used here: the budget is
+// counted in verified draft tokens; the value of verifying request i to depth
+// d is the prefix product P_{i,d} = conf_i0 * ... * conf_i(d-1) (the
+// probability that the first d drafts are all accepted when conf is the
+// conditional acceptance probability), so keeping the `budget` largest
+// products over the whole batch maximises the expected number of accepted
+// tokens; a product below `min_gain` is never worth its cost.
+//
+// Kernel: every candidate (i, d) becomes one 64-bit key
+//   hi 32 bits: 0x3F800000 - bits(P)   (P in [0,1]: larger P -> smaller key)
+//   lo 32 bits: i * Kp + (d - 1)       (ties: lower request, then lower depth)
+// Each request's keys are already ascending (P never grows with d), so the
+// batch is sorted by log2(#requests) rounds of pairwise merges of sorted runs
+// in shared memory: an element's place in the merged run is its index in its
+// own run plus the number of smaller keys in the partner run (binary search;
+// keys are unique).  The first min(budget, #{P >= min_gain}) keys are kept.
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace sv {
+
+constexpr int kDcutThreads = 1024;
+
+struct DcutParams {
+    const float *conf;
+    const int32_t *kmax;
+    int B, Kmax, Kp, Bp;
+    int budget;
+    float min_gain;
+    int32_t *out_depth;
+    int32_t *out_cu;
+    float *out_expected;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ int block_excl_scan_int(int v, int *warp_tot /* [32] */, int &total)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += n;
+    }
+    if (lane == 31)
+        warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int t = warp_tot[lane];
+        int ti = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, ti, o);
+            if (lane >= o)
+                ti += n;
+        }
+        warp_tot[lane] = ti - t;  // exclusive offset of each warp
+        if (lane == 31)
+            warp_tot[32] = ti;
+    }
+    __syncthreads();
+    total = warp_tot[32];
+    return warp_tot[warp] + incl - v;
+}
+
+__global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    const int Np = p.Bp * p.Kp;
+    uint64_t *ka = reinterpret_cast<uint64_t *>(dsm);
+    uint64_t *kb = ka + Np;
+    int *depth_s = reinterpret_cast<int *>(kb + Np);
+    __shared__ int warp_tot[33];
+    __shared__ int s_elig;
+
+    const int tid = threadIdx.x;
+    if (tid == 0)
+        s_elig = 0;
+    for (int r = tid; r < p.Bp; r += kDcutThreads)
+        depth_s[r] = 0;
+    __syncthreads();
+
+    // 1. prefix products (fp32, left to right) -> keys; validate inputs
+    int bad = 0, elig = 0;
+    for (int r = tid; r < p.Bp; r += kDcutThreads) {
+        int km = r < p.B ? __ldg(p.kmax + r) : 0;
+        if (km < 0 || km > p.Kmax) {
+            bad = 1;
+            km = 0;
+        }
+        float P = 1.f;
+        for (int d = 1; d <= p.Kp; ++d) {
+            const uint64_t lo = (uint32_t)(r * p.Kp + (d - 1));
+            uint64_t key;
+            if (d <= km) {
+                float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
+                if (!(c >= 0.f && c <= 1.f)) {
+                    bad = 1;
+                    c = 0.f;
+                }
+                P = __fadd_rn(__fmul_rn(P, c), 0.f);  // + 0 turns -0 into +0
+                key = ((uint64_t)(0x3F800000u - __float_as_uint(P)) << 32) | lo;
+                elig += P >= p.min_gain;
+            } else {
+                key = (0xFFFFFFFFull << 32) | lo;  // not a candidate: sorts last
+            }
+            ka[r * p.Kp + (d - 1)] = key;
+        }
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (tid == 0)
+            set_status(p.status, ST_INVALID);
+        for (int r = tid; r < p.B; r += kDcutThreads) {
+            p.out_depth[r] = -1;
+            if (p.out_expected)
+                p.out_expected[r] = __int_as_float(0x7fc00000);
+        }
+        for (int r = tid; r <= p.B; r += kDcutThreads)
+            p.out_cu[r] = -1;
+        return;
+    }
+    if (elig)
+        atomicAdd(&s_elig, elig);
+
+    // 2. merge sorted runs of length L pairwise until one run remains
+    uint64_t *src = ka, *dst = kb;
+    for (int L = p.Kp; L < Np; L <<= 1) {
+        for (int e = tid; e < Np; e += kDcutThreads) {
+            const int run = e / L;
+            const int pos = e - run * L;
+            const uint64_t key = src[e];
+            const uint64_t *other = src + (size_t)((run ^ 1) * L);
+            int lo = 0, hi = L;
+            while (lo < hi) {
+                const int mid = (lo + hi) >> 1;
+                if (other[mid] < key)
+                    lo = mid + 1;
+                else
+                    hi = mid;
+            }
+            dst[(run & ~1) * L + pos + lo] = key;
+        }
+        __syncthreads();
+        uint64_t *t = src;
+        src = dst;
+        dst = t;
+    }
+
+    // 3. keep the first min(budget, eligible) keys; count them per request
+    const int keep = min(p.budget, s_elig);
+    for (int t = tid; t < keep; t += kDcutThreads) {
+        const uint32_t lo = (uint32_t)src[t];
+        atomicAdd(&depth_s[lo / (uint32_t)p.Kp], 1);
+    }
+    __syncthreads();
+
+    // 4. offsets (exclusive scan), depths, expected accepted drafts
+    const int per = (p.B + kDcutThreads - 1) / kDcutThreads;
+    const int r0 = min(p.B, tid * per), r1 = min(p.B, r0 + per);
+    int seg = 0;
+    for (int r = r0; r < r1; ++r)
+        seg += depth_s[r];
+    int total = 0;
+    int off = block_excl_scan_int(seg, warp_tot, total);
+    for (int r = r0; r < r1; ++r) {
+        p.out_cu[r] = off;
+        off += depth_s[r];
+        p.out_depth[r] = depth_s[r];
+        if (p.out_expected) {
+            float P = 1.f;
+            double e = 0.0;
+            for (int d = 1; d <= depth_s[r]; ++d) {
+                P = __fadd_rn(__fmul_rn(P, __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1))), 0.f);
+                e += (double)P;
+            }
+            p.out_expected[r] = (float)e;
+        }
+    }
+    if (tid == 0)
+        p.out_cu[p.B] = total;
+}
+
+static int next_pow2(int x)
+{
+    int p = 1;
+    while (p < x)
+        p <<= 1;
+    return p;
+}
+
+cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
+{
+    static cudaError_t once = cudaFuncSetAttribute(
+        dcut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        2 * 8 * kDcutMaxCand + 4 * kMaxBatch);
+    if (once != cudaSuccess)
+        return once;
+    DcutParams p{};
+    p.conf = a.conf;
+    p.kmax = a.kmax;
+    p.B = a.B;
+    p.Kmax = a.Kmax;
+    p.Kp = next_pow2(a.Kmax > 0 ? a.Kmax : 1);
+    p.Bp = next_pow2(a.B > 0 ? a.B : 1);
+    p.budget = a.budget;
+    p.min_gain = a.min_gain;
+    p.out_depth = a.out_depth;
+    p.out_cu = a.out_cu;
+    p.out_expected = a.out_expected;
+    const WsLayout L = ws_layout(0, 0, 0);
+    p.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
+    const size_t smem = 2 * sizeof(uint64_t) * (size_t)p.Bp * p.Kp + 4 * (size_t)p.Bp;
+    tr.begin(s);
+    dcut_kernel<<<1, kDcutThreads, smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+}  // namespace sv

@@ -1,0 +1,57 @@
+// launch.h - host-side interface between the C-ABI layer (api.cu) and the
+// kernel launchers (verify.cu, dcut.cu).  Plain structs, no torch types.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+// Kernel-boundary hook: records the caller's trace events and counts launches.
+struct Tracer {
+    cudaEvent_t const *events = nullptr;
+    int n = 0;
+    int next = 0;
+    void begin(cudaStream_t s);
+    void after_kernel(cudaStream_t s);
+};
+
+struct VerifyArgs {
+    const void *target;
+    const void *draft;  // nullptr for greedy
+    int dtype;          // 0 = f32, 1 = bf16
+    const int32_t *tokens;
+    const int32_t *cu;
+    int B;
+    int V;
+    int64_t max_rows;
+    int draft_stride;
+    double temperature;  // 0 = greedy
+    const float *u_accept;
+    const float *u_final;
+    int32_t *out_tokens;
+    int32_t *out_len;
+    float *out_p;
+    float *out_q;
+    void *ws;
+};
+
+// Enqueue the verification kernels (1 launch greedy, 2 launches sampling).
+cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t stream, Tracer &tr);
+
+struct DcutArgs {
+    const float *conf;
+    const int32_t *kmax;
+    int B;
+    int Kmax;
+    int budget;
+    float min_gain;
+    int32_t *out_depth;
+    int32_t *out_cu;
+    float *out_expected;
+    void *ws;
+};
+
+cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t stream, Tracer &tr);
+
+}  // namespace sv

@@ -1,0 +1,198 @@
+/*
+ * specverify.h - C ABI of the B300 (sm_103a) batched draft-verification
+ * library: lossless rejection-sampling verification of drafted tokens, greedy
+ * verification at T = 0, and D-cut's batch-level allocation of verification
+ * depth.
+ *
+ * What the calls compute
+ * ----------------------
+ * Speculative decoding has a cheap drafter propose several tokens; the target
+ * model scores the whole drafted block in one forward pass and rejection
+ * sampling keeps the accepted prefix plus one extra token ("Tencent Hunyuan
+ * Turns Speculative Decoding Into a Full Open-Source Stack", section "What
+ * problem does it solve").  The accepted length is the number of drafted
+ * tokens approved before the first mismatch ("Tencent rilascia AngelSpec in
+ * open source ...", section "Come AngelSpec rende DFly piu selettivo"), and
+ * the procedure is lossless: its output law is the target's ("Tencent ...
+ * AngelSpec ...", section "Qu'est-ce que le speculative decoding").  The pages
+ * do not write the accept/reject formulas; these calls use the standard ones
+ * (Leviathan, Kalman & Matias 2023, "Fast Inference from Transformers via
+ * Speculative Decoding", section "Speculative Sampling").
+ *
+ * Layout (all calls)
+ * ------------------
+ * B requests.  Request i verifies K_i drafted tokens (0 <= K_i <= 32).
+ * cu_draft[B+1] (device, int32): cu_draft[0] = 0, cu_draft[i+1] = cu_draft[i] + K_i.
+ * Target row j of request i (j = 0..K_i; j = K_i is the bonus row) is row
+ *   cu_draft[i] + i + j of target_logits[rows][V] (row-major, stride V).
+ * Draft index of (i, j), j < K_i:
+ *   draft_stride == 0 (packed): cu_draft[i] + j
+ *   draft_stride  > 0 (padded): i * draft_stride + j   (requires K_i <= draft_stride)
+ * draft_tokens, draft_logits rows, u_accept, out_p and out_q use the draft index.
+ * out_tokens uses the target-row index: out_tokens[cu_draft[i] + i + j] for j = 0..K_i
+ * holds the accepted drafts (j < a_i), the final token (j = a_i) and -1 after it.
+ *
+ * Buffers
+ * -------
+ * Every pointer is caller-owned DEVICE memory; the library allocates nothing.
+ * max_target_rows is a host-known upper bound on cu_draft[B] + B (it sizes
+ * the grids, so cu_draft may be produced on the device, e.g. by
+ * dcut_allocate, with no host round trip).  target_logits must be readable
+ * for max_target_rows rows and out_tokens writable for max_target_rows
+ * entries; a packed draft side must be readable for max_target_rows - B rows,
+ * a padded one for B * draft_stride rows.  Rows past cu_draft[B] + B may be
+ * read (their values are ignored) and are never written.
+ * Logits are float32 (SPEC_F32) or bfloat16 (SPEC_BF16); -inf marks a
+ * masked vocabulary entry; NaN and +inf are errors.  Pointers should be
+ * 16-byte aligned and V * element size a multiple of 16 for the fast TMA
+ * path; other shapes run a slower plain-load path with the same results.
+ *
+ * Streams and errors
+ * ------------------
+ * Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ * stream) and returns without synchronising.  Argument errors are returned
+ * before anything is enqueued.  Data-dependent errors (NaN/+inf logits, a
+ * row with every entry masked, a drafted token outside [0, V), malformed
+ * cu_draft, a bounded wait that expired) set a status word inside the
+ * workspace and poison the affected outputs (tokens -1, accepted length
+ * -1); spec_get_device_status reads and clears that word.
+ *
+ * Workspace
+ * ---------
+ * spec_workspace_size(B, max_target_rows, V) bytes of device memory,
+ * zero-filled once before first use (spec_workspace_init does this); every
+ * call leaves it ready for the next.  One workspace serves one stream at a
+ * time: calls on different streams need different workspaces.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = -1, /* bad argument, or (device) malformed offsets / token id */
+    SPEC_ERR_WORKSPACE = -2,   /* workspace missing or smaller than spec_workspace_size */
+    SPEC_ERR_CUDA = -3,        /* a CUDA runtime call or kernel launch failed */
+    SPEC_ERR_NONFINITE = -4,   /* (device) NaN or +inf logit, or a fully masked row */
+    SPEC_ERR_TIMEOUT = -5      /* (device) a bounded wait for a copy expired */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Largest K_i, B and B*Kmax the calls accept. */
+#define SPEC_MAX_DRAFT 32
+#define SPEC_MAX_BATCH 4096
+#define SPEC_DCUT_MAX_CANDIDATES 8192
+
+/*
+ * Bytes of workspace needed by spec_verify_greedy / spec_verify_sample for up
+ * to B requests, max_target_rows target rows and vocabulary V (either dtype),
+ * and by dcut_allocate (any B, V = 0).  Returns 0 for invalid sizes.
+ */
+size_t spec_workspace_size(int32_t B, int64_t max_target_rows, int32_t V);
+
+/* Zero-fill a workspace (enqueued on stream).  Needed once before first use. */
+int spec_workspace_init(void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Greedy verification (T = 0).  g_j = lowest index of the maximum of target
+ * row j; draft j is accepted iff draft_tokens[j] == g_j; a_i = first mismatch
+ * (K_i if none); the final token is g_{a_i} (the bonus row's argmax when every
+ * draft is accepted).  Draft logits are not read.  One kernel launch.
+ * Pages: greedy acceptance rates "at T = 0" ("Tencent ... AngelSpec ...",
+ * bullet list); ties to the lowest index is this library's reading.
+ *
+ *   target_logits  [max_target_rows][V]  f32 or bf16 (dtype)
+ *   draft_tokens   draft index -> int32 token id
+ *   out_tokens     int32 [max_target_rows]
+ *   out_accept_len int32 [B]: a_i
+ */
+int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draft_tokens,
+                       const int32_t *cu_draft, int32_t B, int32_t V, int64_t max_target_rows,
+                       int32_t draft_stride, int32_t *out_tokens, int32_t *out_accept_len,
+                       void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Sampling verification (T > 0).  With p_j = softmax(target row j / T) and
+ * q_j = softmax(draft row j / T):
+ *   accept draft j iff u_accept[j] < p_j(x_j) / q_j(x_j)  (q_j(x_j) = 0: iff p_j(x_j) > 0)
+ *   a_i = first rejected position (K_i if none)
+ *   final weights w = max(0, p_a - q_a) after a rejection (w = p_a if that is
+ *   all zero), w = p_{K_i} (bonus row) when every draft is accepted;
+ *   final token = smallest v with sum_{v' <= v} w(v') > u_final[i] * sum(w).
+ * out_p / out_q (draft index, may be NULL) receive p_j(x_j) and q_j(x_j) for
+ * every j < K_i.  temperature == 0 runs spec_verify_greedy (out_p/out_q are
+ * then left untouched).  Two kernel launches.
+ *
+ *   draft_logits  [draft rows][V], same dtype as target_logits
+ *   u_accept      float [draft index] in [0,1)
+ *   u_final       float [B] in [0,1)
+ */
+int spec_verify_sample(const void *target_logits, const void *draft_logits, int dtype,
+                       const int32_t *draft_tokens, const int32_t *cu_draft, int32_t B,
+                       int32_t V, int64_t max_target_rows, int32_t draft_stride,
+                       float temperature, const float *u_accept, const float *u_final,
+                       int32_t *out_tokens, int32_t *out_accept_len, float *out_p,
+                       float *out_q, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * D-cut: batch-level allocation of verification depth under a total
+ * verify-token budget.  The pages describe D-cut as treating verification
+ * capacity as a batch-level shared resource, weighing the expected value of
+ * keeping more positions against their cost and sending depth to
+ * high-confidence prefixes ("Tencent rilascia AngelSpec in open source ...",
+ * "Come AngelSpec rende DFly piu selettivo"; "Tencent Hunyuan Turns
+ * Speculative Decoding ...", "What problem does it solve", inference layer).
+ *
+ * conf[i*Kmax + j] in [0,1] (j < kmax[i]) is request i's confidence in its
+ * drafted token j.  P_{i,d} = conf[i][0] * ... * conf[i][d-1] (fp32, left to
+ * right).  All (i, d) are ranked by P descending, ties by request then depth
+ * ascending; the first min(budget, #{P >= min_gain}) are kept.  out_depth[i]
+ * = number kept for request i (always a prefix), out_cu = exclusive prefix
+ * sum of out_depth (feeds cu_draft of the verify call; target rows needed =
+ * budget + B at most), out_expected_len[i] = sum_{d <= depth_i} P_{i,d}
+ * (may be NULL).  The bonus row of every request is always verified and is
+ * not counted against the budget.  Invalid confidences set
+ * SPEC_ERR_INVALID_ARG on the device and write -1 depths and offsets.
+ * One kernel launch (one CTA).  Requires B * Kmax <= SPEC_DCUT_MAX_CANDIDATES.
+ */
+int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kmax,
+                  int32_t budget, float min_gain, int32_t *out_depth, int32_t *out_cu,
+                  float *out_expected_len, void *workspace, size_t ws_bytes,
+                  spec_stream_t stream);
+
+/*
+ * Synchronise `stream`, then read and clear the workspace status word.
+ * Returns SPEC_OK or the device-side error (SPEC_ERR_TIMEOUT before
+ * SPEC_ERR_INVALID_ARG before SPEC_ERR_NONFINITE when several are set).
+ */
+int spec_get_device_status(void *workspace, spec_stream_t stream);
+
+/* Static description of a status code. */
+const char *spec_status_string(int status);
+
+/*
+ * Optional timing hook for benchmarks.  After spec_set_trace(events, n) the
+ * calling thread's subsequent calls record events[0] (a cudaEvent_t) on the
+ * stream before their first kernel and events[k] after their k-th kernel
+ * (k < n).  spec_set_trace(NULL, 0) turns it off.  Thread-local.
+ */
+int spec_set_trace(void *const *events, int n_events);
+
+/* Number of kernels the calling thread has launched through this library. */
+int64_t spec_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -293,7 +293,7 @@ int oracle_verify_greedy(const void *target, int dtype, const int32_t *tokens,
                 err = ORC_ERR_INVALID_ARG;
         }
         /* every row of the request is read: g_0..g_K first, then the match */
-        int32_t g[ORC_MAX_DRAFT + 1];
+        int32_t g[ORC_MAX_DRAFT + 1] = {0};
         for (int32_t j = 0; j <= k && err == ORC_OK; ++j)
             err = oracle_argmax_row(target, dtype, target_row(cu, i, j), V, &g[j]);
         int32_t a = k, y = -1;

@@ -14,6 +14,12 @@ if TESTS not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (B300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running check")
+    # build (or refresh) the oracle and the CUDA library before collection;
+    # both are no-ops when the built files are newer than their sources
+    import oracle
+    from draft_verification_02_b300 import build as cuda_build
+    oracle.build()
+    cuda_build.build()
 
 
 @pytest.fixture(scope="session")
