@@ -48,18 +48,29 @@ int check_verify_sizes(int32_t B, int32_t V, int64_t max_target_rows, int32_t dr
 
 namespace sv {
 
+// Inside stream capture a plain record only orders streams; the external
+// flag makes it a timestamp node of the graph.
+static void record_event(cudaEvent_t e, cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(e, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(e, s);
+}
+
 void Tracer::begin(cudaStream_t s)
 {
     next = 0;
     if (next < n)
-        cudaEventRecord(events[next++], s);
+        record_event(events[next++], s);
 }
 
 void Tracer::after_kernel(cudaStream_t s)
 {
     ++g_launches;
     if (next < n)
-        cudaEventRecord(events[next++], s);
+        record_event(events[next++], s);
 }
 
 }  // namespace sv

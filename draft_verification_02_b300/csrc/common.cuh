@@ -17,10 +17,16 @@ constexpr int kMaxBatch = 4096;
 constexpr int kDcutMaxCand = 8192;
 
 #ifndef SV_CHUNK_BYTES
-#define SV_CHUNK_BYTES 32768  // bytes of one row chunk staged in shared memory
+#define SV_CHUNK_BYTES 32768  // bytes of one final-draw chunk staged in shared memory
 #endif
 constexpr int kChunkBytes = SV_CHUNK_BYTES;
-constexpr int kMaxChunks = 1024;  // chunks per row (bounds V)
+constexpr int kDrawChunkBytes = SV_CHUNK_BYTES;
+constexpr int kMaxChunks = 1024;  // draw chunks per row (bounds V)
+#ifndef SV_PIECE_BYTES
+#define SV_PIECE_BYTES 4096  // largest unit of the streaming kernel
+#endif
+constexpr int kPieceBytesMax = SV_PIECE_BYTES;
+constexpr int kMaxWorkers = 8192;  // warp workers of the streaming kernel
 
 // Device status bits (the workspace status word).
 enum : uint32_t { ST_INVALID = 1u, ST_NONFINITE = 2u, ST_TIMEOUT = 4u };
@@ -39,16 +45,6 @@ struct __align__(16) Partial {
     float m;
     int32_t idx;
     double s;
-};
-
-// Per-request result of the accept stage, consumed by the final-draw kernel.
-struct __align__(16) Handoff {
-    int32_t a;      // accepted length; -1 = request poisoned / nothing to draw
-    int32_t pad;
-    int64_t trow;   // target row of the final draw
-    int64_t drow;   // draft row of a rejection, -1 for the bonus draw
-    float m_t, m_d; // row maxima
-    double s_t, s_d;// row sums of exp((l - m) / T)
 };
 
 struct Chunking {
@@ -75,27 +71,26 @@ inline Chunking chunking(int V, int elem_bytes)
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace: status word (+ offsets-valid flag) | per-request ticket
+// counters | stream partials (one per (row, warp) segment: at most
+// rows + warps) | per-request draw-chunk sums.  Sized for the worst case over
+// both dtypes (fp32 has the most draw chunks).
 struct WsLayout {
-    size_t status, cnt1, cnt2, part1, hand, part2, total;
+    size_t status, cnt2, part1, part2, total;
 };
 
-// Sized for the worst case over both dtypes (fp32 has the most chunks).
 inline WsLayout ws_layout(int B, int64_t max_rows, int V)
 {
     WsLayout L{};
     const int nch = V > 0 ? chunking(V, 4).nchunks : 0;
-    const int64_t slots = max_rows > 0 ? 2 * max_rows - B : 0;
+    const int64_t rows = max_rows > 0 ? 2 * max_rows - B : 0;
     size_t off = 0;
     L.status = off;
     off += 256;
-    L.cnt1 = off;
-    off = align_up(off + (size_t)B * 4, 256);
     L.cnt2 = off;
     off = align_up(off + (size_t)B * 4, 256);
     L.part1 = off;
-    off = align_up(off + (size_t)(slots > 0 ? slots : 0) * nch * sizeof(Partial), 256);
-    L.hand = off;
-    off = align_up(off + (size_t)B * sizeof(Handoff), 256);
+    off = align_up(off + (size_t)(max_rows > 0 ? rows + kMaxWorkers : 0) * sizeof(Partial), 256);
     L.part2 = off;
     off = align_up(off + (size_t)B * nch * sizeof(double), 256);
     L.total = off;

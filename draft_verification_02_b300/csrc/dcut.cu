@@ -80,20 +80,28 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
     uint64_t *ka = reinterpret_cast<uint64_t *>(dsm);
     uint64_t *kb = ka + Np;
     int *depth_s = reinterpret_cast<int *>(kb + Np);
+    int *kmax_s = depth_s + p.Bp;
+    float *conf_s = reinterpret_cast<float *>(kmax_s + p.Bp);
     __shared__ int warp_tot[33];
     __shared__ int s_elig;
 
     const int tid = threadIdx.x;
     if (tid == 0)
         s_elig = 0;
-    for (int r = tid; r < p.Bp; r += kDcutThreads)
+    // stage the inputs with coalesced loads (one round trip), then work from
+    // shared memory
+    for (int r = tid; r < p.Bp; r += kDcutThreads) {
         depth_s[r] = 0;
+        kmax_s[r] = r < p.B ? __ldg(p.kmax + r) : 0;
+    }
+    for (int k = tid; k < p.B * p.Kmax; k += kDcutThreads)
+        conf_s[k] = __ldg(p.conf + k);
     __syncthreads();
 
     // 1. prefix products (fp32, left to right) -> keys; validate inputs
     int bad = 0, elig = 0;
     for (int r = tid; r < p.Bp; r += kDcutThreads) {
-        int km = r < p.B ? __ldg(p.kmax + r) : 0;
+        int km = kmax_s[r];
         if (km < 0 || km > p.Kmax) {
             bad = 1;
             km = 0;
@@ -103,7 +111,7 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
             const uint64_t lo = (uint32_t)(r * p.Kp + (d - 1));
             uint64_t key;
             if (d <= km) {
-                float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
+                float c = conf_s[r * p.Kmax + (d - 1)];
                 if (!(c >= 0.f && c <= 1.f)) {
                     bad = 1;
                     c = 0.f;
@@ -181,7 +189,7 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
             float P = 1.f;
             double e = 0.0;
             for (int d = 1; d <= depth_s[r]; ++d) {
-                P = __fadd_rn(__fmul_rn(P, __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1))), 0.f);
+                P = __fadd_rn(__fmul_rn(P, conf_s[r * p.Kmax + (d - 1)]), 0.f);
                 e += (double)P;
             }
             p.out_expected[r] = (float)e;
@@ -203,7 +211,7 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 {
     static cudaError_t once = cudaFuncSetAttribute(
         dcut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        2 * 8 * kDcutMaxCand + 4 * kMaxBatch);
+        2 * 8 * kDcutMaxCand + 8 * kMaxBatch + 4 * kDcutMaxCand);
     if (once != cudaSuccess)
         return once;
     DcutParams p{};
@@ -220,7 +228,8 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
     p.out_expected = a.out_expected;
     const WsLayout L = ws_layout(0, 0, 0);
     p.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
-    const size_t smem = 2 * sizeof(uint64_t) * (size_t)p.Bp * p.Kp + 4 * (size_t)p.Bp;
+    const size_t smem = 2 * sizeof(uint64_t) * (size_t)p.Bp * p.Kp + 8 * (size_t)p.Bp +
+                        4 * (size_t)p.B * p.Kmax;
     tr.begin(s);
     dcut_kernel<<<1, kDcutThreads, smem, s>>>(p);
     cudaError_t e = cudaGetLastError();

@@ -16,21 +16,25 @@
 // residual formulas are the standard ones (Leviathan, Kalman & Matias 2023,
 // "Speculative Sampling").
 //
-// Kernels
-//   rows_kernel  (one CTA per (row, chunk) of every target row and, at T > 0,
-//                every draft row): streams one chunk of <= 32 KB into shared
-//                memory with a 1-D TMA bulk copy (cp.async.bulk + mbarrier),
-//                reduces it (argmax at T = 0; max and sum of exp at T > 0) and
-//                writes a partial.  The CTA that completes a request's last
-//                chunk (atomic ticket, no spinning) merges the request's
-//                partials in a fixed order and runs the accept test and the
-//                first-rejection scan (one warp ballot).  At T = 0 it also
-//                emits the tokens; that is the whole greedy call.
-//   final_kernel (T > 0; one CTA per (request, chunk)): sums the final-draw
-//                weights of its chunk; the request's last CTA picks the chunk
-//                holding u * S and runs a block scan inside it to find the
-//                token.
+// Kernel 1, stream_kernel: the HBM-bound pass.  Every row that must be read
+// (all target rows; at T > 0 all draft rows) is cut into units of Q elements;
+// the units, in row order, are split into P contiguous, equal ranges, one per
+// warp of a persistent grid (a few CTAs per SM).  Each warp keeps a ring of
+// kRing units in flight with 1-D TMA bulk copies (cp.async.bulk into shared
+// memory, mbarrier completion, bounded waits) and reduces each unit from
+// registers: T > 0 takes the maximum with packed bf16x2 max, then sums
+// exp2(x*c - m*c) with one FFMA + ex2.approx + FADD per element (the rounding
+// of m*c is corrected exactly once per unit); T = 0 keeps the lowest index of
+// the maximum.  No fp64 on this path (B300's fp64 rate is a small fraction of
+// its fp32 rate).  Every (row, warp) segment leaves one partial.
+// Kernel 2, finish_kernel: one CTA per (request, draw chunk), launched as a
+// programmatic dependent of kernel 1 so its launch overlaps kernel 1's tail.
+// Each CTA merges its request's partials in a fixed order (identical in every
+// CTA of the request), runs the accept test and the first-rejection ballot,
+// then sums the final-draw weights of its chunk; the request's last CTA
+// (atomic ticket) picks the chunk holding u*S and scans inside it.
 // Every merge runs in a fixed order, so repeated calls give identical bits.
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <cmath>
@@ -40,7 +44,37 @@
 
 namespace sv {
 
-struct VerifyParams {
+// ---------------------------------------------------------------------------
+// parameters
+// ---------------------------------------------------------------------------
+
+struct Geometry {  // the unit split of kernel 1, needed by kernel 2 to find partials
+    int64_t max_rows;  // target rows (host bound)
+    int64_t U;         // units
+    int cpr;           // units per row
+    int Q;             // elements per unit (the last unit of a row may be shorter)
+    int P;             // warp workers
+};
+
+struct StreamParams {
+    const void *target;
+    const void *draft;
+    const int32_t *cu;
+    int32_t *out_tokens;
+    int32_t *out_len;
+    int B, V;
+    int64_t draft_slots;  // draft rows read (packed index space); 0 at T = 0
+    int draft_stride;
+    Geometry g;
+    int tma;
+    int piece_smem;  // bytes per ring slot (multiple of 128)
+    float c;         // log2(e) / T
+    uint32_t *status;
+    uint32_t *cu_flag;
+    Partial *part;
+};
+
+struct FinishParams {
     const void *target;
     const void *draft;
     const int32_t *tokens;
@@ -52,31 +86,632 @@ struct VerifyParams {
     float *out_p;
     float *out_q;
     int B, V;
-    int64_t max_rows;
-    int64_t draft_rows;  // rows the draft side may index (packed or padded)
+    int64_t draft_rows;  // rows the draft side may index
     int draft_stride;
-    int nchunks, chunk_elems;
-    int tma;         // rows start on 16-byte boundaries: use TMA bulk copies
-    int chunk_smem;  // bytes reserved per staged chunk (multiple of 128)
-    float c_hi, c_lo;  // log2(e) / T as an unevaluated pair of floats
-    double inv_T;
-    uint32_t *status, *cnt1, *cnt2;
-    Partial *part1;
-    Handoff *hand;
+    Geometry g;
+    int NC;          // draw chunks per row
+    int nce;         // elements per draw chunk
+    int chunk_smem;  // bytes per staged draw chunk (multiple of 128)
+    int tma;
+    float c;
+    uint32_t *status;
+    const uint32_t *cu_flag;
+    uint32_t *cnt2;
+    const Partial *part;
     double *part2;
 };
 
-__device__ __forceinline__ int64_t draft_index(const VerifyParams &p, const int32_t *cu, int i,
-                                               int j)
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_trigger()
 {
-    return p.draft_stride > 0 ? (int64_t)i * p.draft_stride + j : (int64_t)cu[i] + j;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// exp2 argument for (x - m) / T: d * log2(e)/T with the constant split in two
-// floats, so the product carries only the final rounding.
-__device__ __forceinline__ float exp_arg(float d, float c_hi, float c_lo)
+__device__ __forceinline__ void pdl_wait()
 {
-    return fmaf(d, c_hi, d * c_lo);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// 2^x on the SFU (PTX ex2.approx.ftz.f32); results below 2^-126 flush to 0.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Owner warp of unit u when warp w owns units [w*U/P, (w+1)*U/P).
+__device__ __forceinline__ int owner_of(int64_t u, const Geometry &g)
+{
+    return (int)(((u + 1) * (int64_t)g.P - 1) / g.U);
+}
+
+// The unit sums use exp2(x*c - fl(m*c)) = exp2((x - m)*c) * 2^-(fl(m*c) - m*c);
+// this returns the factor 2^(fl(m*c) - m*c) that undoes the rounding.  The
+// rounding error fl(m*c) - m*c is exact as -fma(m, c, -fl(m*c)) and below
+// 2^-17 in magnitude, so 1 + delta*ln2 is the factor to fp32 precision.
+__device__ __forceinline__ float mc_correction(float m, float mc, float c)
+{
+    const float delta = -fmaf(m, c, -mc);
+    return fmaf(delta, 0.69314718f, 1.0f);
+}
+
+// 2^x for x <= 0 given in fp64: split x = n + f exactly (n integer, f in
+// [0,1)), take 2^f with CUDA's exp2f (2 ulp) and scale by 2^n.  A handful of
+// fp64 operations instead of a full fp64 exp2.
+__device__ __forceinline__ float exp2_split(double x)
+{
+    if (x < -200.0)
+        return 0.f;
+    const double n = floor(x);
+    return ldexpf(exp2f((float)(x - n)), (int)n);
+}
+
+__device__ __forceinline__ int64_t draft_index(int draft_stride, const int32_t *cu, int i, int j)
+{
+    return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)__ldg(cu + i) + j;
+}
+
+__device__ __forceinline__ double qnan_d() { return __longlong_as_double(0x7ff8000000000000ll); }
+
+// ---------------------------------------------------------------------------
+// kernel 1: stream the rows
+// ---------------------------------------------------------------------------
+
+#ifndef SV_RING
+#define SV_RING 3
+#endif
+#ifndef SV_STREAM_CTAS_PER_SM
+#define SV_STREAM_CTAS_PER_SM 2
+#endif
+constexpr int kRing = SV_RING;
+constexpr int kStreamWarps = 8;
+constexpr int kStreamThreads = kStreamWarps * 32;
+
+// Per-lane running state of one row segment.  The running sum is fp32 with
+// Kahan compensation: one term per unit.
+struct LaneAcc {
+    float m;     // running max (T > 0) / best value (T = 0)
+    float s;     // running sum of exp2((x - m) c)  (T > 0)
+    float comp;  // Kahan compensation of s
+    int idx;     // best index (T = 0)
+    int nan;     // a NaN was seen (T = 0)
+};
+
+// Fold a unit's maximum pm into the running (m, s); false when nothing more
+// is to be summed (NaN, all masked, or +inf - the merge flags those rows).
+__device__ __forceinline__ bool fold_max(LaneAcc &a, float pm, float c)
+{
+    const float mn = max_nan(a.m, pm);
+    if (mn != mn) {
+        a.m = mn;
+        a.s = __int_as_float(0x7fc00000);
+        return false;
+    }
+    if (mn > a.m) {
+        if (a.m != -INFINITY) {
+            const float f = exp2f((a.m - mn) * c);
+            a.s *= f;
+            a.comp *= f;
+        }
+        a.m = mn;
+    }
+    return a.m != -INFINITY && a.m != INFINITY && a.s == a.s;
+}
+
+// Add one unit's sum (taken relative to fl(m c)) to the running sum.
+__device__ __forceinline__ void add_unit(LaneAcc &a, float unit_sum, float mc, float c)
+{
+    const float y = unit_sum * mc_correction(a.m, mc, c) - a.comp;
+    const float t = a.s + y;
+    a.comp = (t - a.s) - y;
+    a.s = t;
+}
+
+// One unit of bf16 data at T > 0 from shared memory (lane-strided 16-byte
+// vectors held in registers between the max and the sum); a tail that is not
+// a whole vector (plain-load path only) is handled element-wise.
+template <int MAXV>
+__device__ __forceinline__ void unit_softmax_bf16(const uint16_t *buf, int len, float c,
+                                                  LaneAcc &a)
+{
+    const int lane = threadIdx.x & 31;
+    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
+    const int nvec = len >> 3;
+    uint4 r[MAXV];
+    uint32_t hm = 0xff80ff80u;  // (-inf, -inf)
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            r[t] = vb[v];
+            hm = max_nan_bf16x2(hm, r[t].x);
+            hm = max_nan_bf16x2(hm, r[t].y);
+            hm = max_nan_bf16x2(hm, r[t].z);
+            hm = max_nan_bf16x2(hm, r[t].w);
+        }
+    }
+    float pm = max_nan(bf16_lo(hm), bf16_hi(hm));
+    for (int k = nvec * 8 + lane; k < len; k += 32)
+        pm = max_nan(pm, bf16_lo((uint32_t)buf[k]));
+    if (!fold_max(a, pm, c))
+        return;
+    const float mc = a.m * c;
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
+            float e[8];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                e[2 * h] = ex2_approx(fmaf(bf16_lo(w4[h]), c, -mc));
+                e[2 * h + 1] = ex2_approx(fmaf(bf16_hi(w4[h]), c, -mc));
+            }
+            acc += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+        }
+    }
+    for (int k = nvec * 8 + lane; k < len; k += 32)
+        acc += ex2_approx(fmaf(bf16_lo((uint32_t)buf[k]), c, -mc));
+    add_unit(a, acc, mc, c);
+}
+
+template <int MAXV>
+__device__ __forceinline__ void unit_softmax_f32(const float *buf, int len, float c, LaneAcc &a)
+{
+    const int lane = threadIdx.x & 31;
+    const float4 *vb = reinterpret_cast<const float4 *>(buf);
+    const int nvec = len >> 2;
+    float4 r[MAXV];
+    float pm = -INFINITY;
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            r[t] = vb[v];
+            pm = max_nan(pm, max_nan(max_nan(r[t].x, r[t].y), max_nan(r[t].z, r[t].w)));
+        }
+    }
+    for (int k = nvec * 4 + lane; k < len; k += 32)
+        pm = max_nan(pm, buf[k]);
+    if (!fold_max(a, pm, c))
+        return;
+    const float mc = a.m * c;
+    float acc = 0.f;
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            const float e0 = ex2_approx(fmaf(r[t].x, c, -mc));
+            const float e1 = ex2_approx(fmaf(r[t].y, c, -mc));
+            const float e2 = ex2_approx(fmaf(r[t].z, c, -mc));
+            const float e3 = ex2_approx(fmaf(r[t].w, c, -mc));
+            acc += (e0 + e1) + (e2 + e3);
+        }
+    }
+    for (int k = nvec * 4 + lane; k < len; k += 32)
+        acc += ex2_approx(fmaf(buf[k], c, -mc));
+    add_unit(a, acc, mc, c);
+}
+
+// T = 0: lowest index of the maximum.  Each lane visits its elements in
+// increasing index order, so a strict > keeps the lowest index.
+template <int MAXV>
+__device__ __forceinline__ void unit_argmax_bf16(const uint16_t *buf, int len, int col0,
+                                                 LaneAcc &a)
+{
+    const int lane = threadIdx.x & 31;
+    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
+    const int nvec = len >> 3;
+    uint4 r[MAXV];
+    uint32_t hm = 0xff80ff80u;
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            r[t] = vb[v];
+            hm = max_nan_bf16x2(hm, r[t].x);
+            hm = max_nan_bf16x2(hm, r[t].y);
+            hm = max_nan_bf16x2(hm, r[t].z);
+            hm = max_nan_bf16x2(hm, r[t].w);
+        }
+    }
+    const float pm = max_nan(bf16_lo(hm), bf16_hi(hm));
+    if (pm != pm) {
+        a.nan = 1;
+    } else if (pm > a.m) {  // locate the first element equal to the new maximum
+        int found = INT_MAX;
+#pragma unroll
+        for (int t = 0; t < MAXV; ++t) {
+            const int v = lane + 32 * t;
+            if (v < nvec && found == INT_MAX) {
+                const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    if (found == INT_MAX && bf16_lo(w4[h]) == pm)
+                        found = v * 8 + 2 * h;
+                    if (found == INT_MAX && bf16_hi(w4[h]) == pm)
+                        found = v * 8 + 2 * h + 1;
+                }
+            }
+        }
+        a.m = pm;
+        a.idx = col0 + found;
+    }
+    for (int k = nvec * 8 + lane; k < len; k += 32) {  // tail (plain path), in order
+        const float x = bf16_lo((uint32_t)buf[k]);
+        if (x != x)
+            a.nan = 1;
+        else if (x > a.m) {
+            a.m = x;
+            a.idx = col0 + k;
+        }
+    }
+}
+
+template <int MAXV>
+__device__ __forceinline__ void unit_argmax_f32(const float *buf, int len, int col0, LaneAcc &a)
+{
+    const int lane = threadIdx.x & 31;
+    const float4 *vb = reinterpret_cast<const float4 *>(buf);
+    const int nvec = len >> 2;
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        if (v < nvec) {
+            const float4 q = vb[v];
+            const float x4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                if (x4[h] != x4[h])
+                    a.nan = 1;
+                else if (x4[h] > a.m) {
+                    a.m = x4[h];
+                    a.idx = col0 + v * 4 + h;
+                }
+            }
+        }
+    }
+    for (int k = nvec * 4 + lane; k < len; k += 32) {
+        const float x = buf[k];
+        if (x != x)
+            a.nan = 1;
+        else if (x > a.m) {
+            a.m = x;
+            a.idx = col0 + k;
+        }
+    }
+}
+
+// Reduce the lanes' state of a finished row segment, store its partial and
+// reset the state.
+template <bool GREEDY>
+__device__ __forceinline__ void store_partial(LaneAcc &a, float c, Partial *slot)
+{
+    const int lane = threadIdx.x & 31;
+    Partial out;
+    if (GREEDY) {
+        float best = a.m;
+        int bidx = a.idx;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+            if (ob > best || (ob == best && oi < bidx)) {
+                best = ob;
+                bidx = oi;
+            }
+        }
+        const int nan = __any_sync(0xffffffffu, a.nan);
+        out.m = best;
+        out.idx = nan ? -2 : (bidx == INT_MAX ? -1 : bidx);
+        out.s = 0.0;
+    } else {
+        const float m = warp_max_nan(a.m);
+        double s = 0.0;
+        if (m == m && m != -INFINITY && m != INFINITY) {
+            if (a.s != 0.f)
+                s = (double)(a.s - a.comp) * (double)exp2f((a.m - m) * c);
+        } else if (m != -INFINITY) {
+            s = qnan_d();
+        }
+        s = warp_sum_d(s);
+        out.m = m;
+        out.idx = 0;
+        out.s = s;
+    }
+    if (lane == 0)
+        *slot = out;
+    a.m = -INFINITY;
+    a.s = 0.f;
+    a.comp = 0.f;
+    a.idx = INT_MAX;
+    a.nan = 0;
+}
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
+    stream_kernel(const StreamParams p)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    __shared__ __align__(8) uint64_t bars[kStreamWarps][kRing];
+    const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+    const int w = blockIdx.x * kStreamWarps + wib;
+    const Geometry g = p.g;
+    const int B = p.B, V = p.V;
+    unsigned char *ring = dsm + (size_t)wib * kRing * p.piece_smem;
+    int32_t *cu_s = reinterpret_cast<int32_t *>(dsm + (size_t)kStreamWarps * kRing * p.piece_smem);
+    constexpr int MAXV = (kPieceBytesMax / 16 + 31) / 32;  // 16-byte vectors per lane per unit
+
+    pdl_trigger();  // the finish kernel may launch now; it waits for this grid to complete
+    if (lane == 0) {
+        for (int k = 0; k < kRing; ++k)
+            mbar_init(&bars[wib][k], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const int64_t u0 = w < g.P ? (int64_t)w * g.U / g.P : 0;
+    const int64_t u1 = w < g.P ? (int64_t)(w + 1) * g.U / g.P : 0;
+    const T *tbase = reinterpret_cast<const T *>(p.target);
+    const T *dbase = reinterpret_cast<const T *>(p.draft);
+    const bool padded = !GREEDY && p.draft_stride > 0;
+
+    // Where the unit at (row rg, column chunk q) comes from; false when the
+    // row lies past the real rows (nt target, nd draft) and `check` is set.
+    auto locate = [&](int64_t rg, int q, const T *&src, int &len, int &col0, int64_t nt,
+                      int64_t nd, bool check) -> bool {
+        col0 = q * g.Q;
+        len = min(g.Q, V - col0);
+        if (rg < g.max_rows) {
+            if (check && rg >= nt)
+                return false;
+            src = tbase + rg * (int64_t)V + col0;
+            return true;
+        }
+        const int64_t slot = rg - g.max_rows;
+        if (check && slot >= nd)
+            return false;
+        int64_t row = slot;
+        if (padded) {  // packed slot -> (request, position) -> padded row
+            int lo = 0, hi = B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (cu_s[mid] <= slot)
+                    lo = mid;
+                else
+                    hi = mid - 1;
+            }
+            row = (int64_t)lo * p.draft_stride + (slot - cu_s[lo]);
+        }
+        src = dbase + row * (int64_t)V + col0;
+        return true;
+    };
+
+    uint32_t issued = 0, phase = 0;
+    auto issue = [&](int64_t rg, int q, int k, int64_t nt, int64_t nd, bool check) {
+        const T *src;
+        int len, col0;
+        if (!locate(rg, q, src, len, col0, nt, nd, check))
+            return;
+        T *dst = reinterpret_cast<T *>(ring + (size_t)k * p.piece_smem);
+        if (p.tma) {
+            if (lane == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
+                mbar_arrive_expect_tx(&bars[wib][k], bytes);
+                bulk_g2s(dst, src, bytes, &bars[wib][k]);
+            }
+        } else {
+            for (int e = lane; e < len; e += 32)
+                dst[e] = src[e];
+            __syncwarp();
+        }
+        issued |= 1u << k;
+    };
+
+    // cursors: (row, column chunk) of the next unit to consume and to issue
+    int64_t c_rg = u0 / g.cpr;
+    int c_q = (int)(u0 - c_rg * g.cpr);
+    int64_t i_rg = c_rg;
+    int i_q = c_q;
+    const int64_t n_units = u1 - u0;
+    auto advance = [&](int64_t &rg, int &q) {
+        if (++q == g.cpr) {
+            q = 0;
+            ++rg;
+        }
+    };
+
+    // Packed rows have known addresses: their first copies start before the
+    // offsets arrive (the offsets only tell which rows past the real count
+    // to skip).  Padded draft rows need the offsets first.
+    int64_t nt = g.max_rows, nd = p.draft_slots;
+    int n_issued = 0;
+    if (!padded)
+        for (; n_issued < kRing && n_issued < n_units; ++n_issued) {
+            issue(i_rg, i_q, n_issued, nt, nd, false);
+            advance(i_rg, i_q);
+        }
+    // CTA 0 validates the offsets for both kernels (and every CTA does when
+    // it maps padded rows through them).
+    if (padded || blockIdx.x == 0) {
+        int bad = 0;
+        for (int k = threadIdx.x; k <= B; k += kStreamThreads) {
+            const int v = __ldg(p.cu + k);
+            if (padded)
+                cu_s[k] = v;
+            if (k < B) {
+                const int K = __ldg(p.cu + k + 1) - v;
+                if (K < 0 || K > kMaxDraft || (p.draft_stride > 0 && K > p.draft_stride))
+                    bad = 1;
+            } else if ((int64_t)v + B > g.max_rows) {
+                bad = 1;
+            }
+            if (k == 0 && v != 0)
+                bad = 1;
+        }
+        bad = __syncthreads_or(bad);
+        if (blockIdx.x == 0) {
+            if (threadIdx.x == 0) {
+                *p.cu_flag = bad ? 0u : 1u;
+                if (bad)
+                    set_status(p.status, ST_INVALID);
+            }
+            if (bad) {
+                for (int64_t k = threadIdx.x; k < g.max_rows; k += kStreamThreads)
+                    p.out_tokens[k] = -1;
+                for (int k = threadIdx.x; k < B; k += kStreamThreads)
+                    p.out_len[k] = -1;
+            }
+        }
+        if (bad) {  // malformed offsets: drain the copies in flight, read nothing more
+            if (p.tma)
+                for (int k = 0; k < kRing; ++k)
+                    if (issued >> k & 1)
+                        mbar_wait_bounded(&bars[wib][k], 0);
+            return;
+        }
+    }
+    {
+        int v = lane == 0 ? __ldg(p.cu + B) : 0;
+        v = __shfl_sync(0xffffffffu, v, 0);
+        nd = min(nd, (int64_t)v);
+        nt = min(g.max_rows, (int64_t)v + B);
+    }
+    if (padded)
+        for (; n_issued < kRing && n_issued < n_units; ++n_issued) {
+            issue(i_rg, i_q, n_issued, nt, nd, true);
+            advance(i_rg, i_q);
+        }
+
+    LaneAcc acc{-INFINITY, 0.f, 0.f, INT_MAX, 0};
+    bool seg_active = false;
+    int k = 0;  // ring slot of the unit being consumed
+    for (int64_t n = 0; n < n_units; ++n) {
+        const T *src;
+        int len, col0;
+        const int64_t rg = c_rg;
+        const bool live = locate(c_rg, c_q, src, len, col0, nt, nd, true);
+        if (issued >> k & 1) {
+            if (p.tma) {
+                if (!mbar_wait_bounded(&bars[wib][k], phase >> k & 1)) {
+                    set_status(p.status, ST_TIMEOUT);
+                    mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                }
+                phase ^= 1u << k;
+            }
+            issued &= ~(1u << k);
+            if (live) {
+                const T *buf = reinterpret_cast<const T *>(ring + (size_t)k * p.piece_smem);
+                if constexpr (GREEDY) {
+                    if constexpr (sizeof(T) == 2)
+                        unit_argmax_bf16<MAXV>(reinterpret_cast<const uint16_t *>(buf), len, col0,
+                                               acc);
+                    else
+                        unit_argmax_f32<MAXV>(reinterpret_cast<const float *>(buf), len, col0,
+                                              acc);
+                } else {
+                    if constexpr (sizeof(T) == 2)
+                        unit_softmax_bf16<MAXV>(reinterpret_cast<const uint16_t *>(buf), len, p.c,
+                                                acc);
+                    else
+                        unit_softmax_f32<MAXV>(reinterpret_cast<const float *>(buf), len, p.c,
+                                               acc);
+                }
+                seg_active = true;
+            }
+        }
+        __syncwarp();  // every lane is done with slot k before it is refilled
+        if (n_issued < n_units) {
+            issue(i_rg, i_q, k, nt, nd, true);
+            advance(i_rg, i_q);
+            ++n_issued;
+        }
+        advance(c_rg, c_q);
+        const bool row_ends = (n + 1 == n_units) || (c_rg != rg);
+        if (row_ends && seg_active) {
+            store_partial<GREEDY>(acc, p.c, p.part + rg + w);
+            seg_active = false;
+        }
+        if (++k == kRing)
+            k = 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// kernel 2: merge, accept test, final draw
+// ---------------------------------------------------------------------------
+
+constexpr int kFinishThreads = 256;
+constexpr int kFinishWarps = kFinishThreads / 32;
+
+// Merge the partials of flattened row rg (one warp), T > 0: (m, s) with
+// s = sum_v exp2((x_v - m) c).
+__device__ __forceinline__ void merge_softmax_row(const FinishParams &p, int64_t rg, float &m_out,
+                                                  double &s_out)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t ua = rg * p.g.cpr, ub = ua + p.g.cpr - 1;
+    const int wf = owner_of(ua, p.g), wl = owner_of(ub, p.g);
+    float m = -INFINITY;
+    for (int w = wf + lane; w <= wl; w += 32)
+        m = max_nan(m, __ldcg(&p.part[rg + w].m));
+    m = warp_max_nan(m);
+    double s = 0.0;
+    for (int w = wf + lane; w <= wl; w += 32) {
+        const double sw = __ldcg(&p.part[rg + w].s);
+        if (sw != 0.0)
+            s += sw * (double)exp2f((__ldcg(&p.part[rg + w].m) - m) * p.c);
+    }
+    s = warp_sum_d(s);
+    m_out = m;
+    s_out = s;
+}
+
+// T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
+__device__ __forceinline__ int merge_argmax_row(const FinishParams &p, int64_t rg)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t ua = rg * p.g.cpr, ub = ua + p.g.cpr - 1;
+    const int wf = owner_of(ua, p.g), wl = owner_of(ub, p.g);
+    float best = -INFINITY;
+    int bidx = INT_MAX, nan = 0;
+    for (int w = wf + lane; w <= wl; w += 32) {
+        const float m = __ldcg(&p.part[rg + w].m);
+        const int ix = __ldcg(&p.part[rg + w].idx);
+        if (ix == -2)
+            nan = 1;
+        else if (ix >= 0 && (m > best || (m == best && ix < bidx))) {
+            best = m;
+            bidx = ix;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (ob > best || (ob == best && oi < bidx)) {
+            best = ob;
+            bidx = oi;
+        }
+    }
+    nan = __any_sync(0xffffffffu, nan);
+    return nan ? -2 : (bidx == INT_MAX ? -1 : (best == INFINITY ? -3 : bidx));
 }
 
 __device__ __forceinline__ bool row_ok(float m, double s)
@@ -84,692 +719,461 @@ __device__ __forceinline__ bool row_ok(float m, double s)
     return isfinite(m) && isfinite(s) && s > 0.0;
 }
 
-// Thread 0 only: arm `bar` for `len` elements and start the bulk copy.
-template <typename T>
-__device__ __forceinline__ void tma_issue(T *dst, const T *src, int len, uint64_t *bar)
-{
-    const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
-    mbar_arrive_expect_tx(bar, bytes);
-    bulk_g2s(dst, src, bytes, bar);
-}
-
-// Every thread: wait for the copy; on expiry flag a timeout and wait once more
-// (bounded) so no copy is left writing into shared memory.
-__device__ __forceinline__ void tma_wait(uint64_t *bar, uint32_t phase, uint32_t *status)
-{
-    if (!mbar_wait_bounded(bar, phase)) {
-        set_status(status, ST_TIMEOUT);
-        mbar_wait_bounded(bar, phase);
-    }
-}
-
-template <typename T>
-__device__ __forceinline__ void plain_copy(T *dst, const T *src, int len)
-{
-    for (int k = threadIdx.x; k < len; k += kThreads)
-        dst[k] = src[k];
-}
-
-// CTA 0 only, when the offsets are malformed: poison every output.
-__device__ void poison_all(const VerifyParams &p)
-{
-    if (threadIdx.x == 0)
-        set_status(p.status, ST_INVALID);
-    for (int64_t k = threadIdx.x; k < p.max_rows; k += kThreads)
-        p.out_tokens[k] = -1;
-    for (int k = threadIdx.x; k < p.B; k += kThreads) {
-        p.out_len[k] = -1;
-        p.hand[k].a = -1;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// per-request stages (run by the CTA that completes the request)
-// ---------------------------------------------------------------------------
-
-template <typename T>
-__device__ void greedy_stage(const VerifyParams &p, const int32_t *cu_s, int i, int *row_g)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = cu_s[i + 1] - cu_s[i];
-    const int64_t t0 = (int64_t)cu_s[i] + i;
-    for (int rho = warp; rho <= K; rho += kWarps) {
-        const Partial *P = p.part1 + (t0 + rho) * p.nchunks;
-        float best = -INFINITY;
-        int bidx = INT_MAX;
-        int nan = 0;
-        for (int c = lane; c < p.nchunks; c += 32) {
-            const float m = __ldcg(&P[c].m);
-            const int ix = __ldcg(&P[c].idx);
-            if (ix == -2)
-                nan = 1;
-            else if (ix >= 0 && (m > best || (m == best && ix < bidx))) {
-                best = m;
-                bidx = ix;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-            if (ob > best || (ob == best && oi < bidx)) {
-                best = ob;
-                bidx = oi;
-            }
-        }
-        nan = __any_sync(0xffffffffu, nan);
-        if (lane == 0)
-            row_g[rho] = nan ? -2 : (bidx == INT_MAX ? -1 : (best == INFINITY ? -3 : bidx));
-    }
-    __syncthreads();
-    if (warp != 0)
-        return;
-    const int j = lane;
-    const bool act = j < K;
-    int x = -1;
-    bool bad_tok = false;
-    if (act) {
-        x = __ldg(p.tokens + draft_index(p, cu_s, i, j));
-        bad_tok = x < 0 || x >= p.V;
-    }
-    bool bad_nf = false;
-    for (int jj = lane; jj <= K; jj += 32)
-        bad_nf |= row_g[jj] < 0;
-    const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
-    const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
-    const unsigned rej = __ballot_sync(0xffffffffu, act && x != row_g[j < K ? j : 0]);
-    const bool timeout = read_status(p.status) & ST_TIMEOUT;
-    if (nf || bt || timeout) {
-        if (lane == 0)
-            set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
-        for (int jj = lane; jj <= K; jj += 32)
-            p.out_tokens[t0 + jj] = -1;
-        if (lane == 0)
-            p.out_len[i] = -1;
-        return;
-    }
-    const int a = rej ? __ffs(rej) - 1 : K;
-    for (int jj = lane; jj <= K; jj += 32)
-        p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
-    if (lane == 0)
-        p.out_len[i] = a;
-}
-
-template <typename T>
-__device__ void sample_stage(const VerifyParams &p, const int32_t *cu_s, int i, float *row_m,
-                             double *row_s)
-{
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int K = cu_s[i + 1] - cu_s[i];
-    const int64_t t0 = (int64_t)cu_s[i] + i;
-    const int nrows = 2 * K + 1;
-    // merge the chunk partials of every row: m = max, s = sum s_c * exp((m_c - m) / T)
-    for (int rho = warp; rho < nrows; rho += kWarps) {
-        const int64_t gslot = rho <= K ? t0 + rho : p.max_rows + cu_s[i] + (rho - K - 1);
-        const Partial *P = p.part1 + gslot * p.nchunks;
-        float m = -INFINITY;
-        for (int c = lane; c < p.nchunks; c += 32)
-            m = max_nan(m, __ldcg(&P[c].m));
-        m = warp_max_nan(m);
-        double s = 0.0;
-        for (int c = lane; c < p.nchunks; c += 32) {
-            const double sc = __ldcg(&P[c].s);
-            if (sc != 0.0)
-                s += sc * exp(((double)__ldcg(&P[c].m) - (double)m) * p.inv_T);
-        }
-        s = warp_sum_d(s);
-        if (lane == 0) {
-            row_m[rho] = m;
-            row_s[rho] = s;
-        }
-    }
-    __syncthreads();
-    if (warp != 0)
-        return;
-    const int j = lane;
-    const bool act = j < K;
-    int x = -1;
-    bool bad_tok = false, bad_nf = false, acc = true;
-    if (act) {
-        const int64_t di = draft_index(p, cu_s, i, j);
-        x = __ldg(p.tokens + di);
-        if (x < 0 || x >= p.V) {
-            bad_tok = true;
-        } else {
-            const float mt = row_m[j], md = row_m[K + 1 + j];
-            const double st = row_s[j], sd = row_s[K + 1 + j];
-            if (!row_ok(mt, st) || !row_ok(md, sd)) {
-                bad_nf = true;
-            } else {
-                const T *trow = reinterpret_cast<const T *>(p.target) + (t0 + j) * p.V;
-                const T *drow = reinterpret_cast<const T *>(p.draft) + di * p.V;
-                const double gt = Elem<T>::ld_global(trow, x);
-                const double gd = Elem<T>::ld_global(drow, x);
-                const double pp = exp((gt - (double)mt) * p.inv_T) / st;
-                const double qq = exp((gd - (double)md) * p.inv_T) / sd;
-                const double ratio = qq > 0.0 ? pp / qq : (pp > 0.0 ? INFINITY : 0.0);
-                acc = (double)__ldg(p.u_accept + di) < ratio;
-                if (p.out_p)
-                    p.out_p[di] = (float)pp;
-                if (p.out_q)
-                    p.out_q[di] = (float)qq;
-            }
-        }
-    }
-    if (lane == 0 && !row_ok(row_m[K], row_s[K]))
-        bad_nf = true;
-    const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
-    const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
-    const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
-    const bool timeout = read_status(p.status) & ST_TIMEOUT;
-    if (nf || bt || timeout) {
-        if (lane == 0)
-            set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
-        for (int jj = lane; jj <= K; jj += 32)
-            p.out_tokens[t0 + jj] = -1;
-        if (lane == 0) {
-            p.out_len[i] = -1;
-            p.hand[i].a = -1;
-        }
-        return;
-    }
-    const int a = rej ? __ffs(rej) - 1 : K;
-    for (int jj = lane; jj <= K; jj += 32) {
-        if (jj < a)
-            p.out_tokens[t0 + jj] = x;  // jj == lane here, since a <= 32
-        else if (jj > a)
-            p.out_tokens[t0 + jj] = -1;
-    }
-    if (lane == 0) {
-        p.out_len[i] = a;
-        Handoff h;
-        h.a = a;
-        h.pad = 0;
-        h.trow = t0 + a;
-        h.drow = a < K ? draft_index(p, cu_s, i, a) : -1;
-        h.m_t = row_m[a];
-        h.s_t = row_s[a];
-        h.m_d = a < K ? row_m[K + 1 + a] : 0.f;
-        h.s_d = a < K ? row_s[K + 1 + a] : 0.0;
-        p.hand[i] = h;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// kernel 1: row chunks
-// ---------------------------------------------------------------------------
-
-template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(kThreads) rows_kernel(const VerifyParams p)
-{
-    extern __shared__ __align__(128) unsigned char dsm[];
-    T *buf = reinterpret_cast<T *>(dsm);
-    int32_t *cu_s = reinterpret_cast<int32_t *>(dsm + p.chunk_smem);
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ float red_f[kWarps];
-    __shared__ double red_d[kWarps];
-    __shared__ int red_i[kWarps];
-    __shared__ int s_last;
-    __shared__ float row_m[2 * kMaxDraft + 1];
-    __shared__ double row_s[2 * kMaxDraft + 1];
-    __shared__ int row_g[kMaxDraft + 1];
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int B = p.B, V = p.V;
-    const int64_t tgt_units = p.max_rows * p.nchunks;
-    const int64_t u = blockIdx.x;
-    const bool is_draft = !GREEDY && u >= tgt_units;
-    const int64_t uu = is_draft ? u - tgt_units : u;
-    const int64_t slot = uu / p.nchunks;
-    const int c = (int)(uu % p.nchunks);
-    const int64_t c0 = (int64_t)c * p.chunk_elems;
-    const int len = (int)min((int64_t)p.chunk_elems, (int64_t)V - c0);
-    const T *base = reinterpret_cast<const T *>(is_draft ? p.draft : p.target);
-
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    // Target rows and packed draft rows have a known address: start the copy
-    // before the offsets arrive.
-    bool issued = false;
-    if (p.tma && (!is_draft || p.draft_stride == 0)) {
-        if (tid == 0)
-            tma_issue(buf, base + slot * V + c0, len, &bar);
-        issued = true;
-    }
-    for (int k = tid; k <= B; k += kThreads)
-        cu_s[k] = __ldg(p.cu + k);
-    __syncthreads();
-    int bad = 0;
-    for (int k = tid; k < B; k += kThreads) {
-        const int K = cu_s[k + 1] - cu_s[k];
-        if (K < 0 || K > kMaxDraft || (p.draft_stride > 0 && K > p.draft_stride))
-            bad = 1;
-    }
-    if (tid == 0 && (cu_s[0] != 0 || (int64_t)cu_s[B] + B > p.max_rows))
-        bad = 1;
-    bad = __syncthreads_or(bad);
-    if (bad) {
-        if (blockIdx.x == 0)
-            poison_all(p);
-        if (issued)
-            tma_wait(&bar, 0, p.status);
-        return;
-    }
-    const int nd = cu_s[B];
-    int i, j;
-    bool active;
-    if (!is_draft) {  // target slot: request i owns rows [cu[i] + i, cu[i+1] + i + 1)
-        active = slot < (int64_t)nd + B;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)cu_s[mid] + mid <= slot)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        i = lo;
-        j = (int)(slot - cu_s[i] - i);
-    } else {  // packed draft slot: request i owns [cu[i], cu[i+1])
-        active = slot < nd;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (cu_s[mid] <= slot)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        i = lo;
-        j = (int)(slot - cu_s[i]);
-    }
-    if (!active) {
-        if (issued)
-            tma_wait(&bar, 0, p.status);
-        return;
-    }
-    const int64_t row = (is_draft && p.draft_stride > 0) ? (int64_t)i * p.draft_stride + j : slot;
-    if (p.tma) {
-        if (!issued && tid == 0)
-            tma_issue(buf, base + row * V + c0, len, &bar);
-        tma_wait(&bar, 0, p.status);
-    } else {
-        plain_copy(buf, base + row * V + c0, len);
-        __syncthreads();
-    }
-
-    constexpr int VE = Elem<T>::kPerVec;
-    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
-    const int nvec = len / VE;
-    Partial part;
-    if (GREEDY) {
-        float best = -INFINITY;
-        int bidx = INT_MAX;
-        int nan = 0;
-        for (int v = tid; v < nvec; v += kThreads) {
-            float f[VE];
-            Elem<T>::unpack(vb[v], f);
-#pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                nan |= f[e] != f[e];
-                if (f[e] > best) {
-                    best = f[e];
-                    bidx = v * VE + e;
-                }
-            }
-        }
-        for (int k = nvec * VE + tid; k < len; k += kThreads) {
-            const float x = Elem<T>::at(buf, k);
-            nan |= x != x;
-            if (x > best) {
-                best = x;
-                bidx = k;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-            if (ob > best || (ob == best && oi < bidx)) {
-                best = ob;
-                bidx = oi;
-            }
-        }
-        if (lane == 0) {
-            red_f[warp] = best;
-            red_i[warp] = bidx;
-        }
-        nan = __syncthreads_or(nan);
-        if (tid == 0) {
-            for (int w = 1; w < kWarps; ++w)
-                if (red_f[w] > best || (red_f[w] == best && red_i[w] < bidx)) {
-                    best = red_f[w];
-                    bidx = red_i[w];
-                }
-            part.m = best;
-            part.idx = nan ? -2 : (bidx == INT_MAX ? -1 : (int)(c0 + bidx));
-            part.s = 0.0;
-        }
-    } else {
-        float mx = -INFINITY;
-        for (int v = tid; v < nvec; v += kThreads) {
-            float f[VE];
-            Elem<T>::unpack(vb[v], f);
-#pragma unroll
-            for (int e = 0; e < VE; ++e)
-                mx = max_nan(mx, f[e]);
-        }
-        for (int k = nvec * VE + tid; k < len; k += kThreads)
-            mx = max_nan(mx, Elem<T>::at(buf, k));
-        const float m = block_max_nan(mx, red_f);
-        double s;
-        if (m != m) {
-            s = __longlong_as_double(0x7ff8000000000000ll);
-        } else if (m == -INFINITY) {
-            s = 0.0;  // every entry of the chunk is masked
-        } else {
-            const float ch = p.c_hi, cl = p.c_lo;
-            float acc = 0.f;
-            for (int v = tid; v < nvec; v += kThreads) {
-                float f[VE];
-                Elem<T>::unpack(vb[v], f);
-                float e[VE];
-#pragma unroll
-                for (int k = 0; k < VE; ++k)
-                    e[k] = exp2f(exp_arg(f[k] - m, ch, cl));
-#pragma unroll
-                for (int w = 1; w < VE; w <<= 1)
-#pragma unroll
-                    for (int k = 0; k < VE; k += 2 * w)
-                        e[k] += e[k + w];
-                acc += e[0];
-            }
-            for (int k = nvec * VE + tid; k < len; k += kThreads)
-                acc += exp2f(exp_arg(Elem<T>::at(buf, k) - m, ch, cl));
-            s = block_sum_d((double)acc, red_d);
-        }
-        part.m = m;
-        part.idx = 0;
-        part.s = s;
-    }
-    if (tid == 0) {
-        const int64_t gslot = is_draft ? p.max_rows + slot : slot;
-        p.part1[gslot * p.nchunks + c] = part;
-        __threadfence();
-        const int K = cu_s[i + 1] - cu_s[i];
-        const uint32_t need = (uint32_t)((GREEDY ? K + 1 : 2 * K + 1) * p.nchunks);
-        const uint32_t old = atomicAdd(p.cnt1 + i, 1u);
-        s_last = old == need - 1;
-    }
-    __syncthreads();
-    if (!s_last)
-        return;
-    __threadfence();
-    if (tid == 0)
-        p.cnt1[i] = 0;  // ready for the next call
-    if (GREEDY)
-        greedy_stage<T>(p, cu_s, i, row_g);
-    else
-        sample_stage<T>(p, cu_s, i, row_m, row_s);
-}
-
-// ---------------------------------------------------------------------------
-// kernel 2: final draw (T > 0)
-// ---------------------------------------------------------------------------
-
 struct DrawCtx {
-    const void *trow;
-    const void *drow;
     bool resid;
-    float m_t, m_d, inv_st, inv_sd;
-    float c_hi, c_lo;
+    float c, mct, mcd;  // c and fl(m c) of the two rows
+    float sc_t, sc_d;   // 2^(fl(m c) - m c) / s: normalisers including the rounding fix
 };
 
-template <typename T>
-__device__ __forceinline__ float draw_weight(const DrawCtx &d, const T *tb, const T *db, int k)
+// Final-draw weight of one element (pair).
+__device__ __forceinline__ float draw_w(const DrawCtx &d, float t, float x)
 {
-    const float pt = exp2f(exp_arg(Elem<T>::at(tb, k) - d.m_t, d.c_hi, d.c_lo));
+    const float pt = ex2_approx(fmaf(t, d.c, -d.mct));
     if (!d.resid)
-        return pt;  // bonus draw (unnormalised p)
-    const float pd = exp2f(exp_arg(Elem<T>::at(db, k) - d.m_d, d.c_hi, d.c_lo));
-    return fmaxf(pt * d.inv_st - pd * d.inv_sd, 0.f);
+        return pt;  // bonus draw (or all-zero residual): unnormalised p
+    const float pd = ex2_approx(fmaf(x, d.c, -d.mcd));
+    return fmaxf(pt * d.sc_t - pd * d.sc_d, 0.f);
 }
 
-// Stage chunk c of the draw rows into shared memory (all threads).
 template <typename T>
-__device__ __forceinline__ int stage_draw_chunk(const VerifyParams &p, const DrawCtx &d, int c,
-                                                T *tb, T *db, uint64_t *bar, uint32_t &phase)
+__device__ __forceinline__ int stage_chunk(const FinishParams &p, const T *trow, const T *drow,
+                                           bool resid, int c, T *tb, T *db, uint64_t *bar,
+                                           uint32_t &phase)
 {
-    const int64_t c0 = (int64_t)c * p.chunk_elems;
-    const int len = (int)min((int64_t)p.chunk_elems, (int64_t)p.V - c0);
-    const T *ts = reinterpret_cast<const T *>(d.trow) + c0;
-    const T *dsrc = d.resid ? reinterpret_cast<const T *>(d.drow) + c0 : nullptr;
-    __syncthreads();  // previous users of the buffers are done
+    const int col0 = c * p.nce;
+    const int len = min(p.nce, p.V - col0);
+    __syncthreads();  // earlier readers of the buffers are done
     if (p.tma) {
         if (threadIdx.x == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
-            mbar_arrive_expect_tx(bar, d.resid ? 2 * bytes : bytes);
-            bulk_g2s(tb, ts, bytes, bar);
-            if (d.resid)
-                bulk_g2s(db, dsrc, bytes, bar);
+            mbar_arrive_expect_tx(bar, resid ? 2 * bytes : bytes);
+            bulk_g2s(tb, trow + col0, bytes, bar);
+            if (resid)
+                bulk_g2s(db, drow + col0, bytes, bar);
         }
-        tma_wait(bar, phase, p.status);
+        if (!mbar_wait_bounded(bar, phase)) {
+            set_status(p.status, ST_TIMEOUT);
+            mbar_wait_bounded(bar, phase);
+        }
         phase ^= 1u;
     } else {
-        plain_copy(tb, ts, len);
-        if (d.resid)
-            plain_copy(db, dsrc, len);
+        for (int k = threadIdx.x; k < len; k += kFinishThreads) {
+            tb[k] = trow[col0 + k];
+            if (resid)
+                db[k] = drow[col0 + k];
+        }
         __syncthreads();
     }
     return len;
 }
 
-// Sum of w over this thread's contiguous run of the staged chunk (fp32, in
-// index order).  Runs: thread t owns [t*run, min(len, (t+1)*run)).
 template <typename T>
-__device__ __forceinline__ float run_sum(const DrawCtx &d, const T *tb, const T *db, int len,
-                                         int &k0, int &k1)
+__device__ __forceinline__ float draw_at(const DrawCtx &d, const T *tb, const T *db, int k)
 {
-    const int run = (len + kThreads - 1) / kThreads;
-    k0 = min(len, (int)threadIdx.x * run);
-    k1 = min(len, k0 + run);
-    float acc = 0.f;
-    for (int k = k0; k < k1; ++k)
-        acc += draw_weight<T>(d, tb, db, k);
-    return acc;
+    return draw_w(d, Elem<T>::at(tb, k), d.resid ? Elem<T>::at(db, k) : 0.f);
 }
 
+// Sum of the draw weights of a staged chunk (thread-strided fp32, then fp64
+// across threads in a fixed order).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) final_kernel(const VerifyParams p)
+__device__ __forceinline__ double chunk_sum(const DrawCtx &d, const T *tb, const T *db, int len,
+                                            double *red)
+{
+    float acc = 0.f;
+    for (int k = threadIdx.x; k < len; k += kFinishThreads)
+        acc += draw_at(d, tb, db, k);
+    return block_sum_d((double)acc, red);
+}
+
+// Smallest k of the staged chunk with base + C(k) > target, C the running sum
+// in index order; when rounding leaves none, the last k with weight > 0.
+// Warps own contiguous segments; in the segment holding the target, 32
+// consecutive elements are scanned per step with a warp prefix sum.
+template <typename T>
+__device__ int chunk_search(const DrawCtx &d, const T *tb, const T *db, int len, double base,
+                            double target, double *wtot, int *s_res)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int seg = (len + kFinishWarps - 1) / kFinishWarps;
+    const int k0 = min(len, warp * seg), k1 = min(len, k0 + seg);
+    float acc = 0.f;
+    for (int k = k0 + lane; k < k1; k += 32)
+        acc += draw_at(d, tb, db, k);
+    const double tot = warp_sum_d((double)acc);
+    __syncthreads();
+    if (lane == 0)
+        wtot[warp] = tot;
+    if (threadIdx.x == 0)
+        *s_res = -1;
+    __syncthreads();
+    double lo = base;
+    int wc = -1;
+    for (int w2 = 0; w2 < kFinishWarps; ++w2) {
+        if (lo + wtot[w2] > target) {
+            wc = w2;
+            break;
+        }
+        lo += wtot[w2];
+    }
+    if (warp == wc) {
+        double run = lo;
+        for (int kb = k0; kb < k1; kb += 32) {
+            const int k = kb + lane;
+            const float x = k < k1 ? draw_at(d, tb, db, k) : 0.f;
+            float incl = x;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float n = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o)
+                    incl += n;
+            }
+            const unsigned hit =
+                __ballot_sync(0xffffffffu, k < k1 && run + (double)incl > target);
+            if (hit) {
+                if (lane == 0)
+                    *s_res = kb + __ffs(hit) - 1;
+                break;
+            }
+            run += (double)__shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    __syncthreads();
+    int res = *s_res;
+    if (res < 0) {
+        int best = -1;
+        for (int k = threadIdx.x; k < len; k += kFinishThreads)
+            if (draw_at(d, tb, db, k) > 0.f)
+                best = k;
+        if (best >= 0)
+            atomicMax(s_res, best);
+        __syncthreads();
+        res = *s_res;
+    }
+    return res;
+}
+
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
     T *tb = reinterpret_cast<T *>(dsm);
     T *db = reinterpret_cast<T *>(dsm + p.chunk_smem);
     __shared__ __align__(8) uint64_t bar;
-    __shared__ double red_d[kWarps];
+    __shared__ float row_m[2 * kMaxDraft + 1];
+    __shared__ double row_s[2 * kMaxDraft + 1];
+    __shared__ int row_g[kMaxDraft + 1];
+    __shared__ double red[kFinishWarps];
     __shared__ double s_tot[kMaxChunks];
-    __shared__ int s_last, s_chunk, s_claim, s_y, s_mode;
     __shared__ double s_base, s_target;
+    __shared__ int s_a, s_bad, s_last, s_res, s_mode, s_cs;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int i = blockIdx.x / p.nchunks, c = blockIdx.x % p.nchunks;
-    const Handoff *hp = p.hand + i;
-    const int a = __ldcg(&hp->a);
-    if (a < 0)
-        return;  // poisoned request: nothing to draw
-    DrawCtx d;
-    const int64_t trow = __ldcg(reinterpret_cast<const long long *>(&hp->trow));
-    const int64_t drow = __ldcg(reinterpret_cast<const long long *>(&hp->drow));
-    d.resid = drow >= 0;
-    if (trow < 0 || trow >= p.max_rows || drow >= p.draft_rows) {  // never from a valid handoff
-        if (tid == 0)
-            set_status(p.status, ST_INVALID);
-        return;
-    }
-    d.trow = reinterpret_cast<const T *>(p.target) + trow * p.V;
-    d.drow = d.resid ? reinterpret_cast<const T *>(p.draft) + drow * p.V : nullptr;
-    d.m_t = __ldcg(&hp->m_t);
-    d.m_d = __ldcg(&hp->m_d);
-    d.inv_st = (float)(1.0 / __ldcg(&hp->s_t));
-    d.inv_sd = d.resid ? (float)(1.0 / __ldcg(&hp->s_d)) : 0.f;
-    d.c_hi = p.c_hi;
-    d.c_lo = p.c_lo;
+    const int NC = GREEDY ? 1 : p.NC;
+    const int i = blockIdx.x / NC, c = blockIdx.x % NC;
 
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    uint32_t phase = 0;
-    int k0, k1;
-    int len = stage_draw_chunk<T>(p, d, c, tb, db, &bar, phase);
-    float acc = run_sum<T>(d, tb, db, len, k0, k1);
-    double tot = block_sum_d((double)acc, red_d);
-    if (tid == 0) {
-        p.part2[(int64_t)i * p.nchunks + c] = tot;
-        __threadfence();
-        const uint32_t old = atomicAdd(p.cnt2 + i, 1u);
-        s_last = old == (uint32_t)p.nchunks - 1;
-    }
-    __syncthreads();
-    if (!s_last)
+    pdl_wait();  // kernel 1 has completed and its writes are visible
+    if (__ldcg(p.cu_flag) == 0u)
+        return;  // malformed offsets: kernel 1 poisoned every output
+    const int cu_i = __ldg(p.cu + i);
+    const int K = __ldg(p.cu + i + 1) - cu_i;
+    const int64_t t0 = (int64_t)cu_i + i;
+    const int64_t gmr = p.g.max_rows;
+
+    if constexpr (GREEDY) {
+        for (int rho = warp; rho <= K; rho += kFinishWarps) {
+            const int gj = merge_argmax_row(p, t0 + rho);
+            if (lane == 0)
+                row_g[rho] = gj;
+        }
+        __syncthreads();
+        if (warp != 0)
+            return;
+        const bool act = lane < K;
+        int x = -1;
+        bool bad_tok = false;
+        if (act) {
+            x = __ldg(p.tokens + draft_index(p.draft_stride, p.cu, i, lane));
+            bad_tok = x < 0 || x >= p.V;
+        }
+        bool bad_nf = false;
+        for (int jj = lane; jj <= K; jj += 32)
+            bad_nf |= row_g[jj] < 0;
+        const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
+        const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
+        const unsigned rej = __ballot_sync(0xffffffffu, act && x != row_g[act ? lane : 0]);
+        const bool timeout = read_status(p.status) & ST_TIMEOUT;
+        if (nf || bt || timeout) {
+            if (lane == 0)
+                set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+            for (int jj = lane; jj <= K; jj += 32)
+                p.out_tokens[t0 + jj] = -1;
+            if (lane == 0)
+                p.out_len[i] = -1;
+            return;
+        }
+        const int a = rej ? __ffs(rej) - 1 : K;
+        for (int jj = lane; jj <= K; jj += 32)
+            p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
+        if (lane == 0)
+            p.out_len[i] = a;
         return;
-    __threadfence();
-    if (tid == 0) {
-        p.cnt2[i] = 0;
-        for (int cc = 0; cc < p.nchunks; ++cc)
-            s_tot[cc] = __ldcg(p.part2 + (int64_t)i * p.nchunks + cc);
-        double S = 0.0;
-        for (int cc = 0; cc < p.nchunks; ++cc)
-            S += s_tot[cc];
-        s_mode = (d.resid && !(S > 0.0)) ? 1 : 0;  // all-zero residual: draw from p_a
-    }
-    __syncthreads();
-    if (s_mode == 1) {
-        d.resid = false;
-        for (int cc = 0; cc < p.nchunks; ++cc) {
-            len = stage_draw_chunk<T>(p, d, cc, tb, db, &bar, phase);
-            acc = run_sum<T>(d, tb, db, len, k0, k1);
-            tot = block_sum_d((double)acc, red_d);
-            if (tid == 0)
-                s_tot[cc] = tot;
+    } else {
+        // ---- merge (m, s) of the request's 2K+1 rows
+        for (int rho = warp; rho < 2 * K + 1; rho += kFinishWarps) {
+            const int64_t rg = rho <= K ? t0 + rho : gmr + cu_i + (rho - K - 1);
+            float m;
+            double s;
+            merge_softmax_row(p, rg, m, s);
+            if (lane == 0) {
+                row_m[rho] = m;
+                row_s[rho] = s;
+            }
         }
         __syncthreads();
-    }
-    if (tid == 0) {
-        double S = 0.0;
-        for (int cc = 0; cc < p.nchunks; ++cc)
-            S += s_tot[cc];
-        const double target = (double)__ldg(p.u_final + i) * S;
-        double cum = 0.0;
-        int cs = -1;
-        double base = 0.0;
-        for (int cc = 0; cc < p.nchunks; ++cc) {
-            if (cum + s_tot[cc] > target) {
-                cs = cc;
-                base = cum;
-                break;
-            }
-            cum += s_tot[cc];
-        }
-        int last_pos = 0;
-        if (cs < 0) {  // rounding left u*S at or past the end: last chunk with mass
-            cs = 0;
-            double cum2 = 0.0;
-            for (int cc = 0; cc < p.nchunks; ++cc) {
-                if (s_tot[cc] > 0.0) {
-                    cs = cc;
-                    base = cum2;
+        // ---- accept test and first rejection (warp 0; identical in every CTA)
+        if (warp == 0) {
+            const bool act = lane < K;
+            int x = -1;
+            bool bad_tok = false, bad_nf = false, acc = true;
+            double pp = 0.0, qq = 0.0;
+            int64_t di = 0;
+            if (act) {
+                di = draft_index(p.draft_stride, p.cu, i, lane);
+                x = __ldg(p.tokens + di);
+                if (x < 0 || x >= p.V) {
+                    bad_tok = true;
+                } else {
+                    const float mt = row_m[lane], md = row_m[K + 1 + lane];
+                    const double st = row_s[lane], sd = row_s[K + 1 + lane];
+                    if (!row_ok(mt, st) || !row_ok(md, sd)) {
+                        bad_nf = true;
+                    } else {
+                        const T *trow = reinterpret_cast<const T *>(p.target) + (t0 + lane) * p.V;
+                        const T *drw = reinterpret_cast<const T *>(p.draft) + di * p.V;
+                        const double gt = Elem<T>::ld_global(trow, x);
+                        const double gd = Elem<T>::ld_global(drw, x);
+                        pp = (double)exp2_split((gt - (double)mt) * (double)p.c) / st;
+                        qq = (double)exp2_split((gd - (double)md) * (double)p.c) / sd;
+                        const double ratio = qq > 0.0 ? pp / qq : (pp > 0.0 ? INFINITY : 0.0);
+                        acc = (double)__ldg(p.u_accept + di) < ratio;
+                    }
                 }
-                cum2 += s_tot[cc];
             }
-            last_pos = 1;
-        }
-        s_chunk = cs;
-        s_base = base;
-        s_target = last_pos ? INFINITY : target;
-        s_claim = INT_MAX;
-        s_y = -1;
-    }
-    __syncthreads();
-    const int cs = s_chunk;
-    len = stage_draw_chunk<T>(p, d, cs, tb, db, &bar, phase);
-    acc = run_sum<T>(d, tb, db, len, k0, k1);
-    // exclusive scan of the run sums (fp64, fixed order)
-    const double run_d = (double)acc;
-    double incl = run_d;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double n = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += n;
-    }
-    const double prev = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 31)
-        red_d[warp] = incl;
-    __syncthreads();
-    double woff = 0.0;
-    for (int w = 0; w < warp; ++w)
-        woff += red_d[w];
-    const double lo = s_base + (woff + (lane ? prev : 0.0));
-    const double target = s_target;
-    if (k1 > k0 && lo + (double)acc > target)
-        atomicMin(&s_claim, tid);
-    __syncthreads();
-    const int64_t cbase = (int64_t)cs * p.chunk_elems;
-    if (s_claim == tid) {
-        float run = 0.f;
-        int y = -1;
-        for (int k = k0; k < k1; ++k) {
-            run += draw_weight<T>(d, tb, db, k);
-            if (lo + (double)run > target) {
-                y = k;
-                break;
+            if (lane == 0 && !row_ok(row_m[K], row_s[K]))
+                bad_nf = true;
+            const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
+            const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
+            const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
+            const bool timeout = read_status(p.status) & ST_TIMEOUT;
+            const bool bad = nf || bt || timeout;
+            const int a = rej ? __ffs(rej) - 1 : K;
+            if (c == 0) {  // the request's outputs, written once
+                if (bad) {
+                    if (lane == 0)
+                        set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+                    for (int jj = lane; jj <= K; jj += 32)
+                        p.out_tokens[t0 + jj] = -1;
+                    if (lane == 0)
+                        p.out_len[i] = -1;
+                } else {
+                    if (act && p.out_p)
+                        p.out_p[di] = (float)pp;
+                    if (act && p.out_q)
+                        p.out_q[di] = (float)qq;
+                    for (int jj = lane; jj <= K; jj += 32) {
+                        if (jj < a)
+                            p.out_tokens[t0 + jj] = x;  // jj == lane since a <= 32
+                        else if (jj > a)
+                            p.out_tokens[t0 + jj] = -1;
+                    }
+                    if (lane == 0)
+                        p.out_len[i] = a;
+                }
+            }
+            if (lane == 0) {
+                s_a = a;
+                s_bad = bad;
             }
         }
-        s_y = (int)(cbase + y);
-    }
-    __syncthreads();
-    if (s_claim == INT_MAX) {
-        // u*S at or past the chunk's end after rounding: last entry with w > 0
-        if (tid == 0)
-            s_claim = -1;
         __syncthreads();
-        int best = -1;
-        for (int k = k0; k < k1; ++k)
-            if (draw_weight<T>(d, tb, db, k) > 0.f)
-                best = k;
-        if (best >= 0)
-            atomicMax(&s_claim, best);
+        if (s_bad)
+            return;
+
+        // ---- final draw over chunk c of the rows of position a
+        const int a = s_a;
+        const int64_t trow_i = t0 + a;
+        const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
+        if (trow_i >= gmr || drow_i >= p.draft_rows) {  // never with valid offsets
+            if (tid == 0)
+                set_status(p.status, ST_INVALID);
+            return;
+        }
+        DrawCtx d;
+        d.resid = drow_i >= 0;
+        d.c = p.c;
+        {
+            const float mt = row_m[a];
+            d.mct = mt * p.c;
+            d.sc_t = (float)((double)mc_correction(mt, d.mct, p.c) / row_s[a]);
+            if (d.resid) {
+                const float md = row_m[K + 1 + a];
+                d.mcd = md * p.c;
+                d.sc_d = (float)((double)mc_correction(md, d.mcd, p.c) / row_s[K + 1 + a]);
+            } else {
+                d.mcd = 0.f;
+                d.sc_d = 0.f;
+            }
+        }
+        const T *trow = reinterpret_cast<const T *>(p.target) + trow_i * p.V;
+        const T *drow = d.resid ? reinterpret_cast<const T *>(p.draft) + drow_i * p.V : nullptr;
+
+        if (tid == 0) {
+            mbar_init(&bar, 1);
+            fence_mbar_init();
+        }
         __syncthreads();
-        if (tid == 0)
-            s_y = s_claim >= 0 ? (int)(cbase + s_claim) : -1;
+        uint32_t phase = 0;
+        int len = stage_chunk<T>(p, trow, drow, d.resid, c, tb, db, &bar, phase);
+        double tot = chunk_sum<T>(d, tb, db, len, red);
+        if (tid == 0) {
+            p.part2[(int64_t)i * NC + c] = tot;
+            __threadfence();
+            s_last = atomicAdd(p.cnt2 + i, 1u) == (uint32_t)NC - 1;
+        }
         __syncthreads();
-    }
-    if (tid == 0) {
-        if (s_y < 0)
-            set_status(p.status, ST_NONFINITE);
-        p.out_tokens[trow] = s_y;
+        if (!s_last)
+            return;
+        __threadfence();
+        int staged = c;
+        if (tid == 0) {
+            p.cnt2[i] = 0;  // ready for the next call
+            double S = 0.0;
+            for (int cc = 0; cc < NC; ++cc) {
+                s_tot[cc] = __ldcg(p.part2 + (int64_t)i * NC + cc);
+                S += s_tot[cc];
+            }
+            s_mode = (d.resid && !(S > 0.0)) ? 1 : 0;  // all-zero residual: draw from p_a
+        }
+        __syncthreads();
+        if (s_mode == 1) {
+            d.resid = false;
+            for (int cc = 0; cc < NC; ++cc) {
+                len = stage_chunk<T>(p, trow, drow, false, cc, tb, db, &bar, phase);
+                tot = chunk_sum<T>(d, tb, db, len, red);
+                if (tid == 0)
+                    s_tot[cc] = tot;
+                staged = cc;
+            }
+            __syncthreads();
+        }
+        if (tid == 0) {
+            double S = 0.0;
+            for (int cc = 0; cc < NC; ++cc)
+                S += s_tot[cc];
+            const double target = (double)__ldg(p.u_final + i) * S;
+            double cum = 0.0, base = 0.0, tgt = target;
+            int cs = -1;
+            for (int cc = 0; cc < NC; ++cc) {
+                if (cum + s_tot[cc] > target) {
+                    cs = cc;
+                    base = cum;
+                    break;
+                }
+                cum += s_tot[cc];
+            }
+            if (cs < 0) {  // u*S at or past the end after rounding: last chunk with mass
+                cs = 0;
+                double cum2 = 0.0;
+                for (int cc = 0; cc < NC; ++cc) {
+                    if (s_tot[cc] > 0.0) {
+                        cs = cc;
+                        base = cum2;
+                    }
+                    cum2 += s_tot[cc];
+                }
+                tgt = INFINITY;
+            }
+            s_cs = cs;
+            s_base = base;
+            s_target = tgt;
+        }
+        __syncthreads();
+        const int cs = s_cs;
+        if (cs != staged)
+            len = stage_chunk<T>(p, trow, drow, d.resid, cs, tb, db, &bar, phase);
+        else
+            len = min(p.nce, p.V - cs * p.nce);
+        const int k = chunk_search<T>(d, tb, db, len, s_base, s_target, red, &s_res);
+        if (tid == 0) {
+            const int y = k >= 0 ? cs * p.nce + k : -1;
+            if (y < 0)
+                set_status(p.status, ST_NONFINITE);
+            p.out_tokens[trow_i] = y;
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
-// host launcher
+// host side
 // ---------------------------------------------------------------------------
 
+static int sm_count()
+{
+    static int n = [] {
+        int dev = 0, v = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            return v;
+        return 148;
+    }();
+    return n;
+}
+
+// Unit size for a balanced split: U = rows * ceil(V / Q) units over P warps
+// puts ceil(U / P) units on the busiest warp.  Pick the Q (a multiple of the
+// 16-byte granule, at most kPieceBytesMax) that minimises the busiest warp's
+// elements (plus a fixed per-unit cost), preferring larger Q.
+static Geometry plan(int64_t rows_total, int64_t max_rows, int V, int elem, int P_max)
+{
+    Geometry g{};
+    g.max_rows = max_rows;
+    const int gran = 16 / elem;
+    const int qmax = kPieceBytesMax / elem;
+    const int64_t total = rows_total * (int64_t)V;
+    int64_t P = P_max;
+    const int64_t min_work = 2048 / elem;  // at least ~2 KB per warp
+    if (total / min_work < P)
+        P = std::max<int64_t>(1, total / min_work);
+    double best_cost = 1e300;
+    int best_q = qmax;
+    for (int q = qmax; q >= gran && q >= qmax / 8; q -= gran) {
+        const int64_t cpr = (V + q - 1) / q;
+        const int64_t U = rows_total * cpr;
+        const int64_t per = (U + P - 1) / P;
+        const double cost = (double)per * (double)(std::min<int64_t>(q, V) + 64);
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best_q = q;
+        }
+    }
+    g.Q = std::min(best_q, ((V + gran - 1) / gran) * gran);
+    g.cpr = (V + g.Q - 1) / g.Q;
+    g.U = rows_total * (int64_t)g.cpr;
+    g.P = (int)std::min<int64_t>(P, g.U);
+    return g;
+}
+
 template <typename T, bool GREEDY>
-static cudaError_t prepare_rows_kernel()
+static cudaError_t prepare_stream()
 {
     static cudaError_t once = [] {
-        cudaError_t e = cudaFuncSetAttribute(rows_kernel<T, GREEDY>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kChunkBytes + 128 + 4 * (kMaxBatch + 1));
+        const int smem = kStreamWarps * kRing * (int)align_up(kPieceBytesMax, 128) +
+                         4 * (kMaxBatch + 1);
+        cudaError_t e = cudaFuncSetAttribute(stream_kernel<T, GREEDY>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(rows_kernel<T, GREEDY>,
+            e = cudaFuncSetAttribute(stream_kernel<T, GREEDY>,
                                      cudaFuncAttributePreferredSharedMemoryCarveout,
                                      cudaSharedmemCarveoutMaxShared);
         return e;
@@ -777,91 +1181,115 @@ static cudaError_t prepare_rows_kernel()
     return once;
 }
 
-template <typename T>
-static cudaError_t prepare_final_kernel()
+template <typename T, bool GREEDY>
+static cudaError_t prepare_finish()
 {
     static cudaError_t once = [] {
-        cudaError_t e = cudaFuncSetAttribute(final_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             2 * (kChunkBytes + 128));
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(final_kernel<T>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared);
-        return e;
+        return cudaFuncSetAttribute(finish_kernel<T, GREEDY>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    2 * (kDrawChunkBytes + 128));
     }();
     return once;
 }
 
-template <typename T>
+template <typename T, bool GREEDY>
 static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
 {
-    const bool greedy = a.temperature == 0.0;
-    const Chunking ch = chunking(a.V, (int)sizeof(T));
+    const int e = (int)sizeof(T);
     const WsLayout L = ws_layout(a.B, a.max_rows, a.V);
     unsigned char *ws = static_cast<unsigned char *>(a.ws);
-    VerifyParams p{};
-    p.target = a.target;
-    p.draft = a.draft;
-    p.tokens = a.tokens;
-    p.cu = a.cu;
-    p.u_accept = a.u_accept;
-    p.u_final = a.u_final;
-    p.out_tokens = a.out_tokens;
-    p.out_len = a.out_len;
-    p.out_p = a.out_p;
-    p.out_q = a.out_q;
-    p.B = a.B;
-    p.V = a.V;
-    p.max_rows = a.max_rows;
-    p.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
-    p.draft_stride = a.draft_stride;
-    p.nchunks = ch.nchunks;
-    p.chunk_elems = ch.chunk_elems;
-    const bool row16 = ((int64_t)a.V * (int64_t)sizeof(T)) % 16 == 0;
-    const bool t16 = reinterpret_cast<uintptr_t>(a.target) % 16 == 0;
-    const bool d16 = greedy || reinterpret_cast<uintptr_t>(a.draft) % 16 == 0;
-    p.tma = row16 && t16 && d16;
-    p.chunk_smem = (int)align_up((size_t)ch.chunk_elems * sizeof(T), 128);
-    if (!greedy) {
-        const double c = 1.4426950408889634074 / a.temperature;  // log2(e) / T
-        p.c_hi = (float)c;
-        p.c_lo = (float)(c - (double)p.c_hi);
-        p.inv_T = 1.0 / a.temperature;
-    }
-    p.status = reinterpret_cast<uint32_t *>(ws + L.status);
-    p.cnt1 = reinterpret_cast<uint32_t *>(ws + L.cnt1);
-    p.cnt2 = reinterpret_cast<uint32_t *>(ws + L.cnt2);
-    p.part1 = reinterpret_cast<Partial *>(ws + L.part1);
-    p.hand = reinterpret_cast<Handoff *>(ws + L.hand);
-    p.part2 = reinterpret_cast<double *>(ws + L.part2);
+    const int64_t draft_slots = GREEDY ? 0 : a.max_rows - a.B;
+    const int ctas_max = sm_count() * SV_STREAM_CTAS_PER_SM;
+    const Geometry g = plan(a.max_rows + draft_slots, a.max_rows, a.V, e,
+                            std::min(kMaxWorkers, ctas_max * kStreamWarps));
+    const bool row16 = ((int64_t)a.V * e) % 16 == 0;
+    const bool tma = row16 && reinterpret_cast<uintptr_t>(a.target) % 16 == 0 &&
+                     (GREEDY || reinterpret_cast<uintptr_t>(a.draft) % 16 == 0);
+    const double c = GREEDY ? 0.0 : 1.4426950408889634074 / a.temperature;  // log2(e) / T
 
-    cudaError_t e = greedy ? prepare_rows_kernel<T, true>() : prepare_rows_kernel<T, false>();
-    if (e != cudaSuccess)
-        return e;
-    if (!greedy && (e = prepare_final_kernel<T>()) != cudaSuccess)
-        return e;
-    const int64_t units = (a.max_rows + (greedy ? 0 : a.max_rows - a.B)) * ch.nchunks;
-    const size_t smem1 = (size_t)p.chunk_smem + 4 * (size_t)(a.B + 1);
+    StreamParams sp{};
+    sp.target = a.target;
+    sp.draft = a.draft;
+    sp.cu = a.cu;
+    sp.out_tokens = a.out_tokens;
+    sp.out_len = a.out_len;
+    sp.B = a.B;
+    sp.V = a.V;
+    sp.draft_slots = draft_slots;
+    sp.draft_stride = a.draft_stride;
+    sp.g = g;
+    sp.tma = tma;
+    sp.piece_smem = (int)align_up((size_t)g.Q * e, 128);
+    sp.c = (float)c;
+    sp.status = reinterpret_cast<uint32_t *>(ws + L.status);
+    sp.cu_flag = sp.status + 1;
+    sp.part = reinterpret_cast<Partial *>(ws + L.part1);
+
+    FinishParams fp{};
+    fp.target = a.target;
+    fp.draft = a.draft;
+    fp.tokens = a.tokens;
+    fp.cu = a.cu;
+    fp.u_accept = a.u_accept;
+    fp.u_final = a.u_final;
+    fp.out_tokens = a.out_tokens;
+    fp.out_len = a.out_len;
+    fp.out_p = a.out_p;
+    fp.out_q = a.out_q;
+    fp.B = a.B;
+    fp.V = a.V;
+    fp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
+    fp.draft_stride = a.draft_stride;
+    fp.g = g;
+    const Chunking dc = chunking(a.V, e);
+    fp.NC = GREEDY ? 1 : dc.nchunks;
+    fp.nce = dc.chunk_elems;
+    fp.chunk_smem = (int)align_up((size_t)dc.chunk_elems * e, 128);
+    fp.tma = tma;
+    fp.c = sp.c;
+    fp.status = sp.status;
+    fp.cu_flag = sp.cu_flag;
+    fp.cnt2 = reinterpret_cast<uint32_t *>(ws + L.cnt2);
+    fp.part = sp.part;
+    fp.part2 = reinterpret_cast<double *>(ws + L.part2);
+
+    cudaError_t err = prepare_stream<T, GREEDY>();
+    if (err == cudaSuccess)
+        err = prepare_finish<T, GREEDY>();
+    if (err != cudaSuccess)
+        return err;
+    const int grid1 = (g.P + kStreamWarps - 1) / kStreamWarps;
+    const size_t smem1 = (size_t)kStreamWarps * kRing * sp.piece_smem +
+                         (a.draft_stride > 0 ? 4 * (size_t)(a.B + 1) : 0);
     tr.begin(s);
-    if (greedy)
-        rows_kernel<T, true><<<(unsigned)units, kThreads, smem1, s>>>(p);
-    else
-        rows_kernel<T, false><<<(unsigned)units, kThreads, smem1, s>>>(p);
-    if ((e = cudaGetLastError()) != cudaSuccess)
-        return e;
+    stream_kernel<T, GREEDY><<<grid1, kStreamThreads, smem1, s>>>(sp);
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
     tr.after_kernel(s);
-    if (!greedy) {
-        final_kernel<T><<<(unsigned)(a.B * ch.nchunks), kThreads, 2 * (size_t)p.chunk_smem, s>>>(p);
-        if ((e = cudaGetLastError()) != cudaSuccess)
-            return e;
-        tr.after_kernel(s);
-    }
+
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(a.B * fp.NC));
+    cfg.blockDim = dim3(kFinishThreads);
+    cfg.dynamicSmemBytes = GREEDY ? 0 : 2 * (size_t)fp.chunk_smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, finish_kernel<T, GREEDY>, fp)) != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
     return cudaSuccess;
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
 {
-    return a.dtype == 0 ? launch_typed<float>(a, s, tr) : launch_typed<uint16_t>(a, s, tr);
+    const bool greedy = a.temperature == 0.0;
+    if (a.dtype == 0)
+        return greedy ? launch_typed<float, true>(a, s, tr) : launch_typed<float, false>(a, s, tr);
+    return greedy ? launch_typed<uint16_t, true>(a, s, tr)
+                  : launch_typed<uint16_t, false>(a, s, tr);
 }
 
 }  // namespace sv

@@ -107,7 +107,7 @@ int spec_workspace_init(void *workspace, size_t ws_bytes, spec_stream_t stream);
  * Greedy verification (T = 0).  g_j = lowest index of the maximum of target
  * row j; draft j is accepted iff draft_tokens[j] == g_j; a_i = first mismatch
  * (K_i if none); the final token is g_{a_i} (the bonus row's argmax when every
- * draft is accepted).  Draft logits are not read.  One kernel launch.
+ * draft is accepted).  Draft logits are not read.  Two kernel launches.
  * Pages: greedy acceptance rates "at T = 0" ("Tencent ... AngelSpec ...",
  * bullet list); ties to the lowest index is this library's reading.
  *
@@ -131,7 +131,9 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
  *   final token = smallest v with sum_{v' <= v} w(v') > u_final[i] * sum(w).
  * out_p / out_q (draft index, may be NULL) receive p_j(x_j) and q_j(x_j) for
  * every j < K_i.  temperature == 0 runs spec_verify_greedy (out_p/out_q are
- * then left untouched).  Two kernel launches.
+ * then left untouched).  Two kernel launches: a streaming pass over every
+ * target and draft row, then a per-request pass (accept test, first
+ * rejection, final draw) launched as its programmatic dependent.
  *
  *   draft_logits  [draft rows][V], same dtype as target_logits
  *   u_accept      float [draft index] in [0,1)
