@@ -55,11 +55,11 @@ KERNEL_SOURCES = ["draft_verification_02_b300/csrc/verify.cu",
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mtp")
-    ap.add_argument("--graph-steps", type=int, default=200,
+    ap.add_argument("--graph-steps", type=int, default=500,
                     help="verify steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
@@ -291,6 +291,8 @@ def run_ours(args, dist):
 
     device = torch.device("cuda", dist.local_rank)
     torch.cuda.set_device(device)
+    # the sampler process starts now so that it samples well before the timed region
+    sampler = ClockSampler(device, enabled=not args.no_clocks)
     dist.init("nccl")
     w, T = WORKLOADS[args.workload]
     rows = W.max_target_rows(w)
@@ -397,8 +399,7 @@ def run_ours(args, dist):
 
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(device, enabled=not args.no_clocks)
-    sampler.wait_first_sample()
+    sampler.wait_first_sample(timeout=60.0)
     dist.barrier()
     torch.cuda.synchronize(device)
     t_wall0 = time.time()

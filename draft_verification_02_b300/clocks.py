@@ -38,11 +38,15 @@ def main(argv=None):
     ap.add_argument("--out", required=True)
     ap.add_argument("--max-seconds", type=float, default=600.0)
     a = ap.parse_args(argv)
-    import pynvml
-    pynvml.nvmlInit()
-    h = _handle(pynvml, a.pci)
-    t_end = time.time() + a.max_seconds
     with open(a.out, "w", buffering=1) as f:
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            h = _handle(pynvml, a.pci)
+        except Exception as e:
+            print(f"# nvml unavailable: {e}", file=f)
+            return 1
+        t_end = time.time() + a.max_seconds
         while time.time() < t_end:
             t = time.time()
             try:
@@ -51,7 +55,7 @@ def main(argv=None):
                 pw = pynvml.nvmlDeviceGetPowerUsage(h) / 1000.0
                 rs = pynvml.nvmlDeviceGetCurrentClocksEventReasons(h)
             except Exception as e:  # pragma: no cover
-                print(f"# {e}", file=f)
+                print(f"# nvml query failed: {e}", file=f)
                 break
             f.write(f"{t:.6f} {sm} {smax} {pw:.1f} {int(rs)}\n")
             time.sleep(a.interval_ms / 1000.0)
@@ -61,10 +65,12 @@ def main(argv=None):
 def summarize(path: str, t0: float, t1: float) -> dict:
     """Samples taken inside [t0, t1] (the nearest ones if none fall inside)."""
     rows = []
+    notes = []
     try:
         with open(path) as f:
             for line in f:
                 if line.startswith("#"):
+                    notes.append(line[1:].strip())
                     continue
                 p = line.split()
                 if len(p) == 5:
@@ -72,7 +78,7 @@ def summarize(path: str, t0: float, t1: float) -> dict:
     except FileNotFoundError:
         return {"samples": 0, "error": "no clock samples"}
     if not rows:
-        return {"samples": 0, "error": "no clock samples"}
+        return {"samples": 0, "error": "; ".join(notes) or "no clock samples"}
     inside = [r for r in rows if t0 <= r[0] <= t1]
     note = None
     if not inside:

@@ -609,9 +609,17 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
         const bool live = locate(c_rg, c_q, src, len, col0, nt, nd, true);
         if (issued >> k & 1) {
             if (p.tma) {
-                if (!mbar_wait_bounded(&bars[wib][k], phase >> k & 1)) {
-                    set_status(p.status, ST_TIMEOUT);
-                    mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                const bool ok = mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                if (__any_sync(0xffffffffu, !ok)) {
+                    // a copy never completed: flag it, give every copy still in
+                    // flight one more bounded wait, and stop (the finish kernel
+                    // poisons the outputs when it sees the flag)
+                    if (lane == 0)
+                        set_status(p.status, ST_TIMEOUT);
+                    for (int kk = 0; kk < kRing; ++kk)
+                        if (issued >> kk & 1)
+                            mbar_wait_bounded(&bars[wib][kk], phase >> kk & 1);
+                    return;
                 }
                 phase ^= 1u << k;
             }
@@ -742,7 +750,10 @@ __device__ __forceinline__ int stage_chunk(const FinishParams &p, const T *trow,
 {
     const int col0 = c * p.nce;
     const int len = min(p.nce, p.V - col0);
-    __syncthreads();  // earlier readers of the buffers are done
+    // earlier readers of the buffers are done; once any copy of this call has
+    // timed out, nothing more is copied (the request's outputs are poisoned)
+    if (__syncthreads_or(threadIdx.x == 0 && (read_status(p.status) & ST_TIMEOUT)))
+        return len;
     if (p.tma) {
         if (threadIdx.x == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -754,7 +765,7 @@ __device__ __forceinline__ int stage_chunk(const FinishParams &p, const T *trow,
         }
         if (!mbar_wait_bounded(bar, phase)) {
             set_status(p.status, ST_TIMEOUT);
-            mbar_wait_bounded(bar, phase);
+            mbar_wait_bounded(bar, phase);  // the copy in flight, once more
         }
         phase ^= 1u;
     } else {
@@ -965,11 +976,14 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
             const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
             const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
             const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
+            // bad depends only on the request's data, so every CTA of the
+            // request takes the same branch (and the ticket count stays whole);
+            // an expired wait only poisons outputs (best effort)
+            const bool bad = nf || bt;
             const bool timeout = read_status(p.status) & ST_TIMEOUT;
-            const bool bad = nf || bt || timeout;
             const int a = rej ? __ffs(rej) - 1 : K;
             if (c == 0) {  // the request's outputs, written once
-                if (bad) {
+                if (bad || timeout) {
                     if (lane == 0)
                         set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
                     for (int jj = lane; jj <= K; jj += 32)
@@ -1106,9 +1120,15 @@ __global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishPara
             len = min(p.nce, p.V - cs * p.nce);
         const int k = chunk_search<T>(d, tb, db, len, s_base, s_target, red, &s_res);
         if (tid == 0) {
-            const int y = k >= 0 ? cs * p.nce + k : -1;
+            int y = k >= 0 ? cs * p.nce + k : -1;
             if (y < 0)
                 set_status(p.status, ST_NONFINITE);
+            if (read_status(p.status) & ST_TIMEOUT) {  // staged data may be stale
+                y = -1;
+                p.out_len[i] = -1;
+                for (int jj = 0; jj <= K; ++jj)
+                    p.out_tokens[t0 + jj] = -1;
+            }
             p.out_tokens[trow_i] = y;
         }
     }

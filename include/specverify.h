@@ -55,7 +55,10 @@
  * row with every entry masked, a drafted token outside [0, V), malformed
  * cu_draft, a bounded wait that expired) set a status word inside the
  * workspace and poison the affected outputs (tokens -1, accepted length
- * -1); spec_get_device_status reads and clears that word.
+ * -1); spec_get_device_status reads and clears that word.  A bounded wait
+ * gives up after about two seconds; the kernel then stops copying and
+ * returns, and every output of that call is unspecified (some are poisoned).
+ * After SPEC_ERR_TIMEOUT, zero the workspace again (spec_workspace_init).
  *
  * Workspace
  * ---------

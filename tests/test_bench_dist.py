@@ -1,0 +1,83 @@
+"""The bench's multi-rank host logic on CPU: two gloo ranks, each verifying
+its own independent batches (weak scaling, no data-path collective).  Only
+the timing reductions (barrier, max and sum over ranks) cross ranks."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE=str(world),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import bench
+    from draft_verification_02_b300 import workloads as W
+    d = bench.Dist()
+    d.init("gloo")
+    d.barrier()
+    elapsed = 10.0 + rank  # a rank's own timing
+    mx = d.max(elapsed, "cpu")
+    total = d.sum(48.0 * (rank + 1), "cpu")
+    # each rank draws its own input sets
+    b = W.make_verify_batch(W.TINY, 1.0, "cpu", rep=bench.rank_seed_offset(rank))
+    q.put((rank, mx, total, b.target_logits[0, :4].tolist()))
+    d.barrier()
+    d.close()
+
+
+def test_two_gloo_ranks_reduce_timing_and_draw_independent_inputs():
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = [q.get(timeout=120) for _ in range(world)]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    res.sort()
+    assert all(r[1] == 11.0 for r in res)          # max over ranks
+    assert all(r[2] == 48.0 + 96.0 for r in res)   # sum of units over ranks
+    assert res[0][3] != res[1][3]                  # independent batches per rank
+
+
+def test_reference_arm_other_ranks_exit_without_work(capsys):
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist()
+    d.rank, d.world = 1, 2
+    args = bench.parse_args(["--impl", "reference", "--steps", "1", "--warmup", "0"])
+    bench.run_reference(args, d)
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_line(capsys):
+    import json
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist()
+    args = bench.parse_args(["--impl", "reference", "--workload", "tiny", "--steps", "2",
+                             "--warmup", "1", "--reference-seconds", "2"])
+    bench.run_reference(args, d)
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
