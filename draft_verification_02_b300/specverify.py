@@ -30,7 +30,9 @@ SPEC_DCUT_MAX_CANDIDATES = 8192
 
 EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
-           "spec_status_string", "spec_set_trace", "spec_kernel_launch_count")
+           "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
+           "spec_verify_sample_static")
+SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class SpecError(RuntimeError):
@@ -57,6 +59,9 @@ def _load():
     lib.spec_verify_sample.argtypes = [P, P, INT, P, P, I32, I32, I64, I32, F32, P, P, P, P,
                                        P, P, P, SZ, P]
     lib.spec_verify_sample.restype = INT
+    lib.spec_verify_sample_static.argtypes = [P, P, INT, P, P, I32, I32, I64, I32, F32, P, P,
+                                              P, P, P, P, P]
+    lib.spec_verify_sample_static.restype = INT
     lib.dcut_allocate.argtypes = [P, P, I32, I32, I32, F32, P, P, P, P, SZ, P]
     lib.dcut_allocate.restype = INT
     lib.spec_get_device_status.argtypes = [P, P]
@@ -172,6 +177,36 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, cu_draft, B: i
         _dev(out_p, "out_p", torch.float32, nd, allow_none=True),
         _dev(out_q, "out_q", torch.float32, nd, allow_none=True),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_verify_sample_static(target_logits, draft_logits, draft_tokens, cu_draft, B: int,
+                              V: int, max_target_rows: int, draft_stride: int,
+                              temperature: float, u_accept, u_final, out_tokens,
+                              out_accept_len, out_p, out_q, stream=None) -> int:
+    """spec_verify_sample with the library's fixed scratch array instead of a
+    workspace: for callers that cannot allocate device memory."""
+    if B == 0:
+        return SPEC_OK
+    nd = _draft_extent(B, max_target_rows, draft_stride)
+    code = dtype_code(target_logits)
+    greedy = temperature == 0
+    if not greedy and draft_logits is not None and draft_logits.dtype != target_logits.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    need_draft = (not greedy) and nd > 0
+    return LIB.spec_verify_sample_static(
+        _dev(target_logits, "target_logits", min_numel=max_target_rows * V),
+        _dev(draft_logits, "draft_logits", min_numel=nd * V, allow_none=not need_draft),
+        code,
+        _dev(draft_tokens, "draft_tokens", torch.int32, nd, allow_none=nd == 0),
+        _dev(cu_draft, "cu_draft", torch.int32, B + 1), B, V, max_target_rows, draft_stride,
+        float(temperature),
+        _dev(u_accept, "u_accept", torch.float32, nd, allow_none=not need_draft),
+        _dev(u_final, "u_final", torch.float32, B, allow_none=greedy),
+        _dev(out_tokens, "out_tokens", torch.int32, max_target_rows),
+        _dev(out_accept_len, "out_accept_len", torch.int32, B),
+        _dev(out_p, "out_p", torch.float32, nd, allow_none=True),
+        _dev(out_q, "out_q", torch.float32, nd, allow_none=True),
         _stream(stream))
 
 

@@ -176,6 +176,39 @@ int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kma
                   spec_stream_t stream);
 
 /*
+ * spec_verify_sample without a workspace, for callers that cannot allocate
+ * device memory: an engine whose memory pool already owns all of HBM (for
+ * its KV cache), a plugin whose host runtime forbids allocations outside its
+ * own allocator, or a loop that must not risk the device-wide
+ * synchronisation cudaMalloc can cause.  The pages have no counterpart: this
+ * is a deployment convenience of this library.
+ *
+ * Same arguments, results and kernels as spec_verify_sample (T == 0 runs the
+ * greedy verification), minus workspace/ws_bytes.  The scratch is one
+ * file-scope device array of SPEC_STATIC_SCRATCH_BYTES bytes inside the
+ * library; every GPU that loads the library holds it until the process
+ * exits.  The call allocates nothing: it enqueues a memset of the array's
+ * status word and request tickets, then the two verification kernels.
+ *  - Returns SPEC_ERR_WORKSPACE, with nothing enqueued, when
+ *    spec_workspace_size(B, max_target_rows, V) > SPEC_STATIC_SCRATCH_BYTES.
+ *  - The first call on each device looks up the array's device address
+ *    (with that device current); make that first call before any stream
+ *    capture.
+ *  - Every call on a device shares the one array, and it keeps the previous
+ *    call's contents: calls that may overlap on the GPU (different streams,
+ *    or concurrent host threads) race and must be serialised by the caller.
+ *  - The device status word lives in the array and is cleared by the next
+ *    call; data errors show as poisoned outputs (accepted length -1).
+ */
+#define SPEC_STATIC_SCRATCH_BYTES (1 << 20)
+int spec_verify_sample_static(const void *target_logits, const void *draft_logits, int dtype,
+                              const int32_t *draft_tokens, const int32_t *cu_draft, int32_t B,
+                              int32_t V, int64_t max_target_rows, int32_t draft_stride,
+                              float temperature, const float *u_accept, const float *u_final,
+                              int32_t *out_tokens, int32_t *out_accept_len, float *out_p,
+                              float *out_q, spec_stream_t stream);
+
+/*
  * Synchronise `stream`, then read and clear the workspace status word.
  * Returns SPEC_OK or the device-side error (SPEC_ERR_TIMEOUT before
  * SPEC_ERR_INVALID_ARG before SPEC_ERR_NONFINITE when several are set).
