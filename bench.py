@@ -171,25 +171,30 @@ def l2_bytes(device) -> int:
 def pci_bus_id(device) -> str:
     try:
         p = torch.cuda.get_device_properties(device)
-        return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
     except Exception:
         return ""
 
 
 class ClockSampler:
+    """nvidia-smi sampling SM clocks, power and throttle reasons of this GPU
+    (read-only) from before the timed region until stop()."""
+
     def __init__(self, device, enabled=True):
         self.proc = None
         self.path = None
+        self.file = None
         if not enabled:
             return
+        from draft_verification_02_b300 import clocks
         fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".txt")
-        os.close(fd)
+        self.file = os.fdopen(fd, "w")
         try:
-            self.proc = subprocess.Popen(
-                [sys.executable, "-m", "draft_verification_02_b300.clocks", "--pci",
-                 pci_bus_id(device), "--interval-ms", "5", "--out", self.path],
-                cwd=ROOT, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
-        except Exception:
+            self.proc = subprocess.Popen(clocks.command(pci_bus_id(device), 50),
+                                         stdout=self.file, stderr=subprocess.STDOUT)
+        except OSError as e:
+            self.file.write(f"nvidia-smi unavailable: {e}\n")
+            self.file.flush()
             self.proc = None
 
     def wait_first_sample(self, timeout=5.0):
@@ -209,6 +214,8 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if self.file is not None:
+            self.file.close()
 
     def summary(self, t0, t1):
         if self.path is None:
@@ -495,7 +502,8 @@ def run_ours(args, dist):
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "launch_us_mean": rows_mean},
         "kernels_us": {"stream_kernel": rows_mean,
-                       "finish_kernel": statistics.mean(finish_us),
+                       ("finish_greedy_kernel" if T == 0 else "finish_sample_kernel"):
+                           statistics.mean(finish_us),
                        "dcut_kernel": statistics.mean(dcut_us) if dcut_us else None,
                        "note": "from one traced replay of the step graph after the timed "
                                "region (events between kernels)",

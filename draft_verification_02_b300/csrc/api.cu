@@ -39,7 +39,7 @@ int check_verify_sizes(int32_t B, int32_t V, int64_t max_target_rows, int32_t dr
         return SPEC_ERR_INVALID_ARG;
     if (max_target_rows < B || max_target_rows > (int64_t)B * (SPEC_MAX_DRAFT + 1))
         return SPEC_ERR_INVALID_ARG;
-    if (sv::chunking(V, 4).nchunks > sv::kMaxChunks)
+    if (V > sv::kMaxVocab)
         return SPEC_ERR_INVALID_ARG;
     return SPEC_OK;
 }
@@ -81,7 +81,7 @@ size_t spec_workspace_size(int32_t B, int64_t max_target_rows, int32_t V)
 {
     if (B < 0 || max_target_rows < 0 || V < 0)
         return 0;
-    if (V > 0 && sv::chunking(V, 4).nchunks > sv::kMaxChunks)
+    if (V > sv::kMaxVocab)
         return 0;
     return sv::ws_layout(B, max_target_rows, V).total;
 }

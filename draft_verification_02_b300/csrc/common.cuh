@@ -16,12 +16,7 @@ constexpr int kMaxDraft = 32;  // drafted tokens per request (one warp ballot)
 constexpr int kMaxBatch = 4096;
 constexpr int kDcutMaxCand = 8192;
 
-#ifndef SV_CHUNK_BYTES
-#define SV_CHUNK_BYTES 32768  // bytes of one final-draw chunk staged in shared memory
-#endif
-constexpr int kChunkBytes = SV_CHUNK_BYTES;
-constexpr int kDrawChunkBytes = SV_CHUNK_BYTES;
-constexpr int kMaxChunks = 1024;  // draw chunks per row (bounds V)
+constexpr int kMaxVocab = 1 << 23;  // largest V the calls accept
 #ifndef SV_PIECE_BYTES
 #define SV_PIECE_BYTES 4096  // largest unit of the streaming kernel
 #endif
@@ -40,59 +35,34 @@ enum : uint32_t { ST_INVALID = 1u, ST_NONFINITE = 2u, ST_TIMEOUT = 4u };
 // workspace layout
 // -------------------------------------------------------------------------
 
-// One chunk partial: softmax (m, s) or argmax (m = value, idx = index).
+// One (row, segment) partial: softmax (m, s = s_hi + s_lo, a float-float
+// sum of exp2((x - m) c)) or argmax (m = value, idx = index).
 struct __align__(16) Partial {
     float m;
     int32_t idx;
-    double s;
+    float s_hi;
+    float s_lo;
 };
-
-struct Chunking {
-    int nchunks;
-    int chunk_elems;
-};
-
-// Rows are cut into nearly equal chunks of at most kChunkBytes, each a
-// multiple of 16 bytes long (the TMA bulk-copy granule).
-inline Chunking chunking(int V, int elem_bytes)
-{
-    Chunking c{0, 0};
-    if (V <= 0)
-        return c;
-    const int64_t row_bytes = (int64_t)V * elem_bytes;
-    int n = (int)((row_bytes + kChunkBytes - 1) / kChunkBytes);
-    const int per16 = 16 / elem_bytes;
-    int64_t ce = ((int64_t)V + n - 1) / n;
-    ce = (ce + per16 - 1) / per16 * per16;
-    c.chunk_elems = (int)ce;
-    c.nchunks = (int)(((int64_t)V + ce - 1) / ce);
-    return c;
-}
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: status word (+ offsets-valid flag) | per-request ticket
-// counters | stream partials (one per (row, warp) segment: at most
-// rows + warps) | per-request draw-chunk sums.  Sized for the worst case over
-// both dtypes (fp32 has the most draw chunks).
+// Workspace: status word (+ offsets-valid flag) | stream partials (one per
+// (row, warp) segment: at most rows + warps).  The status word must start at
+// zero; the partials are written before they are read in every call.
 struct WsLayout {
-    size_t status, cnt2, part1, part2, total;
+    size_t status, part1, total;
 };
 
 inline WsLayout ws_layout(int B, int64_t max_rows, int V)
 {
+    (void)V;
     WsLayout L{};
-    const int nch = V > 0 ? chunking(V, 4).nchunks : 0;
     const int64_t rows = max_rows > 0 ? 2 * max_rows - B : 0;
     size_t off = 0;
     L.status = off;
     off += 256;
-    L.cnt2 = off;
-    off = align_up(off + (size_t)B * 4, 256);
     L.part1 = off;
     off = align_up(off + (size_t)(max_rows > 0 ? rows + kMaxWorkers : 0) * sizeof(Partial), 256);
-    L.part2 = off;
-    off = align_up(off + (size_t)B * nch * sizeof(double), 256);
     L.total = off;
     return L;
 }
@@ -156,17 +126,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Wait for phase `phase` of `bar` to complete, giving up after SV_WAIT_NS.
+// Wait for phase `phase` of `bar` to complete, giving up after SV_WAIT_NS
+// (the timer is read once every 64 polls, so a wait that completes soon
+// costs no timer read).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase)
 {
-    if (mbar_try_wait(bar, phase))
-        return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
         if (mbar_try_wait(bar, phase))
             return true;
-        if (globaltimer_ns() - t0 > SV_WAIT_NS)
-            return false;
+        if ((it & 63u) == 63u) {
+            const uint64_t now = globaltimer_ns();
+            if (t0 == 0)
+                t0 = now;
+            else if (now - t0 > SV_WAIT_NS)
+                return false;
+        }
     }
 }
 
@@ -186,14 +161,6 @@ __device__ __forceinline__ float warp_max_nan(float v)
     return v;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-
 // Block-wide NaN-propagating max (kThreads threads, all participate).
 __device__ __forceinline__ float block_max_nan(float v, float *scratch /* [kWarps] */)
 {
@@ -210,20 +177,75 @@ __device__ __forceinline__ float block_max_nan(float v, float *scratch /* [kWarp
     return r;
 }
 
-// Block-wide fp64 sum in a fixed order (deterministic).
-__device__ __forceinline__ double block_sum_d(double v, double *scratch /* [kWarps] */)
+// -------------------------------------------------------------------------
+// float-float arithmetic (no fp64 on the device: B300's fp64 rate is a
+// small fraction of its fp32 rate)
+// -------------------------------------------------------------------------
+
+// A value hi + lo with |lo| <= ulp(hi) / 2.
+struct ff {
+    float hi, lo;
+};
+
+// Exact sum: s + e == a + b (Knuth's TwoSum).  The pair is the exact
+// rounding of a + b, so it does not depend on the order of a and b.
+__device__ __forceinline__ ff two_sum(float a, float b)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    v = warp_sum_d(v);
-    __syncthreads();
-    if (lane == 0)
-        scratch[warp] = v;
-    __syncthreads();
-    double r = 0.0;
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return {s, e};
+}
+
+// (a + b) renormalised, given |a| >= |b| or a == 0.
+__device__ __forceinline__ ff fast_two_sum(float a, float b)
+{
+    const float s = __fadd_rn(a, b);
+    return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+// Sum of two float-float values; ff_add(a, b) and ff_add(b, a) give the same
+// bits.
+__device__ __forceinline__ ff ff_add(ff a, ff b)
+{
+    const ff s = two_sum(a.hi, b.hi);
+    const float lo = __fadd_rn(__fadd_rn(a.lo, b.lo), s.lo);
+    return fast_two_sum(s.hi, lo);
+}
+
+// Product of a float-float value and a float.
+__device__ __forceinline__ ff ff_mul(ff a, float f)
+{
+    const float p = __fmul_rn(a.hi, f);
+    const float e = fmaf(a.hi, f, -p);
+    return fast_two_sum(p, fmaf(a.lo, f, e));
+}
+
+__device__ __forceinline__ bool ff_gt(ff a, ff b)
+{
+    return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo);
+}
+
+__device__ __forceinline__ bool ff_le(ff a, ff b) { return !ff_gt(a, b); }
+
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int o)
+{
+    return {__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o)
+{
+    return {__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+
+// Warp sum; every lane gets the same bits (each butterfly step adds the same
+// two values in either order).
+__device__ __forceinline__ ff warp_sum_ff(ff v)
+{
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w)
-        r += scratch[w];
-    return r;
+    for (int o = 16; o > 0; o >>= 1)
+        v = ff_add(v, ff_shfl_xor(v, o));
+    return v;
 }
 
 // Element access for the two logit dtypes.

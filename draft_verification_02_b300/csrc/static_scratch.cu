@@ -81,8 +81,8 @@ extern "C" int spec_verify_sample_static(const void *target_logits, const void *
     void *scratch = nullptr;
     if (scratch_address(&scratch) != cudaSuccess)
         return SPEC_ERR_CUDA;
-    // The array keeps the previous call's contents.  Its status word and
-    // per-request tickets must start at zero; the partials need no clearing.
+    // The array keeps the previous call's contents.  Its status word must
+    // start at zero; the partials are written before they are read.
     const size_t header = sv::ws_layout(B, max_target_rows, V).part1;
     if (cudaMemsetAsync(scratch, 0, header, (cudaStream_t)stream) != cudaSuccess)
         return SPEC_ERR_CUDA;

@@ -27,12 +27,18 @@
 // of m*c is corrected exactly once per unit); T = 0 keeps the lowest index of
 // the maximum.  No fp64 on this path (B300's fp64 rate is a small fraction of
 // its fp32 rate).  Every (row, warp) segment leaves one partial.
-// Kernel 2, finish_kernel: one CTA per (request, draw chunk), launched as a
-// programmatic dependent of kernel 1 so its launch overlaps kernel 1's tail.
-// Each CTA merges its request's partials in a fixed order (identical in every
-// CTA of the request), runs the accept test and the first-rejection ballot,
-// then sums the final-draw weights of its chunk; the request's last CTA
-// (atomic ticket) picks the chunk holding u*S and scans inside it.
+// Kernel 2, launched as a programmatic dependent of kernel 1: it reads the
+// inputs that do not depend on kernel 1 (offsets, drafted tokens, uniforms,
+// the logits at the drafted tokens) before waiting for kernel 1 to finish.
+//  - T = 0, finish_greedy_kernel: one CTA per request merges the argmax
+//    partials and runs the first-mismatch ballot.
+//  - T > 0, finish_sample_kernel: one cluster of kCluster CTAs per request.
+//    Every CTA merges the request's (m, s) partials and runs the accept test
+//    and first-rejection ballot (identical bits in every CTA), then stages
+//    its 1/kCluster of the final-draw rows with TMA and sums the weights.
+//    The range sums are exchanged through distributed shared memory; the
+//    CTA whose range holds u*S finds the token with a block scan of
+//    per-thread piece sums and one thread's walk through its piece.
 // Every merge runs in a fixed order, so repeated calls give identical bits.
 #include <algorithm>
 #include <cfloat>
@@ -89,16 +95,15 @@ struct FinishParams {
     int64_t draft_rows;  // rows the draft side may index
     int draft_stride;
     Geometry g;
-    int NC;          // draw chunks per row
-    int nce;         // elements per draw chunk
-    int chunk_smem;  // bytes per staged draw chunk (multiple of 128)
+    int R;           // vocabulary entries per cluster CTA in the final draw
+    int slice;       // entries of one row staged at a time (multiple of 16 bytes)
+    int pv;          // 16-byte vectors per thread piece of a slice (odd)
+    int stage_smem;  // bytes per staged row slice (multiple of 128)
     int tma;
     float c;
     uint32_t *status;
     const uint32_t *cu_flag;
-    uint32_t *cnt2;
     const Partial *part;
-    double *part2;
 };
 
 // ---------------------------------------------------------------------------
@@ -149,23 +154,11 @@ __device__ __forceinline__ float mc_correction(float m, float mc, float c)
     return fmaf(delta, 0.69314718f, 1.0f);
 }
 
-// 2^x for x <= 0 given in fp64: split x = n + f exactly (n integer, f in
-// [0,1)), take 2^f with CUDA's exp2f (2 ulp) and scale by 2^n.  A handful of
-// fp64 operations instead of a full fp64 exp2.
-__device__ __forceinline__ float exp2_split(double x)
-{
-    if (x < -200.0)
-        return 0.f;
-    const double n = floor(x);
-    return ldexpf(exp2f((float)(x - n)), (int)n);
-}
-
 __device__ __forceinline__ int64_t draft_index(int draft_stride, const int32_t *cu, int i, int j)
 {
     return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)__ldg(cu + i) + j;
 }
 
-__device__ __forceinline__ double qnan_d() { return __longlong_as_double(0x7ff8000000000000ll); }
 
 // ---------------------------------------------------------------------------
 // kernel 1: stream the rows
@@ -221,50 +214,108 @@ __device__ __forceinline__ void add_unit(LaneAcc &a, float unit_sum, float mc, f
     a.s = t;
 }
 
-// One unit of bf16 data at T > 0 from shared memory (lane-strided 16-byte
-// vectors held in registers between the max and the sum); a tail that is not
-// a whole vector (plain-load path only) is handled element-wise.
+// Units are read from shared memory as lane-strided 16-byte vectors held in
+// registers; vectors past the unit's end read as -inf, which neither the
+// maximum nor the sum of exp2 sees.  Maxima and sums are trees (short
+// dependency chains), not running chains.  A tail that is not a whole vector
+// (plain-load path only) is handled element by element.
+constexpr uint32_t kNegInfBf16x2 = 0xff80ff80u;
+
+template <int MAXV>
+__device__ __forceinline__ void load_unit_bf16(const uint16_t *buf, int nvec, uint4 (&r)[MAXV])
+{
+    const int lane = threadIdx.x & 31;
+    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        r[t] = v < nvec ? vb[v] : make_uint4(kNegInfBf16x2, kNegInfBf16x2, kNegInfBf16x2,
+                                             kNegInfBf16x2);
+    }
+}
+
+template <int MAXV>
+__device__ __forceinline__ void load_unit_f32(const float *buf, int nvec, float4 (&r)[MAXV])
+{
+    const int lane = threadIdx.x & 31;
+    const float4 *vb = reinterpret_cast<const float4 *>(buf);
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t) {
+        const int v = lane + 32 * t;
+        r[t] = v < nvec ? vb[v] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+    }
+}
+
+// Tree maximum of a unit held in registers (NaN-propagating).
+template <int MAXV>
+__device__ __forceinline__ float unit_max_bf16(const uint4 (&r)[MAXV])
+{
+    uint32_t mx[MAXV];
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t)
+        mx[t] = max_nan_bf16x2(max_nan_bf16x2(r[t].x, r[t].y), max_nan_bf16x2(r[t].z, r[t].w));
+#pragma unroll
+    for (int w = MAXV / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int t = 0; t < w; ++t)
+            mx[t] = max_nan_bf16x2(mx[t], mx[t + w]);
+    return max_nan(bf16_lo(mx[0]), bf16_hi(mx[0]));
+}
+
+template <int MAXV>
+__device__ __forceinline__ float unit_max_f32(const float4 (&r)[MAXV])
+{
+    float mx[MAXV];
+#pragma unroll
+    for (int t = 0; t < MAXV; ++t)
+        mx[t] = max_nan(max_nan(r[t].x, r[t].y), max_nan(r[t].z, r[t].w));
+#pragma unroll
+    for (int w = MAXV / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int t = 0; t < w; ++t)
+            mx[t] = max_nan(mx[t], mx[t + w]);
+    return mx[0];
+}
+
+template <int MAXV>
+__device__ __forceinline__ float tree_sum(float (&v)[MAXV])
+{
+#pragma unroll
+    for (int w = MAXV / 2; w >= 1; w /= 2)
+#pragma unroll
+        for (int t = 0; t < w; ++t)
+            v[t] += v[t + w];
+    return v[0];
+}
+
+// One unit of bf16 data at T > 0.
 template <int MAXV>
 __device__ __forceinline__ void unit_softmax_bf16(const uint16_t *buf, int len, float c,
                                                   LaneAcc &a)
 {
     const int lane = threadIdx.x & 31;
-    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
     const int nvec = len >> 3;
     uint4 r[MAXV];
-    uint32_t hm = 0xff80ff80u;  // (-inf, -inf)
-#pragma unroll
-    for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            r[t] = vb[v];
-            hm = max_nan_bf16x2(hm, r[t].x);
-            hm = max_nan_bf16x2(hm, r[t].y);
-            hm = max_nan_bf16x2(hm, r[t].z);
-            hm = max_nan_bf16x2(hm, r[t].w);
-        }
-    }
-    float pm = max_nan(bf16_lo(hm), bf16_hi(hm));
+    load_unit_bf16<MAXV>(buf, nvec, r);
+    float pm = unit_max_bf16<MAXV>(r);
     for (int k = nvec * 8 + lane; k < len; k += 32)
         pm = max_nan(pm, bf16_lo((uint32_t)buf[k]));
     if (!fold_max(a, pm, c))
         return;
     const float mc = a.m * c;
-    float acc = 0.f;
+    float sv[MAXV];
 #pragma unroll
     for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
-            float e[8];
+        const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
+        float e[8];
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                e[2 * h] = ex2_approx(fmaf(bf16_lo(w4[h]), c, -mc));
-                e[2 * h + 1] = ex2_approx(fmaf(bf16_hi(w4[h]), c, -mc));
-            }
-            acc += ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
+        for (int h = 0; h < 4; ++h) {
+            e[2 * h] = ex2_approx(fmaf(bf16_lo(w4[h]), c, -mc));
+            e[2 * h + 1] = ex2_approx(fmaf(bf16_hi(w4[h]), c, -mc));
         }
+        sv[t] = ((e[0] + e[1]) + (e[2] + e[3])) + ((e[4] + e[5]) + (e[6] + e[7]));
     }
+    float acc = tree_sum<MAXV>(sv);
     for (int k = nvec * 8 + lane; k < len; k += 32)
         acc += ex2_approx(fmaf(bf16_lo((uint32_t)buf[k]), c, -mc));
     add_unit(a, acc, mc, c);
@@ -274,92 +325,71 @@ template <int MAXV>
 __device__ __forceinline__ void unit_softmax_f32(const float *buf, int len, float c, LaneAcc &a)
 {
     const int lane = threadIdx.x & 31;
-    const float4 *vb = reinterpret_cast<const float4 *>(buf);
     const int nvec = len >> 2;
     float4 r[MAXV];
-    float pm = -INFINITY;
-#pragma unroll
-    for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            r[t] = vb[v];
-            pm = max_nan(pm, max_nan(max_nan(r[t].x, r[t].y), max_nan(r[t].z, r[t].w)));
-        }
-    }
+    load_unit_f32<MAXV>(buf, nvec, r);
+    float pm = unit_max_f32<MAXV>(r);
     for (int k = nvec * 4 + lane; k < len; k += 32)
         pm = max_nan(pm, buf[k]);
     if (!fold_max(a, pm, c))
         return;
     const float mc = a.m * c;
-    float acc = 0.f;
+    float sv[MAXV];
 #pragma unroll
     for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            const float e0 = ex2_approx(fmaf(r[t].x, c, -mc));
-            const float e1 = ex2_approx(fmaf(r[t].y, c, -mc));
-            const float e2 = ex2_approx(fmaf(r[t].z, c, -mc));
-            const float e3 = ex2_approx(fmaf(r[t].w, c, -mc));
-            acc += (e0 + e1) + (e2 + e3);
-        }
+        const float e0 = ex2_approx(fmaf(r[t].x, c, -mc));
+        const float e1 = ex2_approx(fmaf(r[t].y, c, -mc));
+        const float e2 = ex2_approx(fmaf(r[t].z, c, -mc));
+        const float e3 = ex2_approx(fmaf(r[t].w, c, -mc));
+        sv[t] = (e0 + e1) + (e2 + e3);
     }
+    float acc = tree_sum<MAXV>(sv);
     for (int k = nvec * 4 + lane; k < len; k += 32)
         acc += ex2_approx(fmaf(buf[k], c, -mc));
     add_unit(a, acc, mc, c);
 }
 
-// T = 0: lowest index of the maximum.  Each lane visits its elements in
-// increasing index order, so a strict > keeps the lowest index.
+// T = 0: the warp keeps one running (maximum, lowest index) pair, the same in
+// every lane.  A unit costs a tree maximum and a warp maximum; only when the
+// warp maximum grows does each lane look for its first element equal to it
+// (its elements in increasing index order) and the warp take the lowest.
+// Earlier units hold lower indices, so a strict > keeps the lowest index.
 template <int MAXV>
 __device__ __forceinline__ void unit_argmax_bf16(const uint16_t *buf, int len, int col0,
                                                  LaneAcc &a)
 {
     const int lane = threadIdx.x & 31;
-    const uint4 *vb = reinterpret_cast<const uint4 *>(buf);
     const int nvec = len >> 3;
     uint4 r[MAXV];
-    uint32_t hm = 0xff80ff80u;
-#pragma unroll
-    for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            r[t] = vb[v];
-            hm = max_nan_bf16x2(hm, r[t].x);
-            hm = max_nan_bf16x2(hm, r[t].y);
-            hm = max_nan_bf16x2(hm, r[t].z);
-            hm = max_nan_bf16x2(hm, r[t].w);
-        }
-    }
-    const float pm = max_nan(bf16_lo(hm), bf16_hi(hm));
-    if (pm != pm) {
+    load_unit_bf16<MAXV>(buf, nvec, r);
+    float pm = unit_max_bf16<MAXV>(r);
+    for (int k = nvec * 8 + lane; k < len; k += 32)
+        pm = max_nan(pm, bf16_lo((uint32_t)buf[k]));
+    const float wm = warp_max_nan(pm);
+    if (wm != wm) {
         a.nan = 1;
-    } else if (pm > a.m) {  // locate the first element equal to the new maximum
+    } else if (wm > a.m) {
         int found = INT_MAX;
 #pragma unroll
         for (int t = 0; t < MAXV; ++t) {
-            const int v = lane + 32 * t;
-            if (v < nvec && found == INT_MAX) {
-                const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
+            const uint32_t w4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    if (found == INT_MAX && bf16_lo(w4[h]) == pm)
-                        found = v * 8 + 2 * h;
-                    if (found == INT_MAX && bf16_hi(w4[h]) == pm)
-                        found = v * 8 + 2 * h + 1;
-                }
+            for (int h = 0; h < 4; ++h) {
+                const int k = (lane + 32 * t) * 8 + 2 * h;
+                if (found == INT_MAX && bf16_lo(w4[h]) == wm)
+                    found = k;
+                if (found == INT_MAX && bf16_hi(w4[h]) == wm)
+                    found = k + 1;
             }
         }
-        a.m = pm;
+        for (int k = nvec * 8 + lane; k < len && found == INT_MAX; k += 32)
+            if (bf16_lo((uint32_t)buf[k]) == wm)
+                found = k;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+        a.m = wm;
         a.idx = col0 + found;
-    }
-    for (int k = nvec * 8 + lane; k < len; k += 32) {  // tail (plain path), in order
-        const float x = bf16_lo((uint32_t)buf[k]);
-        if (x != x)
-            a.nan = 1;
-        else if (x > a.m) {
-            a.m = x;
-            a.idx = col0 + k;
-        }
     }
 }
 
@@ -367,33 +397,33 @@ template <int MAXV>
 __device__ __forceinline__ void unit_argmax_f32(const float *buf, int len, int col0, LaneAcc &a)
 {
     const int lane = threadIdx.x & 31;
-    const float4 *vb = reinterpret_cast<const float4 *>(buf);
     const int nvec = len >> 2;
+    float4 r[MAXV];
+    load_unit_f32<MAXV>(buf, nvec, r);
+    float pm = unit_max_f32<MAXV>(r);
+    for (int k = nvec * 4 + lane; k < len; k += 32)
+        pm = max_nan(pm, buf[k]);
+    const float wm = warp_max_nan(pm);
+    if (wm != wm) {
+        a.nan = 1;
+    } else if (wm > a.m) {
+        int found = INT_MAX;
 #pragma unroll
-    for (int t = 0; t < MAXV; ++t) {
-        const int v = lane + 32 * t;
-        if (v < nvec) {
-            const float4 q = vb[v];
-            const float x4[4] = {q.x, q.y, q.z, q.w};
+        for (int t = 0; t < MAXV; ++t) {
+            const float x4[4] = {r[t].x, r[t].y, r[t].z, r[t].w};
 #pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                if (x4[h] != x4[h])
-                    a.nan = 1;
-                else if (x4[h] > a.m) {
-                    a.m = x4[h];
-                    a.idx = col0 + v * 4 + h;
-                }
-            }
+            for (int h = 0; h < 4; ++h)
+                if (found == INT_MAX && x4[h] == wm)
+                    found = (lane + 32 * t) * 4 + h;
         }
-    }
-    for (int k = nvec * 4 + lane; k < len; k += 32) {
-        const float x = buf[k];
-        if (x != x)
-            a.nan = 1;
-        else if (x > a.m) {
-            a.m = x;
-            a.idx = col0 + k;
-        }
+        for (int k = nvec * 4 + lane; k < len && found == INT_MAX; k += 32)
+            if (buf[k] == wm)
+                found = k;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            found = min(found, __shfl_xor_sync(0xffffffffu, found, o));
+        a.m = wm;
+        a.idx = col0 + found;
     }
 }
 
@@ -404,35 +434,25 @@ __device__ __forceinline__ void store_partial(LaneAcc &a, float c, Partial *slot
 {
     const int lane = threadIdx.x & 31;
     Partial out;
-    if (GREEDY) {
-        float best = a.m;
-        int bidx = a.idx;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
-            if (ob > best || (ob == best && oi < bidx)) {
-                best = ob;
-                bidx = oi;
-            }
-        }
-        const int nan = __any_sync(0xffffffffu, a.nan);
-        out.m = best;
-        out.idx = nan ? -2 : (bidx == INT_MAX ? -1 : bidx);
-        out.s = 0.0;
+    if (GREEDY) {  // the running (maximum, index) is already the same in every lane
+        out.m = a.m;
+        out.idx = a.nan ? -2 : (a.idx == INT_MAX ? -1 : a.idx);
+        out.s_hi = 0.f;
+        out.s_lo = 0.f;
     } else {
         const float m = warp_max_nan(a.m);
-        double s = 0.0;
+        ff s{0.f, 0.f};
         if (m == m && m != -INFINITY && m != INFINITY) {
-            if (a.s != 0.f)
-                s = (double)(a.s - a.comp) * (double)exp2f((a.m - m) * c);
+            if (a.s != 0.f)  // the Kahan pair (s, -comp) rescaled to the warp maximum
+                s = ff_mul(fast_two_sum(a.s, -a.comp), exp2f((a.m - m) * c));
         } else if (m != -INFINITY) {
-            s = qnan_d();
+            s.hi = __int_as_float(0x7fc00000);
         }
-        s = warp_sum_d(s);
+        s = warp_sum_ff(s);
         out.m = m;
         out.idx = 0;
-        out.s = s;
+        out.s_hi = s.hi;
+        out.s_lo = s.lo;
     }
     if (lane == 0)
         *slot = out;
@@ -667,46 +687,151 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
 
 constexpr int kFinishThreads = 256;
 constexpr int kFinishWarps = kFinishThreads / 32;
+constexpr int kCluster = 8;                // CTAs per request in the sampling finish kernel
+constexpr int kStageRowBytes = 48 * 1024;  // largest slice of one row staged at a time
+constexpr int kMaxSlices = 96;             // slices per CTA range (bounds V)
+constexpr int kRowsPerWarp = (2 * kMaxDraft + 1 + kFinishWarps - 1) / kFinishWarps;
 
-// Merge the partials of flattened row rg (one warp), T > 0: (m, s) with
-// s = sum_v exp2((x_v - m) c).
-__device__ __forceinline__ void merge_softmax_row(const FinishParams &p, int64_t rg, float &m_out,
-                                                  double &s_out)
+__device__ __forceinline__ uint32_t cluster_ctarank()
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t ua = rg * p.g.cpr, ub = ua + p.g.cpr - 1;
-    const int wf = owner_of(ua, p.g), wl = owner_of(ub, p.g);
-    float m = -INFINITY;
-    for (int w = wf + lane; w <= wl; w += 32)
-        m = max_nan(m, __ldcg(&p.part[rg + w].m));
-    m = warp_max_nan(m);
-    double s = 0.0;
-    for (int w = wf + lane; w <= wl; w += 32) {
-        const double sw = __ldcg(&p.part[rg + w].s);
-        if (sw != 0.0)
-            s += sw * (double)exp2f((__ldcg(&p.part[rg + w].m) - m) * p.c);
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the address `local` has in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_ff(ff *local, uint32_t rank, ff v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.hi), "f"(v.lo)
+                 : "memory");
+}
+
+// One partial, read from L2 in a single 16-byte load.
+__device__ __forceinline__ Partial load_partial(const Partial *p)
+{
+    const uint4 r = __ldcg(reinterpret_cast<const uint4 *>(p));
+    Partial out;
+    out.m = __uint_as_float(r.x);
+    out.idx = (int32_t)r.y;
+    out.s_hi = __uint_as_float(r.z);
+    out.s_lo = __uint_as_float(r.w);
+    return out;
+}
+
+// Combine two softmax partials (m, s), s = sum exp2((x - m) c) held as a
+// float-float pair.  The result does not depend on the order of the two
+// arguments, so a butterfly over a warp leaves the same bits in every lane.
+__device__ __forceinline__ void lse_combine(float &m, ff &s, float mo, ff so, float c)
+{
+    if (so.hi == 0.f)
+        return;  // empty or fully masked partial
+    if (s.hi == 0.f) {
+        m = mo;
+        s = so;
+        return;
     }
-    s = warp_sum_d(s);
-    m_out = m;
-    s_out = s;
+    const float mn = max_nan(m, mo);
+    if (mn != mn || s.hi != s.hi || so.hi != so.hi) {
+        m = __int_as_float(0x7fc00000);
+        s = {__int_as_float(0x7fc00000), 0.f};
+        return;
+    }
+    s = ff_add(ff_mul(s, exp2f((m - mn) * c)), ff_mul(so, exp2f((mo - mn) * c)));
+    m = mn;
+}
+
+__device__ __forceinline__ void row_span(const Geometry &g, int64_t rg, int &wf, int &wl)
+{
+    const int64_t ua = rg * g.cpr;
+    wf = owner_of(ua, g);
+    wl = owner_of(ua + g.cpr - 1, g);
+}
+
+// Merge the partials of up to kRowsPerWarp flattened rows per warp, all
+// loads issued before any is used.  rows(k) gives the k-th row of the
+// request (k < n); warp w takes k = w, w + kFinishWarps, ...  Results go to
+// row_m / row_s (lane 0).
+template <typename RowOf>
+__device__ __forceinline__ void merge_softmax_rows(const Partial *part, const Geometry &g, int n,
+                                                   RowOf rows, float c, float *row_m,
+                                                   ff *row_s)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    Partial first[kRowsPerWarp];
+#pragma unroll
+    for (int t = 0; t < kRowsPerWarp; ++t) {
+        const int k = warp + t * kFinishWarps;
+        first[t].m = -INFINITY;
+        first[t].s_hi = 0.f;
+        first[t].s_lo = 0.f;
+        if (k < n) {
+            const int64_t rg = rows(k);
+            int wf, wl;
+            row_span(g, rg, wf, wl);
+            if (wf + lane <= wl)
+                first[t] = load_partial(part + rg + wf + lane);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kRowsPerWarp; ++t) {
+        const int k = warp + t * kFinishWarps;
+        if (k >= n)
+            break;
+        float m = -INFINITY;
+        ff s{0.f, 0.f};
+        lse_combine(m, s, first[t].m, {first[t].s_hi, first[t].s_lo}, c);
+        const int64_t rg = rows(k);
+        int wf, wl;
+        row_span(g, rg, wf, wl);
+        for (int w = wf + lane + 32; w <= wl; w += 32) {  // rows split over more than 32 warps
+            const Partial q = load_partial(part + rg + w);
+            lse_combine(m, s, q.m, {q.s_hi, q.s_lo}, c);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+            const ff so = ff_shfl_xor(s, o);
+            lse_combine(m, s, mo, so, c);
+        }
+        if (lane == 0) {
+            row_m[k] = m;
+            row_s[k] = s;
+        }
+    }
 }
 
 // T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
-__device__ __forceinline__ int merge_argmax_row(const FinishParams &p, int64_t rg)
+__device__ __forceinline__ int merge_argmax_row(const Partial *part, const Geometry &g, int64_t rg)
 {
     const int lane = threadIdx.x & 31;
-    const int64_t ua = rg * p.g.cpr, ub = ua + p.g.cpr - 1;
-    const int wf = owner_of(ua, p.g), wl = owner_of(ub, p.g);
+    int wf, wl;
+    row_span(g, rg, wf, wl);
     float best = -INFINITY;
     int bidx = INT_MAX, nan = 0;
     for (int w = wf + lane; w <= wl; w += 32) {
-        const float m = __ldcg(&p.part[rg + w].m);
-        const int ix = __ldcg(&p.part[rg + w].idx);
-        if (ix == -2)
+        const Partial q = load_partial(part + rg + w);
+        if (q.idx == -2)
             nan = 1;
-        else if (ix >= 0 && (m > best || (m == best && ix < bidx))) {
-            best = m;
-            bidx = ix;
+        else if (q.idx >= 0 && (q.m > best || (q.m == best && q.idx < bidx))) {
+            best = q.m;
+            bidx = q.idx;
         }
     }
 #pragma unroll
@@ -722,9 +847,90 @@ __device__ __forceinline__ int merge_argmax_row(const FinishParams &p, int64_t r
     return nan ? -2 : (bidx == INT_MAX ? -1 : (best == INFINITY ? -3 : bidx));
 }
 
-__device__ __forceinline__ bool row_ok(float m, double s)
+__device__ __forceinline__ bool row_ok(float m, ff s)
 {
-    return isfinite(m) && isfinite(s) && s > 0.0;
+    return isfinite(m) && isfinite(s.hi) && s.hi > 0.f;
+}
+
+// p(x) = 2^((g - m) c) / s for one row given its (m, s): g - m exactly as a
+// float-float pair, its product with c to float-float, 2^hi with exp2f and
+// the low part to first order, then the division by s.
+__device__ __forceinline__ float softmax_at(float g, float m, ff s, float c)
+{
+    if (g == -INFINITY)
+        return 0.f;  // a masked entry
+    const ff d = two_sum(g, -m);
+    const float xh = __fmul_rn(d.hi, c);
+    const float xl = fmaf(d.lo, c, fmaf(d.hi, c, -xh));
+    const float num = __fmul_rn(exp2f(xh), fmaf(xl, 0.69314718f, 1.f));
+    const float inv = __fdiv_rn(1.f, s.hi);
+    return __fmul_rn(__fmul_rn(num, inv), fmaf(-s.lo, inv, 1.f));
+}
+
+// Request i's offsets checked locally, before the streaming kernel's own
+// validation is visible: only then are its token / logit addresses formed.
+__device__ __forceinline__ bool request_shape_ok(const FinishParams &p, int i, int cu_i, int K)
+{
+    const int64_t t0 = (int64_t)cu_i + i;
+    return cu_i >= 0 && K >= 0 && K <= kMaxDraft && t0 + K < p.g.max_rows &&
+           (p.draft_stride > 0 ? K <= p.draft_stride : (int64_t)cu_i + K <= p.draft_rows);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const FinishParams p)
+{
+    __shared__ int row_g[kMaxDraft + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i = blockIdx.x;
+
+    // inputs that do not depend on kernel 1 are read before waiting for it
+    const int cu_i = __ldg(p.cu + i);
+    const int K = __ldg(p.cu + i + 1) - cu_i;
+    const bool shape = request_shape_ok(p, i, cu_i, K);
+    const bool act = shape && warp == 0 && lane < K;
+    const int x = act ? __ldg(p.tokens + draft_index(p.draft_stride, p.cu, i, lane)) : -1;
+
+    pdl_wait();  // kernel 1 has completed and its writes are visible
+    if (__ldcg(p.cu_flag) == 0u || !shape)
+        return;  // malformed offsets: kernel 1 poisoned every output
+    const int64_t t0 = (int64_t)cu_i + i;
+    for (int rho = warp; rho <= K; rho += kFinishWarps) {
+        const int gj = merge_argmax_row(p.part, p.g, t0 + rho);
+        if (lane == 0)
+            row_g[rho] = gj;
+    }
+    __syncthreads();
+    if (warp != 0)
+        return;
+    const bool bad_tok = act && (x < 0 || x >= p.V);
+    bool bad_nf = false;
+    for (int jj = lane; jj <= K; jj += 32)
+        bad_nf |= row_g[jj] < 0;
+    const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
+    const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
+    const unsigned rej = __ballot_sync(0xffffffffu, act && x != row_g[act ? lane : 0]);
+    const bool timeout = read_status(p.status) & ST_TIMEOUT;
+    if (nf || bt || timeout) {
+        if (lane == 0)
+            set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+        for (int jj = lane; jj <= K; jj += 32)
+            p.out_tokens[t0 + jj] = -1;
+        if (lane == 0)
+            p.out_len[i] = -1;
+        return;
+    }
+    const int a = rej ? __ffs(rej) - 1 : K;
+    for (int jj = lane; jj <= K; jj += 32)
+        p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
+    if (lane == 0)
+        p.out_len[i] = a;
+}
+
+// f / s for a float-float s.
+__device__ __forceinline__ float ff_recip_scaled(float f, ff s)
+{
+    const float inv = __fdiv_rn(1.f, s.hi);
+    return __fmul_rn(__fmul_rn(f, inv), fmaf(-s.lo, inv, 1.f));
 }
 
 struct DrawCtx {
@@ -733,27 +939,64 @@ struct DrawCtx {
     float sc_t, sc_d;   // 2^(fl(m c) - m c) / s: normalisers including the rounding fix
 };
 
-// Final-draw weight of one element (pair).
+// Final-draw weight of one element.  Every operation is explicitly rounded,
+// so the summing pass and the search pass compute identical bits.
 __device__ __forceinline__ float draw_w(const DrawCtx &d, float t, float x)
 {
     const float pt = ex2_approx(fmaf(t, d.c, -d.mct));
     if (!d.resid)
         return pt;  // bonus draw (or all-zero residual): unnormalised p
     const float pd = ex2_approx(fmaf(x, d.c, -d.mcd));
-    return fmaxf(pt * d.sc_t - pd * d.sc_d, 0.f);
+    return fmaxf(__fsub_rn(__fmul_rn(pt, d.sc_t), __fmul_rn(pd, d.sc_d)), 0.f);
 }
 
+// Walk one thread's contiguous piece (16-byte vectors [v0, v1) of a staged
+// slice of len elements) in index order, summing the weights in fp32.  With
+// rem finite, stop at the first element whose running sum exceeds rem and
+// return its index in the slice (-1 if none); *sum gets the running sum.
 template <typename T>
-__device__ __forceinline__ int stage_chunk(const FinishParams &p, const T *trow, const T *drow,
-                                           bool resid, int c, T *tb, T *db, uint64_t *bar,
-                                           uint32_t &phase)
+__device__ __forceinline__ int walk_piece(const DrawCtx &d, const T *tb, const T *db, int len,
+                                          int v0, int v1, float rem, float *sum, int *last_pos)
 {
-    const int col0 = c * p.nce;
-    const int len = min(p.nce, p.V - col0);
-    // earlier readers of the buffers are done; once any copy of this call has
-    // timed out, nothing more is copied (the request's outputs are poisoned)
-    if (__syncthreads_or(threadIdx.x == 0 && (read_status(p.status) & ST_TIMEOUT)))
-        return len;
+    constexpr int E = Elem<T>::kPerVec;
+    const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(db);
+    float acc = 0.f;
+    int lastp = -1;
+    for (int v = v0; v < v1; ++v) {
+        float ft[E], fd[E];
+        Elem<T>::unpack(tv[v], ft);
+        if (d.resid)
+            Elem<T>::unpack(dv[v], fd);
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+            const int k = v * E + h;
+            const float w = k < len ? draw_w(d, ft[h], d.resid ? fd[h] : 0.f) : 0.f;
+            acc = __fadd_rn(acc, w);
+            if (w > 0.f)
+                lastp = k;
+            if (acc > rem) {
+                *sum = acc;
+                *last_pos = lastp;
+                return k;
+            }
+        }
+    }
+    *sum = acc;
+    *last_pos = lastp;
+    return -1;
+}
+
+// Stage elements [col0, col0 + len) of the draw rows into shared memory.
+// Once any copy of this call has timed out, nothing more is copied (the
+// request's outputs are poisoned).
+template <typename T>
+__device__ __forceinline__ void stage_slice(const FinishParams &p, const T *trow, const T *drow,
+                                            bool resid, int col0, int len, T *tb, T *db,
+                                            uint64_t *bar, uint32_t &phase)
+{
+    if (__syncthreads_or(threadIdx.x == 0 && (read_status(p.status) & ST_TIMEOUT)) || len <= 0)
+        return;
     if (p.tma) {
         if (threadIdx.x == 0) {
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -776,361 +1019,347 @@ __device__ __forceinline__ int stage_chunk(const FinishParams &p, const T *trow,
         }
         __syncthreads();
     }
-    return len;
 }
 
+// Sum of the draw weights of a staged slice: every thread sums its
+// contiguous piece (kept in piece[] for the search), then the pieces are
+// added in fp64 in a fixed order.
 template <typename T>
-__device__ __forceinline__ float draw_at(const DrawCtx &d, const T *tb, const T *db, int k)
+__device__ __forceinline__ ff slice_sum(const DrawCtx &d, const T *tb, const T *db, int len,
+                                        int pv, float *piece, ff *wred)
 {
-    return draw_w(d, Elem<T>::at(tb, k), d.resid ? Elem<T>::at(db, k) : 0.f);
-}
-
-// Sum of the draw weights of a staged chunk (thread-strided fp32, then fp64
-// across threads in a fixed order).
-template <typename T>
-__device__ __forceinline__ double chunk_sum(const DrawCtx &d, const T *tb, const T *db, int len,
-                                            double *red)
-{
-    float acc = 0.f;
-    for (int k = threadIdx.x; k < len; k += kFinishThreads)
-        acc += draw_at(d, tb, db, k);
-    return block_sum_d((double)acc, red);
-}
-
-// Smallest k of the staged chunk with base + C(k) > target, C the running sum
-// in index order; when rounding leaves none, the last k with weight > 0.
-// Warps own contiguous segments; in the segment holding the target, 32
-// consecutive elements are scanned per step with a warp prefix sum.
-template <typename T>
-__device__ int chunk_search(const DrawCtx &d, const T *tb, const T *db, int len, double base,
-                            double target, double *wtot, int *s_res)
-{
+    constexpr int E = Elem<T>::kPerVec;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int seg = (len + kFinishWarps - 1) / kFinishWarps;
-    const int k0 = min(len, warp * seg), k1 = min(len, k0 + seg);
-    float acc = 0.f;
-    for (int k = k0 + lane; k < k1; k += 32)
-        acc += draw_at(d, tb, db, k);
-    const double tot = warp_sum_d((double)acc);
-    __syncthreads();
+    const int nv = (len + E - 1) / E;
+    const int v0 = min(nv, threadIdx.x * pv), v1 = min(nv, v0 + pv);
+    float ps;
+    int lp;
+    walk_piece<T>(d, tb, db, len, v0, v1, INFINITY, &ps, &lp);
+    piece[threadIdx.x] = ps;
+    const ff ws = warp_sum_ff({ps, 0.f});
+    __syncthreads();  // piece[] complete; wred free
     if (lane == 0)
-        wtot[warp] = tot;
-    if (threadIdx.x == 0)
-        *s_res = -1;
+        wred[warp] = ws;
     __syncthreads();
-    double lo = base;
-    int wc = -1;
-    for (int w2 = 0; w2 < kFinishWarps; ++w2) {
-        if (lo + wtot[w2] > target) {
-            wc = w2;
-            break;
-        }
-        lo += wtot[w2];
-    }
-    if (warp == wc) {
-        double run = lo;
-        for (int kb = k0; kb < k1; kb += 32) {
-            const int k = kb + lane;
-            const float x = k < k1 ? draw_at(d, tb, db, k) : 0.f;
-            float incl = x;
+    ff tot = wred[0];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o)
-                    incl += n;
-            }
-            const unsigned hit =
-                __ballot_sync(0xffffffffu, k < k1 && run + (double)incl > target);
-            if (hit) {
-                if (lane == 0)
-                    *s_res = kb + __ffs(hit) - 1;
-                break;
-            }
-            run += (double)__shfl_sync(0xffffffffu, incl, 31);
-        }
-    }
-    __syncthreads();
-    int res = *s_res;
-    if (res < 0) {
-        int best = -1;
-        for (int k = threadIdx.x; k < len; k += kFinishThreads)
-            if (draw_at(d, tb, db, k) > 0.f)
-                best = k;
-        if (best >= 0)
-            atomicMax(s_res, best);
-        __syncthreads();
-        res = *s_res;
-    }
-    return res;
+    for (int w = 1; w < kFinishWarps; ++w)
+        tot = ff_add(tot, wred[w]);
+    return tot;
 }
 
-template <typename T, bool GREEDY>
-__global__ void __launch_bounds__(kFinishThreads) finish_kernel(const FinishParams p)
+template <typename T>
+__global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
     T *tb = reinterpret_cast<T *>(dsm);
-    T *db = reinterpret_cast<T *>(dsm + p.chunk_smem);
+    T *db = reinterpret_cast<T *>(dsm + p.stage_smem);
     __shared__ __align__(8) uint64_t bar;
     __shared__ float row_m[2 * kMaxDraft + 1];
-    __shared__ double row_s[2 * kMaxDraft + 1];
-    __shared__ int row_g[kMaxDraft + 1];
-    __shared__ double red[kFinishWarps];
-    __shared__ double s_tot[kMaxChunks];
-    __shared__ double s_base, s_target;
-    __shared__ int s_a, s_bad, s_last, s_res, s_mode, s_cs;
+    __shared__ ff row_s[2 * kMaxDraft + 1];
+    __shared__ float piece[kFinishThreads];
+    __shared__ ff wred[kFinishWarps];
+    __shared__ ff slice_tot[kMaxSlices];
+    __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
+    __shared__ ff s_excl[kFinishWarps];
+    __shared__ int s_a, s_bad, s_hit, s_last;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int NC = GREEDY ? 1 : p.NC;
-    const int i = blockIdx.x / NC, c = blockIdx.x % NC;
+    const uint32_t rank = cluster_ctarank();
+    const int i = blockIdx.x / kCluster;
 
-    pdl_wait();  // kernel 1 has completed and its writes are visible
-    if (__ldcg(p.cu_flag) == 0u)
-        return;  // malformed offsets: kernel 1 poisoned every output
+    // ---- inputs that do not depend on kernel 1, read before waiting for it
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
     const int cu_i = __ldg(p.cu + i);
     const int K = __ldg(p.cu + i + 1) - cu_i;
+    const bool shape = request_shape_ok(p, i, cu_i, K);
     const int64_t t0 = (int64_t)cu_i + i;
-    const int64_t gmr = p.g.max_rows;
+    const bool act = shape && warp == 0 && lane < K;
+    int x = -1;
+    float u = 0.f, gt = 0.f, gd = 0.f;
+    int64_t di = 0;
+    if (act) {
+        di = draft_index(p.draft_stride, p.cu, i, lane);
+        x = __ldg(p.tokens + di);
+        u = __ldg(p.u_accept + di);
+        if (x >= 0 && x < p.V) {
+            gt = Elem<T>::ld_global(reinterpret_cast<const T *>(p.target) + (t0 + lane) * p.V, x);
+            gd = Elem<T>::ld_global(reinterpret_cast<const T *>(p.draft) + di * p.V, x);
+        }
+    }
+    const float uf = __ldg(p.u_final + i);
 
-    if constexpr (GREEDY) {
-        for (int rho = warp; rho <= K; rho += kFinishWarps) {
-            const int gj = merge_argmax_row(p, t0 + rho);
-            if (lane == 0)
-                row_g[rho] = gj;
+    pdl_wait();  // kernel 1 has completed and its writes are visible
+    if (__ldcg(p.cu_flag) == 0u || !shape)
+        return;  // malformed offsets: kernel 1 poisoned every output (same in every CTA)
+
+    // ---- (m, s) of the request's 2K+1 rows: target rows 0..K, then draft rows
+    const int64_t gmr = p.g.max_rows;
+    merge_softmax_rows(
+        p.part, p.g, 2 * K + 1,
+        [&](int k) -> int64_t { return k <= K ? t0 + k : gmr + cu_i + (k - K - 1); }, p.c,
+        row_m, row_s);
+    __syncthreads();
+
+    // ---- accept test and first rejection (warp 0; identical in every CTA)
+    if (warp == 0) {
+        bool bad_tok = act && (x < 0 || x >= p.V), bad_nf = false, acc = true;
+        float pp = 0.f, qq = 0.f;
+        if (act && !bad_tok) {
+            const float mt = row_m[lane], md = row_m[K + 1 + lane];
+            const ff st = row_s[lane], sd = row_s[K + 1 + lane];
+            if (!row_ok(mt, st) || !row_ok(md, sd)) {
+                bad_nf = true;
+            } else {
+                pp = softmax_at(gt, mt, st, p.c);
+                qq = softmax_at(gd, md, sd, p.c);
+                const float ratio = qq > 0.f ? __fdiv_rn(pp, qq) : (pp > 0.f ? INFINITY : 0.f);
+                acc = u < ratio;
+            }
         }
-        __syncthreads();
-        if (warp != 0)
-            return;
-        const bool act = lane < K;
-        int x = -1;
-        bool bad_tok = false;
-        if (act) {
-            x = __ldg(p.tokens + draft_index(p.draft_stride, p.cu, i, lane));
-            bad_tok = x < 0 || x >= p.V;
-        }
-        bool bad_nf = false;
-        for (int jj = lane; jj <= K; jj += 32)
-            bad_nf |= row_g[jj] < 0;
+        if (lane == 0 && !row_ok(row_m[K], row_s[K]))
+            bad_nf = true;
         const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
         const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
-        const unsigned rej = __ballot_sync(0xffffffffu, act && x != row_g[act ? lane : 0]);
+        const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
+        // bad depends only on the request's data, so every CTA of the cluster
+        // takes the same branch; an expired wait only poisons (best effort)
+        const bool bad = nf || bt;
         const bool timeout = read_status(p.status) & ST_TIMEOUT;
-        if (nf || bt || timeout) {
-            if (lane == 0)
-                set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
-            for (int jj = lane; jj <= K; jj += 32)
-                p.out_tokens[t0 + jj] = -1;
-            if (lane == 0)
-                p.out_len[i] = -1;
-            return;
-        }
         const int a = rej ? __ffs(rej) - 1 : K;
-        for (int jj = lane; jj <= K; jj += 32)
-            p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
-        if (lane == 0)
-            p.out_len[i] = a;
-        return;
-    } else {
-        // ---- merge (m, s) of the request's 2K+1 rows
-        for (int rho = warp; rho < 2 * K + 1; rho += kFinishWarps) {
-            const int64_t rg = rho <= K ? t0 + rho : gmr + cu_i + (rho - K - 1);
-            float m;
-            double s;
-            merge_softmax_row(p, rg, m, s);
-            if (lane == 0) {
-                row_m[rho] = m;
-                row_s[rho] = s;
-            }
-        }
-        __syncthreads();
-        // ---- accept test and first rejection (warp 0; identical in every CTA)
-        if (warp == 0) {
-            const bool act = lane < K;
-            int x = -1;
-            bool bad_tok = false, bad_nf = false, acc = true;
-            double pp = 0.0, qq = 0.0;
-            int64_t di = 0;
-            if (act) {
-                di = draft_index(p.draft_stride, p.cu, i, lane);
-                x = __ldg(p.tokens + di);
-                if (x < 0 || x >= p.V) {
-                    bad_tok = true;
-                } else {
-                    const float mt = row_m[lane], md = row_m[K + 1 + lane];
-                    const double st = row_s[lane], sd = row_s[K + 1 + lane];
-                    if (!row_ok(mt, st) || !row_ok(md, sd)) {
-                        bad_nf = true;
-                    } else {
-                        const T *trow = reinterpret_cast<const T *>(p.target) + (t0 + lane) * p.V;
-                        const T *drw = reinterpret_cast<const T *>(p.draft) + di * p.V;
-                        const double gt = Elem<T>::ld_global(trow, x);
-                        const double gd = Elem<T>::ld_global(drw, x);
-                        pp = (double)exp2_split((gt - (double)mt) * (double)p.c) / st;
-                        qq = (double)exp2_split((gd - (double)md) * (double)p.c) / sd;
-                        const double ratio = qq > 0.0 ? pp / qq : (pp > 0.0 ? INFINITY : 0.0);
-                        acc = (double)__ldg(p.u_accept + di) < ratio;
-                    }
-                }
-            }
-            if (lane == 0 && !row_ok(row_m[K], row_s[K]))
-                bad_nf = true;
-            const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
-            const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
-            const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
-            // bad depends only on the request's data, so every CTA of the
-            // request takes the same branch (and the ticket count stays whole);
-            // an expired wait only poisons outputs (best effort)
-            const bool bad = nf || bt;
-            const bool timeout = read_status(p.status) & ST_TIMEOUT;
-            const int a = rej ? __ffs(rej) - 1 : K;
-            if (c == 0) {  // the request's outputs, written once
-                if (bad || timeout) {
-                    if (lane == 0)
-                        set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
-                    for (int jj = lane; jj <= K; jj += 32)
-                        p.out_tokens[t0 + jj] = -1;
-                    if (lane == 0)
-                        p.out_len[i] = -1;
-                } else {
-                    if (act && p.out_p)
-                        p.out_p[di] = (float)pp;
-                    if (act && p.out_q)
-                        p.out_q[di] = (float)qq;
-                    for (int jj = lane; jj <= K; jj += 32) {
-                        if (jj < a)
-                            p.out_tokens[t0 + jj] = x;  // jj == lane since a <= 32
-                        else if (jj > a)
-                            p.out_tokens[t0 + jj] = -1;
-                    }
-                    if (lane == 0)
-                        p.out_len[i] = a;
-                }
-            }
-            if (lane == 0) {
-                s_a = a;
-                s_bad = bad;
-            }
-        }
-        __syncthreads();
-        if (s_bad)
-            return;
-
-        // ---- final draw over chunk c of the rows of position a
-        const int a = s_a;
-        const int64_t trow_i = t0 + a;
-        const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
-        if (trow_i >= gmr || drow_i >= p.draft_rows) {  // never with valid offsets
-            if (tid == 0)
-                set_status(p.status, ST_INVALID);
-            return;
-        }
-        DrawCtx d;
-        d.resid = drow_i >= 0;
-        d.c = p.c;
-        {
-            const float mt = row_m[a];
-            d.mct = mt * p.c;
-            d.sc_t = (float)((double)mc_correction(mt, d.mct, p.c) / row_s[a]);
-            if (d.resid) {
-                const float md = row_m[K + 1 + a];
-                d.mcd = md * p.c;
-                d.sc_d = (float)((double)mc_correction(md, d.mcd, p.c) / row_s[K + 1 + a]);
-            } else {
-                d.mcd = 0.f;
-                d.sc_d = 0.f;
-            }
-        }
-        const T *trow = reinterpret_cast<const T *>(p.target) + trow_i * p.V;
-        const T *drow = d.resid ? reinterpret_cast<const T *>(p.draft) + drow_i * p.V : nullptr;
-
-        if (tid == 0) {
-            mbar_init(&bar, 1);
-            fence_mbar_init();
-        }
-        __syncthreads();
-        uint32_t phase = 0;
-        int len = stage_chunk<T>(p, trow, drow, d.resid, c, tb, db, &bar, phase);
-        double tot = chunk_sum<T>(d, tb, db, len, red);
-        if (tid == 0) {
-            p.part2[(int64_t)i * NC + c] = tot;
-            __threadfence();
-            s_last = atomicAdd(p.cnt2 + i, 1u) == (uint32_t)NC - 1;
-        }
-        __syncthreads();
-        if (!s_last)
-            return;
-        __threadfence();
-        int staged = c;
-        if (tid == 0) {
-            p.cnt2[i] = 0;  // ready for the next call
-            double S = 0.0;
-            for (int cc = 0; cc < NC; ++cc) {
-                s_tot[cc] = __ldcg(p.part2 + (int64_t)i * NC + cc);
-                S += s_tot[cc];
-            }
-            s_mode = (d.resid && !(S > 0.0)) ? 1 : 0;  // all-zero residual: draw from p_a
-        }
-        __syncthreads();
-        if (s_mode == 1) {
-            d.resid = false;
-            for (int cc = 0; cc < NC; ++cc) {
-                len = stage_chunk<T>(p, trow, drow, false, cc, tb, db, &bar, phase);
-                tot = chunk_sum<T>(d, tb, db, len, red);
-                if (tid == 0)
-                    s_tot[cc] = tot;
-                staged = cc;
-            }
-            __syncthreads();
-        }
-        if (tid == 0) {
-            double S = 0.0;
-            for (int cc = 0; cc < NC; ++cc)
-                S += s_tot[cc];
-            const double target = (double)__ldg(p.u_final + i) * S;
-            double cum = 0.0, base = 0.0, tgt = target;
-            int cs = -1;
-            for (int cc = 0; cc < NC; ++cc) {
-                if (cum + s_tot[cc] > target) {
-                    cs = cc;
-                    base = cum;
-                    break;
-                }
-                cum += s_tot[cc];
-            }
-            if (cs < 0) {  // u*S at or past the end after rounding: last chunk with mass
-                cs = 0;
-                double cum2 = 0.0;
-                for (int cc = 0; cc < NC; ++cc) {
-                    if (s_tot[cc] > 0.0) {
-                        cs = cc;
-                        base = cum2;
-                    }
-                    cum2 += s_tot[cc];
-                }
-                tgt = INFINITY;
-            }
-            s_cs = cs;
-            s_base = base;
-            s_target = tgt;
-        }
-        __syncthreads();
-        const int cs = s_cs;
-        if (cs != staged)
-            len = stage_chunk<T>(p, trow, drow, d.resid, cs, tb, db, &bar, phase);
-        else
-            len = min(p.nce, p.V - cs * p.nce);
-        const int k = chunk_search<T>(d, tb, db, len, s_base, s_target, red, &s_res);
-        if (tid == 0) {
-            int y = k >= 0 ? cs * p.nce + k : -1;
-            if (y < 0)
-                set_status(p.status, ST_NONFINITE);
-            if (read_status(p.status) & ST_TIMEOUT) {  // staged data may be stale
-                y = -1;
-                p.out_len[i] = -1;
-                for (int jj = 0; jj <= K; ++jj)
+        if (rank == 0) {  // the request's outputs, written once
+            if (bad || timeout) {
+                if (lane == 0)
+                    set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+                for (int jj = lane; jj <= K; jj += 32)
                     p.out_tokens[t0 + jj] = -1;
+                if (lane == 0)
+                    p.out_len[i] = -1;
+            } else {
+                if (act && p.out_p)
+                    p.out_p[di] = pp;
+                if (act && p.out_q)
+                    p.out_q[di] = qq;
+                for (int jj = lane; jj <= K; jj += 32) {
+                    if (jj < a)
+                        p.out_tokens[t0 + jj] = x;  // jj == lane since a <= 32
+                    else if (jj > a)
+                        p.out_tokens[t0 + jj] = -1;
+                }
+                if (lane == 0)
+                    p.out_len[i] = a;
             }
-            p.out_tokens[trow_i] = y;
         }
+        if (lane == 0) {
+            s_a = a;
+            s_bad = bad;
+        }
+    }
+    __syncthreads();
+    if (s_bad)
+        return;  // same decision in every CTA of the cluster
+
+    // ---- final draw: this CTA sums the weights of its range of the vocabulary
+    const int a = s_a;
+    const int64_t trow_i = t0 + a;
+    const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
+    DrawCtx d;
+    d.resid = drow_i >= 0;
+    d.c = p.c;
+    {
+        const float mt = row_m[a];
+        d.mct = mt * p.c;
+        d.sc_t = ff_recip_scaled(mc_correction(mt, d.mct, p.c), row_s[a]);
+        if (d.resid) {
+            const float md = row_m[K + 1 + a];
+            d.mcd = md * p.c;
+            d.sc_d = ff_recip_scaled(mc_correction(md, d.mcd, p.c), row_s[K + 1 + a]);
+        } else {
+            d.mcd = 0.f;
+            d.sc_d = 0.f;
+        }
+    }
+    const T *trow = reinterpret_cast<const T *>(p.target) + trow_i * p.V;
+    const T *drow = d.resid ? reinterpret_cast<const T *>(p.draft) + drow_i * p.V : nullptr;
+    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
+    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+    uint32_t phase = 0;
+    int staged = -1;  // slice currently in shared memory
+
+    cluster_arrive_relaxed();  // (1) every CTA of the cluster has started
+    auto range_sum = [&]() -> ff {
+        ff tot{0.f, 0.f};
+        for (int sl = 0; sl < nsl; ++sl) {
+            const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+            stage_slice<T>(p, trow, drow, d.resid, c0, len, tb, db, &bar, phase);
+            staged = sl;
+            const ff ss = slice_sum<T>(d, tb, db, len, p.pv, piece, wred);
+            if (tid == 0)
+                slice_tot[sl] = ss;
+            tot = ff_add(tot, ss);
+        }
+        return tot;
+    };
+    ff mine = range_sum();
+    cluster_wait_acquire();  // (1) complete: remote shared memory is live
+    if (tid < kCluster)
+        st_cluster_ff(&cl_sum[0][rank], (uint32_t)tid, mine);
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (2) every CTA holds every range sum
+    int slot = 0;
+    ff S = cl_sum[0][0];
+    for (int r = 1; r < kCluster; ++r)
+        S = ff_add(S, cl_sum[0][r]);
+    if (d.resid && !(S.hi > 0.f)) {  // all-zero residual: draw from p_a instead
+        d.resid = false;
+        mine = range_sum();
+        if (tid < kCluster)
+            st_cluster_ff(&cl_sum[1][rank], (uint32_t)tid, mine);
+        cluster_arrive_release();
+        cluster_wait_acquire();  // (3)
+        slot = 1;
+        S = cl_sum[1][0];
+        for (int r = 1; r < kCluster; ++r)
+            S = ff_add(S, cl_sum[1][r]);
+    }
+    // no shared memory of another CTA is touched after this point
+
+    // ---- the range holding u*S (same choice in every CTA); `past` marks
+    // u*S at or beyond the end after rounding: then the last weight > 0 wins
+    const ff target = ff_mul(S, uf);
+    bool past = false;
+    ff base{0.f, 0.f}, cum{0.f, 0.f};
+    int cs = -1;
+    for (int r = 0; r < kCluster; ++r) {
+        const ff v = cl_sum[slot][r];
+        const ff next = ff_add(cum, v);
+        if (cs < 0 && ff_gt(next, target)) {
+            cs = r;
+            base = cum;
+        }
+        cum = next;
+    }
+    if (cs < 0) {
+        past = true;
+        cum = {0.f, 0.f};
+        for (int r = 0; r < kCluster; ++r) {
+            if (cl_sum[slot][r].hi > 0.f) {
+                cs = r;
+                base = cum;
+            }
+            cum = ff_add(cum, cl_sum[slot][r]);
+        }
+    }
+    if ((int)rank != cs) {
+        if (cs < 0 && rank == 0 && tid == 0) {  // no mass at all (never with finite rows)
+            set_status(p.status, ST_NONFINITE);
+            p.out_tokens[trow_i] = -1;
+        }
+        return;
+    }
+
+    // ---- owner CTA: the slice, then the thread piece, then the element
+    int sl = -1;
+    {
+        ff b2 = base;
+        for (int s2 = 0; s2 < nsl && !past; ++s2) {
+            const ff next = ff_add(b2, slice_tot[s2]);
+            if (ff_gt(next, target)) {
+                sl = s2;
+                break;
+            }
+            b2 = next;
+        }
+        if (sl >= 0) {
+            base = b2;
+        } else {  // the last slice with mass
+            past = true;
+            ff bl = base;
+            b2 = base;
+            sl = nsl - 1;
+            for (int s2 = 0; s2 < nsl; ++s2) {
+                if (slice_tot[s2].hi > 0.f) {
+                    sl = s2;
+                    bl = b2;
+                }
+                b2 = ff_add(b2, slice_tot[s2]);
+            }
+            base = bl;
+        }
+    }
+    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+    if (sl != staged) {
+        stage_slice<T>(p, trow, drow, d.resid, c0, len, tb, db, &bar, phase);
+        slice_sum<T>(d, tb, db, len, p.pv, piece, wred);
+    }
+    // scan of the piece sums (float-float, fixed order).  A piece's lower end
+    // is the previous piece's upper end bit for bit, so the pieces tile the
+    // slice with no gap and no overlap.
+    ff incl{piece[tid], 0.f};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(incl, o);
+        if (lane >= o)
+            incl = ff_add(n, incl);
+    }
+    ff excl = ff_shfl_up(incl, 1);
+    if (lane == 0)
+        excl = {0.f, 0.f};
+    if (tid == 0)
+        s_hit = INT_MAX;
+    if (lane == 31)
+        s_excl[warp] = incl;
+    __syncthreads();
+    ff wbase = base;
+    for (int w = 0; w < warp; ++w)
+        wbase = ff_add(wbase, s_excl[w]);
+    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
+    if (!past && ff_le(lo, target) && ff_gt(hi, target))
+        atomicMin(&s_hit, tid);
+    __syncthreads();
+    int res = -1;
+    constexpr int E = Elem<T>::kPerVec;
+    const int nv = (len + E - 1) / E;
+    if (s_hit != INT_MAX) {
+        if (tid == s_hit) {
+            const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+            float ps;
+            int lp;
+            const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+            int k = walk_piece<T>(d, tb, db, len, v0, v1, rem, &ps, &lp);
+            if (k < 0)
+                k = lp;  // rem rounded up to the piece total: its last element with mass
+            s_last = k;
+        }
+        __syncthreads();
+        res = s_last;
+    } else {  // past the end after rounding: the last element with mass
+        if (tid == 0)
+            s_last = -1;
+        __syncthreads();
+        const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+        float ps;
+        int lp;
+        walk_piece<T>(d, tb, db, len, v0, v1, INFINITY, &ps, &lp);
+        if (lp >= 0)
+            atomicMax(&s_last, lp);
+        __syncthreads();
+        res = s_last;
+    }
+    if (tid == 0) {
+        int y = res >= 0 ? c0 + res : -1;
+        if (y < 0)
+            set_status(p.status, ST_NONFINITE);
+        if (read_status(p.status) & ST_TIMEOUT) {  // staged data may be stale
+            y = -1;
+            p.out_len[i] = -1;
+            for (int jj = 0; jj <= K; ++jj)
+                p.out_tokens[t0 + jj] = -1;
+        }
+        p.out_tokens[trow_i] = y;
     }
 }
 
@@ -1201,13 +1430,13 @@ static cudaError_t prepare_stream()
     return once;
 }
 
-template <typename T, bool GREEDY>
-static cudaError_t prepare_finish()
+template <typename T>
+static cudaError_t prepare_finish_sample()
 {
     static cudaError_t once = [] {
-        return cudaFuncSetAttribute(finish_kernel<T, GREEDY>,
+        return cudaFuncSetAttribute(finish_sample_kernel<T>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    2 * (kDrawChunkBytes + 128));
+                                    2 * kStageRowBytes);
     }();
     return once;
 }
@@ -1261,21 +1490,27 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
     fp.draft_stride = a.draft_stride;
     fp.g = g;
-    const Chunking dc = chunking(a.V, e);
-    fp.NC = GREEDY ? 1 : dc.nchunks;
-    fp.nce = dc.chunk_elems;
-    fp.chunk_smem = (int)align_up((size_t)dc.chunk_elems * e, 128);
+    {  // final-draw geometry: kCluster ranges of R entries, staged in slices
+        const int gran = 16 / e;
+        const int R = (int)((((int64_t)a.V + kCluster - 1) / kCluster + gran - 1) / gran * gran);
+        const int slice = std::min(R, kStageRowBytes / e);
+        const int nv = (slice * e + 15) / 16;
+        fp.R = R;
+        fp.slice = slice;
+        fp.pv = ((nv + kFinishThreads - 1) / kFinishThreads) | 1;  // odd: no bank conflicts
+        fp.stage_smem = (int)align_up((size_t)slice * e, 128);
+        if ((R + slice - 1) / slice > kMaxSlices)
+            return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
+    }
     fp.tma = tma;
     fp.c = sp.c;
     fp.status = sp.status;
     fp.cu_flag = sp.cu_flag;
-    fp.cnt2 = reinterpret_cast<uint32_t *>(ws + L.cnt2);
     fp.part = sp.part;
-    fp.part2 = reinterpret_cast<double *>(ws + L.part2);
 
     cudaError_t err = prepare_stream<T, GREEDY>();
-    if (err == cudaSuccess)
-        err = prepare_finish<T, GREEDY>();
+    if (err == cudaSuccess && !GREEDY)
+        err = prepare_finish_sample<T>();
     if (err != cudaSuccess)
         return err;
     const int grid1 = (g.P + kStreamWarps - 1) / kStreamWarps;
@@ -1288,16 +1523,28 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     tr.after_kernel(s);
 
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)(a.B * fp.NC));
     cfg.blockDim = dim3(kFinishThreads);
-    cfg.dynamicSmemBytes = GREEDY ? 0 : 2 * (size_t)fp.chunk_smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if ((err = cudaLaunchKernelEx(&cfg, finish_kernel<T, GREEDY>, fp)) != cudaSuccess)
+    if (GREEDY) {
+        cfg.gridDim = dim3((unsigned)a.B);
+        cfg.dynamicSmemBytes = 0;
+        cfg.numAttrs = 1;
+        err = cudaLaunchKernelEx(&cfg, finish_greedy_kernel<T>, fp);
+    } else {
+        cfg.gridDim = dim3((unsigned)(a.B * kCluster));
+        cfg.dynamicSmemBytes = 2 * (size_t)fp.stage_smem;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = kCluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+        err = cudaLaunchKernelEx(&cfg, finish_sample_kernel<T>, fp);
+    }
+    if (err != cudaSuccess)
         return err;
     tr.after_kernel(s);
     return cudaSuccess;

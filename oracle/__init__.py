@@ -65,6 +65,9 @@ def load(path: str | None = None):
         lib.oracle_final_cdf.argtypes = [_p, _p, ctypes.c_int, _p, _i32, _i64, _i32, _f64,
                                          _i32, _p]
         lib.oracle_dcut_allocate.argtypes = [_p, _p, _i32, _i32, _i32, _f32, _p, _p, _p]
+        lib.oracle_dcut_cost.argtypes = [_i32]
+        lib.oracle_dcut_cost.restype = _f64
+        lib.oracle_dcut_schedule_cost.argtypes = [_p, _p, _i32, _i32, _f64, _p, _p, _p]
         if path is None:
             _lib = lib
         return lib
@@ -242,3 +245,22 @@ def dcut_allocate(conf, kmax, budget: int, min_gain: float = 0.0, lib=None):
                                               float(min_gain), _ptr(depth), _ptr(cu),
                                               _ptr(exp_len))
     return VerifyResult(status=st, depth=depth[:B], cu=cu, expected=exp_len[:B])
+
+
+def dcut_cost(d: int, lib=None) -> float:
+    return float((lib or load()).oracle_dcut_cost(int(d)))
+
+
+def dcut_schedule_cost(conf, kmax, max_cost: float, lib=None):
+    """The cost-unit D-cut variant: per-request best depth by benefit, then
+    greedy admission under max_cost (latency-cost units)."""
+    c = _np(conf, np.float32)
+    km = _np(kmax, np.int32)
+    B = km.size
+    Kmax = c.shape[1] if c.ndim == 2 else (c.size // B if B else 0)
+    depth = np.full(max(B, 1), -7, np.int32)
+    cu = np.full(B + 1, -7, np.int32)
+    benefit = np.full(max(B, 1), np.nan, np.float64)
+    st = (lib or load()).oracle_dcut_schedule_cost(_ptr(c), _ptr(km), B, Kmax, float(max_cost),
+                                                   _ptr(depth), _ptr(cu), _ptr(benefit))
+    return VerifyResult(status=st, depth=depth[:B], cu=cu, benefit=benefit[:B])

@@ -583,3 +583,117 @@ int oracle_dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int3
     free(cand);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* D-cut, cost-unit variant                                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The deep-dive page ("Tencent AngelSpec Speculative Decoding Framework Deep
+ * Dive ...", its DCutScheduler listing) budgets verification in profiled
+ * latency-cost units instead of tokens.  What it computes:
+ *  - cost(d): the latency of verifying depth d, read from the table
+ *    {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0} by linear interpolation
+ *    between neighbouring entries, clamped to the first / last entry
+ *    outside [1, 16];
+ *  - per request: the depth d in 1..kmax maximising
+ *    benefit(d) = (conf_0 * ... * conf_{d-1}) * d / cost(d)
+ *    (the first such d when several tie);
+ *  - requests in decreasing order of that benefit (equal benefits keep
+ *    request order), each admitted when the running cost total plus its own
+ *    cost stays within max_cost; a request that does not fit is skipped and
+ *    later ones are still tried.
+ * Readings: all of it in fp64 (the page's arithmetic), products left to
+ * right; a request with kmax = 0 is no candidate; a request not admitted
+ * verifies depth 0 (its bonus row only).
+ */
+double oracle_dcut_cost(int32_t d)
+{
+    static const int32_t dep[5] = {1, 2, 4, 8, 16};
+    static const double lat[5] = {1.0, 1.2, 1.5, 2.0, 3.0};
+    if (d <= dep[0])
+        return lat[0];
+    if (d >= dep[4])
+        return lat[4];
+    for (int k = 0; k < 4; ++k) {
+        if (dep[k] <= d && d <= dep[k + 1]) {
+            double r = (double)(d - dep[k]) / (double)(dep[k + 1] - dep[k]);
+            return lat[k] + r * (lat[k + 1] - lat[k]);
+        }
+    }
+    return lat[4];
+}
+
+typedef struct {
+    double benefit;
+    int32_t i;
+    int32_t d;
+} dcut_cost_cand;
+
+static int dcut_cost_cmp(const void *pa, const void *pb)
+{
+    const dcut_cost_cand *a = (const dcut_cost_cand *)pa, *b = (const dcut_cost_cand *)pb;
+    if (a->benefit > b->benefit)
+        return -1;
+    if (a->benefit < b->benefit)
+        return 1;
+    return a->i < b->i ? -1 : (a->i > b->i ? 1 : 0);
+}
+
+int oracle_dcut_schedule_cost(const float *conf, const int32_t *kmax, int32_t B, int32_t Kmax,
+                              double max_cost, int32_t *out_depth, int32_t *out_cu,
+                              double *out_benefit)
+{
+    if (B < 0 || Kmax < 0 || Kmax > ORC_MAX_DRAFT || isnan(max_cost))
+        return ORC_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < B; ++i) {
+        if (kmax[i] < 0 || kmax[i] > Kmax)
+            return ORC_ERR_INVALID_ARG;
+        for (int32_t j = 0; j < kmax[i]; ++j) {
+            float c = conf[(int64_t)i * Kmax + j];
+            if (!(c >= 0.0f && c <= 1.0f))
+                return ORC_ERR_INVALID_ARG;
+        }
+    }
+    dcut_cost_cand *cand = (dcut_cost_cand *)malloc((size_t)(B > 0 ? B : 1) * sizeof *cand);
+    if (!cand)
+        return ORC_ERR_INVALID_ARG;
+    int32_t n = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        out_depth[i] = 0;
+        if (out_benefit)
+            out_benefit[i] = 0.0;
+        if (kmax[i] == 0)
+            continue;
+        double P = 1.0, best = -1.0;
+        int32_t best_d = 0;
+        for (int32_t d = 1; d <= kmax[i]; ++d) {
+            P = P * (double)conf[(int64_t)i * Kmax + (d - 1)];
+            double b = P * (double)d / oracle_dcut_cost(d);
+            if (b > best) { /* strict: the first maximising depth is kept */
+                best = b;
+                best_d = d;
+            }
+        }
+        cand[n].benefit = best;
+        cand[n].i = i;
+        cand[n].d = best_d;
+        ++n;
+    }
+    qsort(cand, (size_t)n, sizeof *cand, dcut_cost_cmp);
+    double total = 0.0;
+    for (int32_t t = 0; t < n; ++t) {
+        double c = oracle_dcut_cost(cand[t].d);
+        if (total + c <= max_cost) {
+            total += c;
+            out_depth[cand[t].i] = cand[t].d;
+            if (out_benefit)
+                out_benefit[cand[t].i] = cand[t].benefit;
+        }
+    }
+    out_cu[0] = 0;
+    for (int32_t i = 0; i < B; ++i)
+        out_cu[i + 1] = out_cu[i] + out_depth[i];
+    free(cand);
+    return ORC_OK;
+}

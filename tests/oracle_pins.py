@@ -598,3 +598,73 @@ ALL_PINS = [
     pin_sample_outputs_layout, pin_sample_errors, pin_dcut_golden, pin_dcut_brute_force,
     pin_dcut_expected_len, pin_dcut_errors,
 ]
+
+
+# ---------------------------------------------------------------------------
+# D-cut, cost-unit variant
+# ---------------------------------------------------------------------------
+
+
+def _padded(conf_rows):
+    K = max(len(r) for r in conf_rows)
+    c = np.zeros((len(conf_rows), K), np.float32)
+    for i, r in enumerate(conf_rows):
+        c[i, :len(r)] = r
+    return c
+
+
+def pin_dcut_cost_table(lib):
+    """Hand-interpolated latency table (tests/golden/dcut_cost.json)."""
+    g = _golden("dcut_cost.json")
+    for d, want in g["cost_table"]:
+        got = O.dcut_cost(d, lib=lib)
+        assert abs(got - want) <= 1e-15, (d, got, want)
+
+
+def pin_dcut_cost_golden(lib):
+    g = _golden("dcut_cost.json")
+    for case in g["cases"]:
+        r = O.dcut_schedule_cost(_padded(case["conf"]), np.array(case["kmax"], np.int32),
+                                 case["max_cost"], lib=lib)
+        assert r.status == O.OK, case["name"]
+        assert r.depth.tolist() == case["expected_depth"], (case["name"], r.depth)
+        assert r.cu.tolist() == [0] + np.cumsum(case["expected_depth"]).tolist(), case["name"]
+
+
+def pin_dcut_cost_invariants(lib):
+    """Random batches: the admitted total stays within the budget (costs read
+    from the hand table), every depth lies in 1..kmax or is 0, and a budget
+    above every request's cost admits every request that drafted something."""
+    g = _golden("dcut_cost.json")
+    table = dict((int(d), c) for d, c in g["cost_table"])
+    full = {d: table.get(d) for d in range(0, 33)}
+    rng = np.random.default_rng(11)
+    for trial in range(40):
+        B = int(rng.integers(1, 9))
+        Kmax = int(rng.integers(1, 9))
+        kmax = rng.integers(0, Kmax + 1, size=B).astype(np.int32)
+        conf = rng.random((B, Kmax)).astype(np.float32)
+        budget = float(rng.choice([0.5, 1.0, 2.5, 4.0, 100.0]))
+        r = O.dcut_schedule_cost(conf, kmax, budget, lib=lib)
+        assert r.status == O.OK
+        d = r.depth
+        assert np.all((d == 0) | ((d >= 1) & (d <= kmax))), (kmax, d)
+        known = [full[int(x)] for x in d if x > 0 and full[int(x)] is not None]
+        if len(known) == int((d > 0).sum()):
+            assert sum(known) <= budget + 1e-12, (d, budget)
+        if budget >= 3.0 * B:
+            assert np.all((d > 0) == (kmax > 0)), (kmax, d)
+
+
+def pin_dcut_cost_errors(lib):
+    c = np.array([[0.5, 1.5]], np.float32)
+    assert O.dcut_schedule_cost(c, np.array([2], np.int32), 4.0, lib=lib).status == \
+        O.ERR_INVALID_ARG
+    assert O.dcut_schedule_cost(np.zeros((1, 2), np.float32), np.array([3], np.int32), 4.0,
+                                lib=lib).status == O.ERR_INVALID_ARG
+    assert O.dcut_schedule_cost(np.zeros((1, 2), np.float32), np.array([2], np.int32),
+                                float("nan"), lib=lib).status == O.ERR_INVALID_ARG
+
+
+ALL_PINS += [pin_dcut_cost_table, pin_dcut_cost_golden, pin_dcut_cost_invariants,
+             pin_dcut_cost_errors]

@@ -100,15 +100,24 @@ def test_drafted_token_masked_in_target_rejects():
 
 
 def test_identical_rows_accept_everything():
+    """q = p makes p/q = 1, so every u < 1 accepts.  The kernels sum the
+    target and draft rows in different orders, so their p/q is 1 only to
+    fp32 rounding; u sits just outside the 1e-6 band in which an accept
+    decision may differ from the oracle's, and the band's edge itself is
+    compared by parity (u = 1 - 2^-24 there)."""
     b = ragged_batch(8, 3000, 0.8, "bf16", seed=6, kmin=1, kmax=10)
     for i in range(8):
         K = int(b.k[i])
         t0, d0 = int(b.cu_draft[i]) + i, int(b.cu_draft[i])
         b.draft_logits[d0:d0 + K] = b.target_logits[t0:t0 + K]
-    b.u_accept[:] = float(np.nextafter(np.float32(1), np.float32(0)))
+    b.u_accept[:] = 1.0 - 2.0 ** -16
     batch, out, v = run_gpu(b)
     assert torch.equal(out["accept_len"].cpu(), b.k)
     parity.compare_batch(batch, out)
+    b.u_accept[:] = float(np.nextafter(np.float32(1), np.float32(0)))
+    batch, out, v = run_gpu(b)
+    rep = parity.compare_batch(batch, out)
+    assert rep["exempt_accept"] <= b.B, rep
 
 
 @pytest.mark.parametrize("T", [0.7, 1.0])

@@ -47,6 +47,17 @@ MUTANTS = [
      "p_out[v] = exp((logit_at(logits, dtype, row, V, v) - m) / T) / s;",
      "p_out[v] = exp(logit_at(logits, dtype, row, V, v) / T) / s;"),
     ("inverse CDF forgets to scale u by S", "double target = u * S;", "double target = u;"),
+    ("cost table interpolates from the wrong end",
+     "return lat[k] + r * (lat[k + 1] - lat[k]);", "return lat[k + 1] - r * (lat[k + 1] - lat[k]) + 0.1;"),
+    ("cost variant stops at the first request that does not fit",
+     "if (total + c <= max_cost) {", "if (total + c > max_cost) break; {"),
+    ("cost variant benefit forgets the depth factor",
+     "double b = P * (double)d / oracle_dcut_cost(d);", "double b = P / oracle_dcut_cost(d);"),
+    ("cost variant keeps the last maximising depth", "if (b > best) { /* strict",
+     "if (b >= best) { /* strict"),
+    ("cost variant sorts ascending",
+     "if (a->benefit > b->benefit)\n        return -1;\n    if (a->benefit < b->benefit)\n        return 1;",
+     "if (a->benefit < b->benefit)\n        return -1;\n    if (a->benefit > b->benefit)\n        return 1;"),
 ]
 
 
