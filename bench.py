@@ -157,6 +157,30 @@ def recorded_traffic(workload: str, kernel: str):
     return None
 
 
+def read_stream_reference(nbytes: int, device, reps: int = 20) -> float:
+    """GB/s of a plain library read of nbytes (torch sum over a bf16 buffer),
+    rotating through enough buffers to exceed twice the L2: what a streaming
+    read of this size reaches on this GPU, as context for the roofline."""
+    n = max(8, nbytes // 2)
+    k = max(2, math.ceil(2.2 * l2_bytes(device) / max(nbytes, 1)))
+    k = min(k, 64)
+    bufs = [torch.ones(n, dtype=torch.bfloat16, device=device) for _ in range(k)]
+    out = torch.empty((), dtype=torch.float32, device=device)
+    for b in bufs[:3]:
+        torch.sum(b, dim=0, dtype=torch.float32, out=out)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record()
+    for r in range(reps):
+        torch.sum(bufs[r % k], dim=0, dtype=torch.float32, out=out)
+    e1.record()
+    torch.cuda.synchronize(device)
+    sec = e0.elapsed_time(e1) / 1e3 / reps
+    del bufs
+    return 2 * n / sec / 1e9
+
+
 def workload_desc(w, T):
     return f"{W.describe(w)}, T={T}"
 
@@ -447,6 +471,7 @@ def run_ours(args, dist):
     value = total_positions / (elapsed_ms_max / 1e3)
     ms_per_step = elapsed_ms_max / K
     peak, peak_kind = measured_hbm_peak()
+    read_ref = read_stream_reference(alg_bytes, device)
     step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
     achieved = alg_bytes / (rows_mean / 1e6) / 1e9
 
@@ -500,6 +525,8 @@ def run_ours(args, dist):
                      "peak": peak, "peak_kind": f"of {peak_kind}", "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": alg_bytes,
+                     "library_read_same_bytes_gbs": read_ref,
+                     "frac_of_library_read": achieved / read_ref,
                      "launch_us_mean": rows_mean},
         "kernels_us": {"stream_kernel": rows_mean,
                        ("finish_greedy_kernel" if T == 0 else "finish_sample_kernel"):

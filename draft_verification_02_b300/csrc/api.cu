@@ -210,6 +210,31 @@ int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kma
     return cuda_status(sv::launch_dcut(a, (cudaStream_t)stream, tr));
 }
 
+int dcut_allocate_cost(const float *conf, const int32_t *kmax, int32_t B, int32_t Kmax,
+                       double max_cost, int32_t *out_depth, int32_t *out_cu,
+                       double *out_benefit, void *workspace, size_t ws_bytes,
+                       spec_stream_t stream)
+{
+    if (B < 0 || B > SPEC_MAX_BATCH || Kmax < 0 || Kmax > SPEC_MAX_DRAFT || std::isnan(max_cost))
+        return SPEC_ERR_INVALID_ARG;
+    if (!out_cu || (B > 0 && (!kmax || !out_depth || (Kmax > 0 && !conf))))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(0, 0, 0))
+        return SPEC_ERR_WORKSPACE;
+    sv::DcutCostArgs a{};
+    a.conf = conf;
+    a.kmax = kmax;
+    a.B = B;
+    a.Kmax = Kmax;
+    a.max_cost = max_cost;
+    a.out_depth = out_depth;
+    a.out_cu = out_cu;
+    a.out_benefit = out_benefit;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_dcut_cost(a, (cudaStream_t)stream, tr));
+}
+
 int spec_get_device_status(void *workspace, spec_stream_t stream)
 {
     if (!workspace)

@@ -46,9 +46,10 @@ struct __align__(16) Partial {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: status word (+ offsets-valid flag) | stream partials (one per
-// (row, warp) segment: at most rows + warps).  The status word must start at
-// zero; the partials are written before they are read in every call.
+// Workspace: status word and offsets-valid flag (256 bytes; the status word
+// must be zero before the first call and every call leaves it so) | stream
+// partials, one per (row, warp) segment: at most rows + warps.  The partials
+// are written before they are read in every call.
 struct WsLayout {
     size_t status, part1, total;
 };

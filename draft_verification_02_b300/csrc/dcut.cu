@@ -240,3 +240,181 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 }
 
 }  // namespace sv
+
+// ---------------------------------------------------------------------------
+// D-cut, cost-unit variant
+// ---------------------------------------------------------------------------
+//
+// The deep-dive page ("Tencent AngelSpec Speculative Decoding Framework Deep
+// Dive ...", its DCutScheduler listing) budgets verification in profiled
+// latency-cost units: cost(d) interpolates the table {1: 1.0, 2: 1.2,
+// 4: 1.5, 8: 2.0, 16: 3.0} linearly (clamped to its ends); each request takes
+// the depth maximising benefit(d) = P_d * d / cost(d) (the first such d);
+// requests are admitted in decreasing benefit (ties by request) while the
+// running cost stays within max_cost, skipping those that do not fit.  The
+// listing's arithmetic is fp64 and every decision here is taken in fp64
+// with each operation explicitly rounded, so depths match a sequential fp64
+// evaluation bit for bit.  One CTA: per-request best depths in parallel,
+// ranks by counting, then one thread walks the ranked requests (the
+// admission is sequential by definition).
+
+namespace sv {
+
+constexpr int kCostThreads = 1024;
+
+struct DcutCostParams {
+    const float *conf;
+    const int32_t *kmax;
+    int B, Kmax;
+    double max_cost;
+    int32_t *out_depth;
+    int32_t *out_cu;
+    double *out_benefit;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ double latency_cost(int d)
+{
+    const int dep[5] = {1, 2, 4, 8, 16};
+    const double lat[5] = {1.0, 1.2, 1.5, 2.0, 3.0};
+    if (d <= dep[0])
+        return lat[0];
+    if (d >= dep[4])
+        return lat[4];
+    for (int k = 0; k < 4; ++k) {
+        if (dep[k] <= d && d <= dep[k + 1]) {
+            const double r = __ddiv_rn((double)(d - dep[k]), (double)(dep[k + 1] - dep[k]));
+            return __dadd_rn(lat[k], __dmul_rn(r, __dsub_rn(lat[k + 1], lat[k])));
+        }
+    }
+    return lat[4];
+}
+
+__global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostParams p)
+{
+    extern __shared__ __align__(16) unsigned char dsm[];
+    double *benefit = reinterpret_cast<double *>(dsm);  // [B]; < 0: no candidate
+    int *best_d = reinterpret_cast<int *>(benefit + p.B);
+    int *order = best_d + p.B;  // request at each rank
+    int *depth = order + p.B;
+    __shared__ int s_ncand;
+    const int tid = threadIdx.x;
+    if (tid == 0)
+        s_ncand = 0;
+    __syncthreads();
+
+    // 1. best depth per request; inputs validated on the way
+    int bad = 0, ncand = 0;
+    for (int r = tid; r < p.B; r += kCostThreads) {
+        int km = __ldg(p.kmax + r);
+        if (km < 0 || km > p.Kmax) {
+            bad = 1;
+            km = 0;
+        }
+        double P = 1.0, best = -1.0;
+        int bd = 0;
+        for (int d = 1; d <= km; ++d) {
+            const float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
+            if (!(c >= 0.f && c <= 1.f))
+                bad = 1;
+            P = __dmul_rn(P, (double)c);
+            const double b = __ddiv_rn(__dmul_rn(P, (double)d), latency_cost(d));
+            if (b > best) {
+                best = b;
+                bd = d;
+            }
+        }
+        benefit[r] = km > 0 ? best : -1.0;
+        best_d[r] = bd;
+        depth[r] = 0;
+        ncand += km > 0;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+        if (tid == 0)
+            set_status(p.status, ST_INVALID);
+        for (int r = tid; r < p.B; r += kCostThreads) {
+            p.out_depth[r] = -1;
+            if (p.out_benefit)
+                p.out_benefit[r] = __longlong_as_double(0x7ff8000000000000ll);
+        }
+        for (int r = tid; r <= p.B; r += kCostThreads)
+            p.out_cu[r] = -1;
+        return;
+    }
+    if (ncand)
+        atomicAdd(&s_ncand, ncand);
+
+    // 2. rank of every candidate: larger benefit first, then lower request
+    for (int r = tid; r < p.B; r += kCostThreads) {
+        const double b = benefit[r];
+        if (b < 0.0)
+            continue;
+        int rank = 0;
+        for (int q = 0; q < p.B; ++q) {
+            const double o = benefit[q];
+            rank += (o > b) || (o == b && q < r);  // no candidate has o < 0 <= b
+        }
+        order[rank] = r;
+    }
+    __syncthreads();
+
+    // 3. admission in rank order (sequential by definition)
+    if (tid == 0) {
+        double total = 0.0;
+        for (int t = 0; t < s_ncand; ++t) {
+            const int r = order[t];
+            const double c = latency_cost(best_d[r]);
+            const double nt = __dadd_rn(total, c);
+            if (nt <= p.max_cost) {
+                total = nt;
+                depth[r] = best_d[r];
+            }
+        }
+    }
+    __syncthreads();
+
+    // 4. depths, offsets, benefits of the admitted requests
+    if (tid == 0) {
+        int off = 0;
+        for (int r = 0; r < p.B; ++r) {
+            p.out_cu[r] = off;
+            off += depth[r];
+        }
+        p.out_cu[p.B] = off;
+    }
+    for (int r = tid; r < p.B; r += kCostThreads) {
+        p.out_depth[r] = depth[r];
+        if (p.out_benefit)
+            p.out_benefit[r] = depth[r] > 0 ? benefit[r] : 0.0;
+    }
+}
+
+cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t s, Tracer &tr)
+{
+    static cudaError_t once = cudaFuncSetAttribute(
+        dcut_cost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 20 * kMaxBatch);
+    if (once != cudaSuccess)
+        return once;
+    DcutCostParams p{};
+    p.conf = a.conf;
+    p.kmax = a.kmax;
+    p.B = a.B;
+    p.Kmax = a.Kmax;
+    p.max_cost = a.max_cost;
+    p.out_depth = a.out_depth;
+    p.out_cu = a.out_cu;
+    p.out_benefit = a.out_benefit;
+    const WsLayout L = ws_layout(0, 0, 0);
+    p.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
+    const size_t smem = 20 * (size_t)(a.B > 0 ? a.B : 1);
+    tr.begin(s);
+    dcut_cost_kernel<<<1, kCostThreads, smem, s>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+}  // namespace sv

@@ -54,4 +54,18 @@ struct DcutArgs {
 
 cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t stream, Tracer &tr);
 
+struct DcutCostArgs {
+    const float *conf;
+    const int32_t *kmax;
+    int B;
+    int Kmax;
+    double max_cost;
+    int32_t *out_depth;
+    int32_t *out_cu;
+    double *out_benefit;
+    void *ws;
+};
+
+cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t stream, Tracer &tr);
+
 }  // namespace sv

@@ -32,13 +32,14 @@
 // the logits at the drafted tokens) before waiting for kernel 1 to finish.
 //  - T = 0, finish_greedy_kernel: one CTA per request merges the argmax
 //    partials and runs the first-mismatch ballot.
-//  - T > 0, finish_sample_kernel: one cluster of kCluster CTAs per request.
-//    Every CTA merges the request's (m, s) partials and runs the accept test
-//    and first-rejection ballot (identical bits in every CTA), then stages
-//    its 1/kCluster of the final-draw rows with TMA and sums the weights.
-//    The range sums are exchanged through distributed shared memory; the
-//    CTA whose range holds u*S finds the token with a block scan of
-//    per-thread piece sums and one thread's walk through its piece.
+//  - T > 0, finish_sample_kernel: one cluster of 8 or 16 CTAs per request.
+//    The request's rows are merged one or two per warp of the cluster (their
+//    (m, s) and p(x) sent to every CTA through distributed shared memory);
+//    every CTA runs the accept test and first-rejection ballot (identical
+//    bits everywhere), then weighs its share of the final-draw rows into
+//    shared memory and sums the weights.  The range sums are exchanged the
+//    same way; the CTA whose range holds u*S finds the token with a block
+//    scan of per-thread piece sums and one thread's walk through its piece.
 // Every merge runs in a fixed order, so repeated calls give identical bits.
 #include <algorithm>
 #include <cfloat>
@@ -95,11 +96,12 @@ struct FinishParams {
     int64_t draft_rows;  // rows the draft side may index
     int draft_stride;
     Geometry g;
-    int R;           // vocabulary entries per cluster CTA in the final draw
-    int slice;       // entries of one row staged at a time (multiple of 16 bytes)
+    int ncl;    // CTAs per request (cluster size) in the final draw: 8 or 16
+    int R;      // vocabulary entries per cluster CTA in the final draw
+    int slice;  // entries of one row weighed at a time (multiple of 16 bytes)
     int pv;          // 16-byte vectors per thread piece of a slice (odd)
     int stage_smem;  // bytes per staged row slice (multiple of 128)
-    int tma;
+    int tma;         // rows 16-byte aligned: TMA bulk copies
     float c;
     uint32_t *status;
     const uint32_t *cu_flag;
@@ -687,10 +689,11 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
 
 constexpr int kFinishThreads = 256;
 constexpr int kFinishWarps = kFinishThreads / 32;
-constexpr int kCluster = 8;                // CTAs per request in the sampling finish kernel
+constexpr int kCluster = 16;               // most CTAs per request in the sampling finish kernel
+constexpr int kSampleThreads = 256;        // threads per CTA of the sampling finish kernel
+constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kStageRowBytes = 48 * 1024;  // largest slice of one row staged at a time
-constexpr int kMaxSlices = 96;             // slices per CTA range (bounds V)
-constexpr int kRowsPerWarp = (2 * kMaxDraft + 1 + kFinishWarps - 1) / kFinishWarps;
+constexpr int kMaxSlices = 64;             // slices per CTA range (bounds V)
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
 {
@@ -757,64 +760,13 @@ __device__ __forceinline__ void lse_combine(float &m, ff &s, float mo, ff so, fl
     m = mn;
 }
 
+// Warps wf..wl left the partials of flattened row rg, in slots rg + wf ..
+// rg + wl (warp w's units are contiguous, so its slots never collide).
 __device__ __forceinline__ void row_span(const Geometry &g, int64_t rg, int &wf, int &wl)
 {
     const int64_t ua = rg * g.cpr;
     wf = owner_of(ua, g);
     wl = owner_of(ua + g.cpr - 1, g);
-}
-
-// Merge the partials of up to kRowsPerWarp flattened rows per warp, all
-// loads issued before any is used.  rows(k) gives the k-th row of the
-// request (k < n); warp w takes k = w, w + kFinishWarps, ...  Results go to
-// row_m / row_s (lane 0).
-template <typename RowOf>
-__device__ __forceinline__ void merge_softmax_rows(const Partial *part, const Geometry &g, int n,
-                                                   RowOf rows, float c, float *row_m,
-                                                   ff *row_s)
-{
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    Partial first[kRowsPerWarp];
-#pragma unroll
-    for (int t = 0; t < kRowsPerWarp; ++t) {
-        const int k = warp + t * kFinishWarps;
-        first[t].m = -INFINITY;
-        first[t].s_hi = 0.f;
-        first[t].s_lo = 0.f;
-        if (k < n) {
-            const int64_t rg = rows(k);
-            int wf, wl;
-            row_span(g, rg, wf, wl);
-            if (wf + lane <= wl)
-                first[t] = load_partial(part + rg + wf + lane);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < kRowsPerWarp; ++t) {
-        const int k = warp + t * kFinishWarps;
-        if (k >= n)
-            break;
-        float m = -INFINITY;
-        ff s{0.f, 0.f};
-        lse_combine(m, s, first[t].m, {first[t].s_hi, first[t].s_lo}, c);
-        const int64_t rg = rows(k);
-        int wf, wl;
-        row_span(g, rg, wf, wl);
-        for (int w = wf + lane + 32; w <= wl; w += 32) {  // rows split over more than 32 warps
-            const Partial q = load_partial(part + rg + w);
-            lse_combine(m, s, q.m, {q.s_hi, q.s_lo}, c);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, m, o);
-            const ff so = ff_shfl_xor(s, o);
-            lse_combine(m, s, mo, so, c);
-        }
-        if (lane == 0) {
-            row_m[k] = m;
-            row_s[k] = s;
-        }
-    }
 }
 
 // T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
@@ -863,7 +815,7 @@ __device__ __forceinline__ float softmax_at(float g, float m, ff s, float c)
     const float xh = __fmul_rn(d.hi, c);
     const float xl = fmaf(d.lo, c, fmaf(d.hi, c, -xh));
     const float num = __fmul_rn(exp2f(xh), fmaf(xl, 0.69314718f, 1.f));
-    const float inv = __fdiv_rn(1.f, s.hi);
+    const float inv = __frcp_rn(s.hi);
     return __fmul_rn(__fmul_rn(num, inv), fmaf(-s.lo, inv, 1.f));
 }
 
@@ -929,7 +881,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const Fin
 // f / s for a float-float s.
 __device__ __forceinline__ float ff_recip_scaled(float f, ff s)
 {
-    const float inv = __fdiv_rn(1.f, s.hi);
+    const float inv = __frcp_rn(s.hi);
     return __fmul_rn(__fmul_rn(f, inv), fmaf(-s.lo, inv, 1.f));
 }
 
@@ -939,30 +891,56 @@ struct DrawCtx {
     float sc_t, sc_d;   // 2^(fl(m c) - m c) / s: normalisers including the rounding fix
 };
 
-// Final-draw weight of one element.  Every operation is explicitly rounded,
-// so the summing pass and the search pass compute identical bits.
+// Final-draw weight of one element: max(0, p - q) after a rejection, the
+// unnormalised p for the bonus draw (or an all-zero residual).
 __device__ __forceinline__ float draw_w(const DrawCtx &d, float t, float x)
 {
     const float pt = ex2_approx(fmaf(t, d.c, -d.mct));
     if (!d.resid)
-        return pt;  // bonus draw (or all-zero residual): unnormalised p
+        return pt;
     const float pd = ex2_approx(fmaf(x, d.c, -d.mcd));
-    return fmaxf(__fsub_rn(__fmul_rn(pt, d.sc_t), __fmul_rn(pd, d.sc_d)), 0.f);
+    return fmaxf(fmaf(pt, d.sc_t, -__fmul_rn(pd, d.sc_d)), 0.f);
 }
 
-// Walk one thread's contiguous piece (16-byte vectors [v0, v1) of a staged
-// slice of len elements) in index order, summing the weights in fp32.  With
-// rem finite, stop at the first element whose running sum exceeds rem and
-// return its index in the slice (-1 if none); *sum gets the running sum.
+// Sum of the final-draw weights of one thread's contiguous piece (16-byte
+// vectors [v0, v1) of a staged slice of len elements), in index order, fp32.
 template <typename T>
-__device__ __forceinline__ int walk_piece(const DrawCtx &d, const T *tb, const T *db, int len,
-                                          int v0, int v1, float rem, float *sum, int *last_pos)
+__device__ __forceinline__ float piece_sum(const DrawCtx d, const T *tb, const T *db, int len,
+                                           int v0, int v1)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(db);
+    float acc = 0.f;
+#pragma unroll 1
+    for (int v = v0; v < v1; ++v) {
+        float ft[E], fd[E];
+        Elem<T>::unpack(tv[v], ft);
+        if (d.resid)
+            Elem<T>::unpack(dv[v], fd);
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+            const float w = v * E + h < len ? draw_w(d, ft[h], d.resid ? fd[h] : 0.f) : 0.f;
+            acc = __fadd_rn(acc, w);
+        }
+    }
+    return acc;
+}
+
+// The same walk, stopping at the first element whose running sum exceeds
+// rem: its index in the slice, or (none) the last element with weight > 0
+// (-1 if there is none).  The running sums are those of piece_sum, bit for
+// bit.
+template <typename T>
+__device__ __forceinline__ int piece_find(const DrawCtx d, const T *tb, const T *db, int len,
+                                          int v0, int v1, float rem)
 {
     constexpr int E = Elem<T>::kPerVec;
     const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
     const uint4 *dv = reinterpret_cast<const uint4 *>(db);
     float acc = 0.f;
     int lastp = -1;
+#pragma unroll 1
     for (int v = v0; v < v1; ++v) {
         float ft[E], fd[E];
         Elem<T>::unpack(tv[v], ft);
@@ -975,119 +953,149 @@ __device__ __forceinline__ int walk_piece(const DrawCtx &d, const T *tb, const T
             acc = __fadd_rn(acc, w);
             if (w > 0.f)
                 lastp = k;
-            if (acc > rem) {
-                *sum = acc;
-                *last_pos = lastp;
+            if (acc > rem)
                 return k;
-            }
         }
     }
-    *sum = acc;
-    *last_pos = lastp;
-    return -1;
+    return lastp;
 }
 
-// Stage elements [col0, col0 + len) of the draw rows into shared memory.
-// Once any copy of this call has timed out, nothing more is copied (the
-// request's outputs are poisoned).
+// Stage elements [c0, c0 + len) of the draw rows into shared memory (one
+// TMA bulk copy per row, or plain loads when the rows are not 16-byte
+// aligned), then every thread sums its contiguous piece (kept in piece[]
+// for the search) and the pieces are added as float-float pairs in a fixed
+// order.  Once any copy of this call has timed out nothing more is copied.
 template <typename T>
-__device__ __forceinline__ void stage_slice(const FinishParams &p, const T *trow, const T *drow,
-                                            bool resid, int col0, int len, T *tb, T *db,
-                                            uint64_t *bar, uint32_t &phase)
-{
-    if (__syncthreads_or(threadIdx.x == 0 && (read_status(p.status) & ST_TIMEOUT)) || len <= 0)
-        return;
-    if (p.tma) {
-        if (threadIdx.x == 0) {
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
-            mbar_arrive_expect_tx(bar, resid ? 2 * bytes : bytes);
-            bulk_g2s(tb, trow + col0, bytes, bar);
-            if (resid)
-                bulk_g2s(db, drow + col0, bytes, bar);
-        }
-        if (!mbar_wait_bounded(bar, phase)) {
-            set_status(p.status, ST_TIMEOUT);
-            mbar_wait_bounded(bar, phase);  // the copy in flight, once more
-        }
-        phase ^= 1u;
-    } else {
-        for (int k = threadIdx.x; k < len; k += kFinishThreads) {
-            tb[k] = trow[col0 + k];
-            if (resid)
-                db[k] = drow[col0 + k];
-        }
-        __syncthreads();
-    }
-}
-
-// Sum of the draw weights of a staged slice: every thread sums its
-// contiguous piece (kept in piece[] for the search), then the pieces are
-// added in fp64 in a fixed order.
-template <typename T>
-__device__ __forceinline__ ff slice_sum(const DrawCtx &d, const T *tb, const T *db, int len,
-                                        int pv, float *piece, ff *wred)
+__device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, const T *trow,
+                                       const T *drow, int c0, int len, T *tb, T *db,
+                                       uint64_t *bar, uint32_t *phase, float *piece, ff *wred,
+                                       int *expired)
 {
     constexpr int E = Elem<T>::kPerVec;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // earlier readers of the buffers, piece and wred are done
+    const bool stop = __syncthreads_or(tid == 0 && (read_status(p.status) & ST_TIMEOUT));
+    if (!stop && len > 0) {
+        if (p.tma) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
+                mbar_arrive_expect_tx(bar, d.resid ? 2 * bytes : bytes);
+                bulk_g2s(tb, trow + c0, bytes, bar);
+                if (d.resid)
+                    bulk_g2s(db, drow + c0, bytes, bar);
+            }
+            if (!mbar_wait_bounded(bar, *phase)) {
+                set_status(p.status, ST_TIMEOUT);
+                *expired = 1;
+                mbar_wait_bounded(bar, *phase);  // the copy in flight, once more
+            }
+            *phase ^= 1u;
+        } else {
+            for (int k = tid; k < len; k += kSampleThreads) {
+                tb[k] = trow[c0 + k];
+                if (d.resid)
+                    db[k] = drow[c0 + k];
+            }
+            __syncthreads();
+        }
+    }
     const int nv = (len + E - 1) / E;
-    const int v0 = min(nv, threadIdx.x * pv), v1 = min(nv, v0 + pv);
-    float ps;
-    int lp;
-    walk_piece<T>(d, tb, db, len, v0, v1, INFINITY, &ps, &lp);
-    piece[threadIdx.x] = ps;
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    const float ps = piece_sum<T>(d, tb, db, len, v0, v1);
+    piece[tid] = ps;
     const ff ws = warp_sum_ff({ps, 0.f});
     __syncthreads();  // piece[] complete; wred free
     if (lane == 0)
         wred[warp] = ws;
     __syncthreads();
     ff tot = wred[0];
-#pragma unroll
-    for (int w = 1; w < kFinishWarps; ++w)
-        tot = ff_add(tot, wred[w]);
+    for (int q = 1; q < kSampleWarps; ++q)
+        tot = ff_add(tot, wred[q]);
     return tot;
 }
 
+// Store (m, s, p(x)) of row k into the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_row(float *row_m, ff *row_s, float *row_p, int k,
+                                               uint32_t rank, float m, ff s, float px)
+{
+    uint32_t rm, rs, rp;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rm) : "r"(smem_u32(row_m + k)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(smem_u32(row_s + k)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rp) : "r"(smem_u32(row_p + k)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rm), "f"(m) : "memory");
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(rs), "f"(s.hi), "f"(s.lo)
+                 : "memory");
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rp), "f"(px) : "memory");
+}
+
 template <typename T>
-__global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const FinishParams p)
+__global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
-    T *tb = reinterpret_cast<T *>(dsm);
-    T *db = reinterpret_cast<T *>(dsm + p.stage_smem);
+    T *tb = reinterpret_cast<T *>(dsm);  // staged slice of the target row
+    T *db = reinterpret_cast<T *>(dsm + p.stage_smem);  // and of the draft row
     __shared__ __align__(8) uint64_t bar;
-    __shared__ float row_m[2 * kMaxDraft + 1];
-    __shared__ ff row_s[2 * kMaxDraft + 1];
-    __shared__ float piece[kFinishThreads];
-    __shared__ ff wred[kFinishWarps];
+    __shared__ float row_m[2 * kMaxDraft + 1];            // written by every CTA of the cluster
+    __shared__ __align__(8) ff row_s[2 * kMaxDraft + 1];  // likewise
+    __shared__ float row_p[2 * kMaxDraft + 1];            // likewise: p_j(x_j), q_j(x_j)
+    __shared__ float piece[kSampleThreads];
+    __shared__ ff wred[kSampleWarps];
     __shared__ ff slice_tot[kMaxSlices];
     __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
-    __shared__ ff s_excl[kFinishWarps];
-    __shared__ int s_a, s_bad, s_hit, s_last;
+    __shared__ ff s_excl[kSampleWarps];
+    __shared__ int s_a, s_bad, s_hit, s_last, s_cs, s_past, s_redo, s_expired;
+    __shared__ ff s_base, s_target;
+    __shared__ DrawCtx s_d;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_ctarank();
-    const int i = blockIdx.x / kCluster;
+    const int ncl = p.ncl;
+    const int i = blockIdx.x / ncl;
+    const T *tbase = reinterpret_cast<const T *>(p.target);
+    const T *dbase = reinterpret_cast<const T *>(p.draft);
 
     // ---- inputs that do not depend on kernel 1, read before waiting for it
     if (tid == 0) {
         mbar_init(&bar, 1);
         fence_mbar_init();
+        s_expired = 0;
     }
     const int cu_i = __ldg(p.cu + i);
     const int K = __ldg(p.cu + i + 1) - cu_i;
     const bool shape = request_shape_ok(p, i, cu_i, K);
     const int64_t t0 = (int64_t)cu_i + i;
+    const int nrows = 2 * K + 1;
+    // warp 0, lane j < K: the drafted token and its uniform (accept test)
     const bool act = shape && warp == 0 && lane < K;
     int x = -1;
-    float u = 0.f, gt = 0.f, gd = 0.f;
+    float u = 0.f;
     int64_t di = 0;
     if (act) {
         di = draft_index(p.draft_stride, p.cu, i, lane);
         x = __ldg(p.tokens + di);
         u = __ldg(p.u_accept + di);
-        if (x >= 0 && x < p.V) {
-            gt = Elem<T>::ld_global(reinterpret_cast<const T *>(p.target) + (t0 + lane) * p.V, x);
-            gd = Elem<T>::ld_global(reinterpret_cast<const T *>(p.draft) + di * p.V, x);
+    }
+    // the rows this warp merges (k = rank + ncl * (warp + kSampleWarps * t)):
+    // target rows 0..K, then draft rows 0..K-1; the logit at the drafted
+    // token of each such row
+    int my_k[2];
+    float g[2] = {-INFINITY, -INFINITY};
+    bool g_ok[2] = {false, false};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        my_k[t] = (int)rank + ncl * (warp + kSampleWarps * t);
+        if (!shape || my_k[t] >= nrows)
+            my_k[t] = -1;
+        else if (my_k[t] != K) {
+            const int j = my_k[t] < K ? my_k[t] : my_k[t] - K - 1;
+            const int64_t dj = draft_index(p.draft_stride, p.cu, i, j);
+            const int xj = __ldg(p.tokens + dj);
+            if (xj >= 0 && xj < p.V) {
+                g_ok[t] = true;
+                g[t] = my_k[t] < K ? Elem<T>::ld_global(tbase + (t0 + j) * p.V, xj)
+                                   : Elem<T>::ld_global(dbase + dj * p.V, xj);
+            }
         }
     }
     const float uf = __ldg(p.u_final + i);
@@ -1095,27 +1103,54 @@ __global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const 
     pdl_wait();  // kernel 1 has completed and its writes are visible
     if (__ldcg(p.cu_flag) == 0u || !shape)
         return;  // malformed offsets: kernel 1 poisoned every output (same in every CTA)
+    cluster_arrive_relaxed();  // (0) this CTA has started
+    // an expired wait of kernel 1 only poisons; its flag is read now, off the
+    // critical path
+    const bool timeout = warp == 0 && (read_status(p.status) & ST_TIMEOUT);
 
-    // ---- (m, s) of the request's 2K+1 rows: target rows 0..K, then draft rows
-    const int64_t gmr = p.g.max_rows;
-    merge_softmax_rows(
-        p.part, p.g, 2 * K + 1,
-        [&](int k) -> int64_t { return k <= K ? t0 + k : gmr + cu_i + (k - K - 1); }, p.c,
-        row_m, row_s);
-    __syncthreads();
+    // ---- (m, s) and p(x) of the request's rows, one or two rows per warp of
+    // the cluster, sent to every CTA
+    float mm[2] = {-INFINITY, -INFINITY}, px[2] = {0.f, 0.f};
+    ff sm[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (my_k[t] < 0)
+            continue;
+        const int k = my_k[t];
+        const int64_t rg = k <= K ? t0 + k : p.g.max_rows + cu_i + (k - K - 1);
+        int wf, wl;
+        row_span(p.g, rg, wf, wl);
+        for (int w = wf + lane; w <= wl; w += 32) {
+            const Partial pt = load_partial(p.part + rg + w);
+            lse_combine(mm[t], sm[t], pt.m, {pt.s_hi, pt.s_lo}, p.c);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mm[t], o);
+            const ff so = ff_shfl_xor(sm[t], o);
+            lse_combine(mm[t], sm[t], mo, so, p.c);
+        }
+        px[t] = g_ok[t] && row_ok(mm[t], sm[t]) ? softmax_at(g[t], mm[t], sm[t], p.c) : 0.f;
+    }
+    cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        if (my_k[t] >= 0 && lane < ncl)
+            st_cluster_row(row_m, row_s, row_p, my_k[t], (uint32_t)lane, mm[t], sm[t], px[t]);
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
 
     // ---- accept test and first rejection (warp 0; identical in every CTA)
     if (warp == 0) {
         bool bad_tok = act && (x < 0 || x >= p.V), bad_nf = false, acc = true;
         float pp = 0.f, qq = 0.f;
         if (act && !bad_tok) {
-            const float mt = row_m[lane], md = row_m[K + 1 + lane];
-            const ff st = row_s[lane], sd = row_s[K + 1 + lane];
-            if (!row_ok(mt, st) || !row_ok(md, sd)) {
+            if (!row_ok(row_m[lane], row_s[lane]) ||
+                !row_ok(row_m[K + 1 + lane], row_s[K + 1 + lane])) {
                 bad_nf = true;
             } else {
-                pp = softmax_at(gt, mt, st, p.c);
-                qq = softmax_at(gd, md, sd, p.c);
+                pp = row_p[lane];
+                qq = row_p[K + 1 + lane];
                 const float ratio = qq > 0.f ? __fdiv_rn(pp, qq) : (pp > 0.f ? INFINITY : 0.f);
                 acc = u < ratio;
             }
@@ -1128,7 +1163,6 @@ __global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const 
         // bad depends only on the request's data, so every CTA of the cluster
         // takes the same branch; an expired wait only poisons (best effort)
         const bool bad = nf || bt;
-        const bool timeout = read_status(p.status) & ST_TIMEOUT;
         const int a = rej ? __ffs(rej) - 1 : K;
         if (rank == 0) {  // the request's outputs, written once
             if (bad || timeout) {
@@ -1156,103 +1190,101 @@ __global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const 
         if (lane == 0) {
             s_a = a;
             s_bad = bad;
+            // the final draw's constants, once for the CTA
+            DrawCtx d0;
+            d0.resid = a < K;
+            d0.c = p.c;
+            const float mt = row_m[a];
+            d0.mct = mt * p.c;
+            d0.sc_t = ff_recip_scaled(mc_correction(mt, d0.mct, p.c), row_s[a]);
+            d0.mcd = 0.f;
+            d0.sc_d = 0.f;
+            if (d0.resid) {
+                const float md = row_m[K + 1 + a];
+                d0.mcd = md * p.c;
+                d0.sc_d = ff_recip_scaled(mc_correction(md, d0.mcd, p.c), row_s[K + 1 + a]);
+            }
+            s_d = d0;
         }
     }
     __syncthreads();
     if (s_bad)
-        return;  // same decision in every CTA of the cluster
+        return;  // same decision in every CTA of the cluster; no more cluster traffic
 
-    // ---- final draw: this CTA sums the weights of its range of the vocabulary
+    // ---- final draw: this CTA weighs its range of the vocabulary
     const int a = s_a;
     const int64_t trow_i = t0 + a;
     const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
-    DrawCtx d;
-    d.resid = drow_i >= 0;
-    d.c = p.c;
-    {
-        const float mt = row_m[a];
-        d.mct = mt * p.c;
-        d.sc_t = ff_recip_scaled(mc_correction(mt, d.mct, p.c), row_s[a]);
-        if (d.resid) {
-            const float md = row_m[K + 1 + a];
-            d.mcd = md * p.c;
-            d.sc_d = ff_recip_scaled(mc_correction(md, d.mcd, p.c), row_s[K + 1 + a]);
-        } else {
-            d.mcd = 0.f;
-            d.sc_d = 0.f;
-        }
-    }
-    const T *trow = reinterpret_cast<const T *>(p.target) + trow_i * p.V;
-    const T *drow = d.resid ? reinterpret_cast<const T *>(p.draft) + drow_i * p.V : nullptr;
+    DrawCtx d = s_d;
+    const T *trow = tbase + trow_i * p.V;
+    const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
     const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
     const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+    int weighed = -1;  // slice staged in shared memory
     uint32_t phase = 0;
-    int staged = -1;  // slice currently in shared memory
 
-    cluster_arrive_relaxed();  // (1) every CTA of the cluster has started
-    auto range_sum = [&]() -> ff {
-        ff tot{0.f, 0.f};
+    // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
+    // second pass over p_a (the same decision in every CTA)
+    int slot = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        ff mine{0.f, 0.f};
         for (int sl = 0; sl < nsl; ++sl) {
             const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-            stage_slice<T>(p, trow, drow, d.resid, c0, len, tb, db, &bar, phase);
-            staged = sl;
-            const ff ss = slice_sum<T>(d, tb, db, len, p.pv, piece, wred);
+            const ff ss = weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
+                                         wred, &s_expired);
+            weighed = sl;
             if (tid == 0)
                 slice_tot[sl] = ss;
-            tot = ff_add(tot, ss);
+            mine = ff_add(mine, ss);
         }
-        return tot;
-    };
-    ff mine = range_sum();
-    cluster_wait_acquire();  // (1) complete: remote shared memory is live
-    if (tid < kCluster)
-        st_cluster_ff(&cl_sum[0][rank], (uint32_t)tid, mine);
-    cluster_arrive_release();
-    cluster_wait_acquire();  // (2) every CTA holds every range sum
-    int slot = 0;
-    ff S = cl_sum[0][0];
-    for (int r = 1; r < kCluster; ++r)
-        S = ff_add(S, cl_sum[0][r]);
-    if (d.resid && !(S.hi > 0.f)) {  // all-zero residual: draw from p_a instead
-        d.resid = false;
-        mine = range_sum();
-        if (tid < kCluster)
-            st_cluster_ff(&cl_sum[1][rank], (uint32_t)tid, mine);
+        if (tid < ncl)
+            st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
         cluster_arrive_release();
-        cluster_wait_acquire();  // (3)
-        slot = 1;
-        S = cl_sum[1][0];
-        for (int r = 1; r < kCluster; ++r)
-            S = ff_add(S, cl_sum[1][r]);
+        cluster_wait_acquire();  // (2 + pass) every CTA holds every range sum
+        slot = pass;
+        // S and the range holding u*S, by warp 0 (lane r holds range r): an
+        // inclusive float-float scan in range order, the same in every CTA.
+        // `past` marks u*S at or beyond the end after rounding: then the
+        // last weight > 0 wins.
+        if (warp == 0) {
+            const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
+            ff incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff n = ff_shfl_up(incl, o);
+                if (lane >= o)
+                    incl = ff_add(n, incl);
+            }
+            const ff S = {__shfl_sync(0xffffffffu, incl.hi, 31),
+                          __shfl_sync(0xffffffffu, incl.lo, 31)};
+            const ff target = ff_mul(S, uf);
+            const unsigned over = __ballot_sync(0xffffffffu, lane < ncl && ff_gt(incl, target));
+            const unsigned mass = __ballot_sync(0xffffffffu, lane < ncl && v.hi > 0.f);
+            const int cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
+            ff excl = ff_shfl_up(incl, 1);
+            if (lane == 0)
+                excl = {0.f, 0.f};
+            const int src = cs < 0 ? 0 : cs;
+            const ff base = {__shfl_sync(0xffffffffu, excl.hi, src),
+                             __shfl_sync(0xffffffffu, excl.lo, src)};
+            if (lane == 0) {
+                s_cs = cs;
+                s_past = over == 0u;
+                s_base = base;
+                s_target = target;
+                s_redo = !(S.hi > 0.f);
+            }
+        }
+        __syncthreads();
+        if (!(d.resid && s_redo))
+            break;
+        d.resid = false;  // all-zero residual: draw from p_a instead
     }
     // no shared memory of another CTA is touched after this point
-
-    // ---- the range holding u*S (same choice in every CTA); `past` marks
-    // u*S at or beyond the end after rounding: then the last weight > 0 wins
-    const ff target = ff_mul(S, uf);
-    bool past = false;
-    ff base{0.f, 0.f}, cum{0.f, 0.f};
-    int cs = -1;
-    for (int r = 0; r < kCluster; ++r) {
-        const ff v = cl_sum[slot][r];
-        const ff next = ff_add(cum, v);
-        if (cs < 0 && ff_gt(next, target)) {
-            cs = r;
-            base = cum;
-        }
-        cum = next;
-    }
-    if (cs < 0) {
-        past = true;
-        cum = {0.f, 0.f};
-        for (int r = 0; r < kCluster; ++r) {
-            if (cl_sum[slot][r].hi > 0.f) {
-                cs = r;
-                base = cum;
-            }
-            cum = ff_add(cum, cl_sum[slot][r]);
-        }
-    }
+    const int cs = s_cs;
+    bool past = s_past != 0;
+    ff base = s_base;
+    const ff target = s_target;
     if ((int)rank != cs) {
         if (cs < 0 && rank == 0 && tid == 0) {  // no mass at all (never with finite rows)
             set_status(p.status, ST_NONFINITE);
@@ -1291,10 +1323,8 @@ __global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const 
         }
     }
     const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-    if (sl != staged) {
-        stage_slice<T>(p, trow, drow, d.resid, c0, len, tb, db, &bar, phase);
-        slice_sum<T>(d, tb, db, len, p.pv, piece, wred);
-    }
+    if (sl != weighed)
+        weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
     // scan of the piece sums (float-float, fixed order).  A piece's lower end
     // is the previous piece's upper end bit for bit, so the pieces tile the
     // slice with no gap and no overlap.
@@ -1308,52 +1338,41 @@ __global__ void __launch_bounds__(kFinishThreads, 2) finish_sample_kernel(const 
     ff excl = ff_shfl_up(incl, 1);
     if (lane == 0)
         excl = {0.f, 0.f};
-    if (tid == 0)
+    if (tid == 0) {
         s_hit = INT_MAX;
+        s_last = -1;
+    }
     if (lane == 31)
         s_excl[warp] = incl;
     __syncthreads();
     ff wbase = base;
-    for (int w = 0; w < warp; ++w)
-        wbase = ff_add(wbase, s_excl[w]);
+    for (int q = 0; q < warp; ++q)
+        wbase = ff_add(wbase, s_excl[q]);
     const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
     if (!past && ff_le(lo, target) && ff_gt(hi, target))
         atomicMin(&s_hit, tid);
     __syncthreads();
-    int res = -1;
+    // the piece walk repeats the piece sum's additions, so it meets the same
+    // running sums; rem may round up to the piece total: then the piece's
+    // last element with weight > 0
     constexpr int E = Elem<T>::kPerVec;
     const int nv = (len + E - 1) / E;
-    if (s_hit != INT_MAX) {
-        if (tid == s_hit) {
-            const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
-            float ps;
-            int lp;
-            const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
-            int k = walk_piece<T>(d, tb, db, len, v0, v1, rem, &ps, &lp);
-            if (k < 0)
-                k = lp;  // rem rounded up to the piece total: its last element with mass
-            s_last = k;
-        }
-        __syncthreads();
-        res = s_last;
-    } else {  // past the end after rounding: the last element with mass
-        if (tid == 0)
-            s_last = -1;
-        __syncthreads();
-        const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
-        float ps;
-        int lp;
-        walk_piece<T>(d, tb, db, len, v0, v1, INFINITY, &ps, &lp);
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    if (s_hit == tid) {
+        const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+        s_last = piece_find<T>(d, tb, db, len, v0, v1, rem);
+    } else if (s_hit == INT_MAX) {  // past the end after rounding: the last element with mass
+        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
         if (lp >= 0)
             atomicMax(&s_last, lp);
-        __syncthreads();
-        res = s_last;
     }
+    __syncthreads();
     if (tid == 0) {
+        const int res = s_last;
         int y = res >= 0 ? c0 + res : -1;
         if (y < 0)
             set_status(p.status, ST_NONFINITE);
-        if (read_status(p.status) & ST_TIMEOUT) {  // staged data may be stale
+        if (timeout || s_expired) {  // a copy gave up: the data may be stale
             y = -1;
             p.out_len[i] = -1;
             for (int jj = 0; jj <= K; ++jj)
@@ -1434,9 +1453,13 @@ template <typename T>
 static cudaError_t prepare_finish_sample()
 {
     static cudaError_t once = [] {
-        return cudaFuncSetAttribute(finish_sample_kernel<T>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    2 * kStageRowBytes);
+        cudaError_t e = cudaFuncSetAttribute(finish_sample_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             2 * kStageRowBytes);
+        if (e == cudaSuccess)  // clusters of 16 CTAs
+            e = cudaFuncSetAttribute(finish_sample_kernel<T>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e;
     }();
     return once;
 }
@@ -1490,14 +1513,18 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
     fp.draft_stride = a.draft_stride;
     fp.g = g;
-    {  // final-draw geometry: kCluster ranges of R entries, staged in slices
+    {  // final-draw geometry: ncl ranges of R entries, weighed in slices.  16
+        // CTAs per request while the clusters fit the GPU at one CTA per SM
+        // (larger clusters are harder to place), else 8.
         const int gran = 16 / e;
-        const int R = (int)((((int64_t)a.V + kCluster - 1) / kCluster + gran - 1) / gran * gran);
+        const int ncl = (int64_t)a.B * kCluster <= (int64_t)sm_count() ? kCluster : kCluster / 2;
+        fp.ncl = ncl;
+        const int R = (int)((((int64_t)a.V + ncl - 1) / ncl + gran - 1) / gran * gran);
         const int slice = std::min(R, kStageRowBytes / e);
         const int nv = (slice * e + 15) / 16;
         fp.R = R;
         fp.slice = slice;
-        fp.pv = ((nv + kFinishThreads - 1) / kFinishThreads) | 1;  // odd: no bank conflicts
+        fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
         fp.stage_smem = (int)align_up((size_t)slice * e, 128);
         if ((R + slice - 1) / slice > kMaxSlices)
             return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
@@ -1535,10 +1562,11 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
         cfg.numAttrs = 1;
         err = cudaLaunchKernelEx(&cfg, finish_greedy_kernel<T>, fp);
     } else {
-        cfg.gridDim = dim3((unsigned)(a.B * kCluster));
+        cfg.gridDim = dim3((unsigned)(a.B * fp.ncl));
+        cfg.blockDim = dim3(kSampleThreads);
         cfg.dynamicSmemBytes = 2 * (size_t)fp.stage_smem;
         attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = kCluster;
+        attr[1].val.clusterDim.x = fp.ncl;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;

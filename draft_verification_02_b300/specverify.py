@@ -31,7 +31,7 @@ SPEC_DCUT_MAX_CANDIDATES = 8192
 EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
            "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
-           "spec_verify_sample_static")
+           "spec_verify_sample_static", "dcut_allocate_cost")
 SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -63,6 +63,8 @@ def _load():
                                               P, P, P, P, P]
     lib.spec_verify_sample_static.restype = INT
     lib.dcut_allocate.argtypes = [P, P, I32, I32, I32, F32, P, P, P, P, SZ, P]
+    lib.dcut_allocate_cost.argtypes = [P, P, I32, I32, ctypes.c_double, P, P, P, P, SZ, P]
+    lib.dcut_allocate_cost.restype = INT
     lib.dcut_allocate.restype = INT
     lib.spec_get_device_status.argtypes = [P, P]
     lib.spec_get_device_status.restype = INT
@@ -219,6 +221,18 @@ def dcut_allocate(conf, kmax, B: int, Kmax: int, budget: int, min_gain: float, o
         _dev(out_depth, "out_depth", torch.int32, B, allow_none=B == 0),
         _dev(out_cu, "out_cu", torch.int32, B + 1),
         _dev(out_expected_len, "out_expected_len", torch.float32, B, allow_none=True),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def dcut_allocate_cost(conf, kmax, B: int, Kmax: int, max_cost: float, out_depth, out_cu,
+                       out_benefit, workspace, stream=None) -> int:
+    return LIB.dcut_allocate_cost(
+        _dev(conf, "conf", torch.float32, B * Kmax, allow_none=B * Kmax == 0),
+        _dev(kmax, "kmax", torch.int32, B, allow_none=B == 0), B, Kmax, float(max_cost),
+        _dev(out_depth, "out_depth", torch.int32, B, allow_none=B == 0),
+        _dev(out_cu, "out_cu", torch.int32, B + 1),
+        _dev(out_benefit, "out_benefit", torch.float64, B, allow_none=True),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
 

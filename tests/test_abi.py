@@ -95,6 +95,17 @@ def test_host_checks_reject_before_any_launch():
                            null) == sv.SPEC_ERR_INVALID_ARG  # 16384 candidates
     assert L.dcut_allocate(FAKE, FAKE, 4, 4, 4, 0.0, FAKE, FAKE, null, null, 0,
                            null) == sv.SPEC_ERR_WORKSPACE
+    # D-cut, cost-unit variant
+    assert L.dcut_allocate_cost(FAKE, FAKE, -1, 4, 4.0, FAKE, FAKE, null, FAKE, 1 << 20,
+                                null) == sv.SPEC_ERR_INVALID_ARG
+    assert L.dcut_allocate_cost(FAKE, FAKE, 4, 33, 4.0, FAKE, FAKE, null, FAKE, 1 << 20,
+                                null) == sv.SPEC_ERR_INVALID_ARG
+    assert L.dcut_allocate_cost(FAKE, FAKE, 4, 4, float("nan"), FAKE, FAKE, null, FAKE, 1 << 20,
+                                null) == sv.SPEC_ERR_INVALID_ARG
+    assert L.dcut_allocate_cost(FAKE, FAKE, 4097, 4, 4.0, FAKE, FAKE, null, FAKE, 1 << 20,
+                                null) == sv.SPEC_ERR_INVALID_ARG
+    assert L.dcut_allocate_cost(FAKE, FAKE, 4, 4, 4.0, FAKE, FAKE, null, null, 0,
+                                null) == sv.SPEC_ERR_WORKSPACE
 
 
 def test_trace_hook_arguments():
