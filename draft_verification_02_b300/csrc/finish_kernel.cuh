@@ -1,0 +1,708 @@
+// finish_kernel.cuh - kernel 2 of the verification path: merge, accept test
+// and final draw (see verify.cu for the whole path).
+#pragma once
+
+#include "verify_params.cuh"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// kernel 2: merge, accept test, final draw
+// ---------------------------------------------------------------------------
+
+constexpr int kFinishThreads = 256;
+constexpr int kFinishWarps = kFinishThreads / 32;
+constexpr int kCluster = 16;               // most CTAs per request in the sampling finish kernel
+constexpr int kSampleThreads = 256;        // threads per CTA of the sampling finish kernel
+constexpr int kSampleWarps = kSampleThreads / 32;
+constexpr int kStageRowBytes = 48 * 1024;  // largest slice of one row staged at a time
+constexpr int kMaxSlices = 64;             // slices per CTA range (bounds V)
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store v at the address `local` has in the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_ff(ff *local, uint32_t rank, ff v)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.hi), "f"(v.lo)
+                 : "memory");
+}
+
+// One partial, read from L2 in a single 16-byte load.
+__device__ __forceinline__ Partial load_partial(const Partial *p)
+{
+    const uint4 r = __ldcg(reinterpret_cast<const uint4 *>(p));
+    Partial out;
+    out.m = __uint_as_float(r.x);
+    out.idx = (int32_t)r.y;
+    out.s_hi = __uint_as_float(r.z);
+    out.s_lo = __uint_as_float(r.w);
+    return out;
+}
+
+// Combine two softmax partials (m, s), s = sum exp2((x - m) c) held as a
+// float-float pair.  The result does not depend on the order of the two
+// arguments, so a butterfly over a warp leaves the same bits in every lane.
+__device__ __forceinline__ void lse_combine(float &m, ff &s, float mo, ff so, float c)
+{
+    if (so.hi == 0.f)
+        return;  // empty or fully masked partial
+    if (s.hi == 0.f) {
+        m = mo;
+        s = so;
+        return;
+    }
+    const float mn = max_nan(m, mo);
+    if (mn != mn || s.hi != s.hi || so.hi != so.hi) {
+        m = __int_as_float(0x7fc00000);
+        s = {__int_as_float(0x7fc00000), 0.f};
+        return;
+    }
+    s = ff_add(ff_mul(s, exp2f((m - mn) * c)), ff_mul(so, exp2f((mo - mn) * c)));
+    m = mn;
+}
+
+// Warps wf..wl left the partials of flattened row rg, in slots rg + wf ..
+// rg + wl (warp w's units are contiguous, so its slots never collide).
+__device__ __forceinline__ void row_span(const Geometry &g, int64_t rg, int &wf, int &wl)
+{
+    const int64_t ua = rg * g.cpr;
+    wf = owner_of(ua, g);
+    wl = owner_of(ua + g.cpr - 1, g);
+}
+
+// T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
+__device__ __forceinline__ int merge_argmax_row(const Partial *part, const Geometry &g, int64_t rg)
+{
+    const int lane = threadIdx.x & 31;
+    int wf, wl;
+    row_span(g, rg, wf, wl);
+    float best = -INFINITY;
+    int bidx = INT_MAX, nan = 0;
+    for (int w = wf + lane; w <= wl; w += 32) {
+        const Partial q = load_partial(part + rg + w);
+        if (q.idx == -2)
+            nan = 1;
+        else if (q.idx >= 0 && (q.m > best || (q.m == best && q.idx < bidx))) {
+            best = q.m;
+            bidx = q.idx;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bidx, o);
+        if (ob > best || (ob == best && oi < bidx)) {
+            best = ob;
+            bidx = oi;
+        }
+    }
+    nan = __any_sync(0xffffffffu, nan);
+    return nan ? -2 : (bidx == INT_MAX ? -1 : (best == INFINITY ? -3 : bidx));
+}
+
+__device__ __forceinline__ bool row_ok(float m, ff s)
+{
+    return isfinite(m) && isfinite(s.hi) && s.hi > 0.f;
+}
+
+// p(x) = 2^((g - m) c) / s for one row given its (m, s): g - m exactly as a
+// float-float pair, its product with c to float-float, 2^hi with exp2f and
+// the low part to first order, then the division by s.
+__device__ __forceinline__ float softmax_at(float g, float m, ff s, float c)
+{
+    if (g == -INFINITY)
+        return 0.f;  // a masked entry
+    const ff d = two_sum(g, -m);
+    const float xh = __fmul_rn(d.hi, c);
+    const float xl = fmaf(d.lo, c, fmaf(d.hi, c, -xh));
+    const float num = __fmul_rn(exp2f(xh), fmaf(xl, 0.69314718f, 1.f));
+    const float inv = __frcp_rn(s.hi);
+    return __fmul_rn(__fmul_rn(num, inv), fmaf(-s.lo, inv, 1.f));
+}
+
+// Request i's offsets checked locally, before the streaming kernel's own
+// validation is visible: only then are its token / logit addresses formed.
+__device__ __forceinline__ bool request_shape_ok(const FinishParams &p, int i, int cu_i, int K)
+{
+    const int64_t t0 = (int64_t)cu_i + i;
+    return cu_i >= 0 && K >= 0 && K <= kMaxDraft && t0 + K < p.g.max_rows &&
+           (p.draft_stride > 0 ? K <= p.draft_stride : (int64_t)cu_i + K <= p.draft_rows);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const FinishParams p)
+{
+    __shared__ int row_g[kMaxDraft + 1];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int i = blockIdx.x;
+
+    // inputs that do not depend on kernel 1 are read before waiting for it
+    const int cu_i = __ldg(p.cu + i);
+    const int K = __ldg(p.cu + i + 1) - cu_i;
+    const bool shape = request_shape_ok(p, i, cu_i, K);
+    const bool act = shape && warp == 0 && lane < K;
+    const int x = act ? __ldg(p.tokens + draft_index(p.draft_stride, p.cu, i, lane)) : -1;
+
+    pdl_wait();  // kernel 1 has completed and its writes are visible
+    if (__ldcg(p.cu_flag) == 0u || !shape)
+        return;  // malformed offsets: kernel 1 poisoned every output
+    const int64_t t0 = (int64_t)cu_i + i;
+    for (int rho = warp; rho <= K; rho += kFinishWarps) {
+        const int gj = merge_argmax_row(p.part, p.g, t0 + rho);
+        if (lane == 0)
+            row_g[rho] = gj;
+    }
+    __syncthreads();
+    if (warp != 0)
+        return;
+    const bool bad_tok = act && (x < 0 || x >= p.V);
+    bool bad_nf = false;
+    for (int jj = lane; jj <= K; jj += 32)
+        bad_nf |= row_g[jj] < 0;
+    const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
+    const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
+    const unsigned rej = __ballot_sync(0xffffffffu, act && x != row_g[act ? lane : 0]);
+    const bool timeout = read_status(p.status) & ST_TIMEOUT;
+    if (nf || bt || timeout) {
+        if (lane == 0)
+            set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+        for (int jj = lane; jj <= K; jj += 32)
+            p.out_tokens[t0 + jj] = -1;
+        if (lane == 0)
+            p.out_len[i] = -1;
+        return;
+    }
+    const int a = rej ? __ffs(rej) - 1 : K;
+    for (int jj = lane; jj <= K; jj += 32)
+        p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
+    if (lane == 0)
+        p.out_len[i] = a;
+}
+
+// f / s for a float-float s.
+__device__ __forceinline__ float ff_recip_scaled(float f, ff s)
+{
+    const float inv = __frcp_rn(s.hi);
+    return __fmul_rn(__fmul_rn(f, inv), fmaf(-s.lo, inv, 1.f));
+}
+
+struct DrawCtx {
+    bool resid;
+    float c, mct, mcd;  // c and fl(m c) of the two rows
+    float sc_t, sc_d;   // 2^(fl(m c) - m c) / s: normalisers including the rounding fix
+};
+
+// Final-draw weight of one element: max(0, p - q) after a rejection, the
+// unnormalised p for the bonus draw (or an all-zero residual).
+__device__ __forceinline__ float draw_w(const DrawCtx &d, float t, float x)
+{
+    const float pt = ex2_approx(fmaf(t, d.c, -d.mct));
+    if (!d.resid)
+        return pt;
+    const float pd = ex2_approx(fmaf(x, d.c, -d.mcd));
+    return fmaxf(fmaf(pt, d.sc_t, -__fmul_rn(pd, d.sc_d)), 0.f);
+}
+
+// Sum of the final-draw weights of one thread's contiguous piece (16-byte
+// vectors [v0, v1) of a staged slice of len elements), in index order, fp32.
+template <typename T>
+__device__ __forceinline__ float piece_sum(const DrawCtx d, const T *tb, const T *db, int len,
+                                           int v0, int v1)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(db);
+    float acc = 0.f;
+#pragma unroll 1
+    for (int v = v0; v < v1; ++v) {
+        float ft[E], fd[E];
+        Elem<T>::unpack(tv[v], ft);
+        if (d.resid)
+            Elem<T>::unpack(dv[v], fd);
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+            const float w = v * E + h < len ? draw_w(d, ft[h], d.resid ? fd[h] : 0.f) : 0.f;
+            acc = __fadd_rn(acc, w);
+        }
+    }
+    return acc;
+}
+
+// The same walk, stopping at the first element whose running sum exceeds
+// rem: its index in the slice, or (none) the last element with weight > 0
+// (-1 if there is none).  The running sums are those of piece_sum, bit for
+// bit.
+template <typename T>
+__device__ __forceinline__ int piece_find(const DrawCtx d, const T *tb, const T *db, int len,
+                                          int v0, int v1, float rem)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
+    const uint4 *dv = reinterpret_cast<const uint4 *>(db);
+    float acc = 0.f;
+    int lastp = -1;
+#pragma unroll 1
+    for (int v = v0; v < v1; ++v) {
+        float ft[E], fd[E];
+        Elem<T>::unpack(tv[v], ft);
+        if (d.resid)
+            Elem<T>::unpack(dv[v], fd);
+#pragma unroll
+        for (int h = 0; h < E; ++h) {
+            const int k = v * E + h;
+            const float w = k < len ? draw_w(d, ft[h], d.resid ? fd[h] : 0.f) : 0.f;
+            acc = __fadd_rn(acc, w);
+            if (w > 0.f)
+                lastp = k;
+            if (acc > rem)
+                return k;
+        }
+    }
+    return lastp;
+}
+
+// Stage elements [c0, c0 + len) of the draw rows into shared memory (one
+// TMA bulk copy per row, or plain loads when the rows are not 16-byte
+// aligned), then every thread sums its contiguous piece (kept in piece[]
+// for the search) and the pieces are added as float-float pairs in a fixed
+// order.  Once any copy of this call has timed out nothing more is copied.
+template <typename T>
+__device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, const T *trow,
+                                       const T *drow, int c0, int len, T *tb, T *db,
+                                       uint64_t *bar, uint32_t *phase, float *piece, ff *wred,
+                                       int *expired)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    // earlier readers of the buffers, piece and wred are done
+    const bool stop = __syncthreads_or(tid == 0 && (read_status(p.status) & ST_TIMEOUT));
+    if (!stop && len > 0) {
+        if (p.tma) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
+                mbar_arrive_expect_tx(bar, d.resid ? 2 * bytes : bytes);
+                bulk_g2s(tb, trow + c0, bytes, bar);
+                if (d.resid)
+                    bulk_g2s(db, drow + c0, bytes, bar);
+            }
+            if (!mbar_wait_bounded(bar, *phase)) {
+                set_status(p.status, ST_TIMEOUT);
+                *expired = 1;
+                mbar_wait_bounded(bar, *phase);  // the copy in flight, once more
+            }
+            *phase ^= 1u;
+        } else {
+            for (int k = tid; k < len; k += kSampleThreads) {
+                tb[k] = trow[c0 + k];
+                if (d.resid)
+                    db[k] = drow[c0 + k];
+            }
+            __syncthreads();
+        }
+    }
+    const int nv = (len + E - 1) / E;
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    const float ps = piece_sum<T>(d, tb, db, len, v0, v1);
+    piece[tid] = ps;
+    const ff ws = warp_sum_ff({ps, 0.f});
+    __syncthreads();  // piece[] complete; wred free
+    if (lane == 0)
+        wred[warp] = ws;
+    __syncthreads();
+    ff tot = wred[0];
+    for (int q = 1; q < kSampleWarps; ++q)
+        tot = ff_add(tot, wred[q]);
+    return tot;
+}
+
+// Store (m, s, p(x)) of row k into the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_row(float *row_m, ff *row_s, float *row_p, int k,
+                                               uint32_t rank, float m, ff s, float px)
+{
+    uint32_t rm, rs, rp;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rm) : "r"(smem_u32(row_m + k)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rs) : "r"(smem_u32(row_s + k)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rp) : "r"(smem_u32(row_p + k)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rm), "f"(m) : "memory");
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(rs), "f"(s.hi), "f"(s.lo)
+                 : "memory");
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rp), "f"(px) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const FinishParams p)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    T *tb = reinterpret_cast<T *>(dsm);  // staged slice of the target row
+    T *db = reinterpret_cast<T *>(dsm + p.stage_smem);  // and of the draft row
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float row_m[2 * kMaxDraft + 1];            // written by every CTA of the cluster
+    __shared__ __align__(8) ff row_s[2 * kMaxDraft + 1];  // likewise
+    __shared__ float row_p[2 * kMaxDraft + 1];            // likewise: p_j(x_j), q_j(x_j)
+    __shared__ float piece[kSampleThreads];
+    __shared__ ff wred[kSampleWarps];
+    __shared__ ff slice_tot[kMaxSlices];
+    __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
+    __shared__ ff s_excl[kSampleWarps];
+    __shared__ int s_a, s_bad, s_hit, s_last, s_cs, s_past, s_redo, s_expired;
+    __shared__ ff s_base, s_target;
+    __shared__ DrawCtx s_d;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int ncl = p.ncl;
+    const int i = blockIdx.x / ncl;
+    const T *tbase = reinterpret_cast<const T *>(p.target);
+    const T *dbase = reinterpret_cast<const T *>(p.draft);
+
+    // ---- inputs that do not depend on kernel 1, read before waiting for it
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        s_expired = 0;
+    }
+    const int cu_i = __ldg(p.cu + i);
+    const int K = __ldg(p.cu + i + 1) - cu_i;
+    const bool shape = request_shape_ok(p, i, cu_i, K);
+    const int64_t t0 = (int64_t)cu_i + i;
+    const int nrows = 2 * K + 1;
+    // warp 0, lane j < K: the drafted token and its uniform (accept test)
+    const bool act = shape && warp == 0 && lane < K;
+    int x = -1;
+    float u = 0.f;
+    int64_t di = 0;
+    if (act) {
+        di = draft_index(p.draft_stride, p.cu, i, lane);
+        x = __ldg(p.tokens + di);
+        u = __ldg(p.u_accept + di);
+    }
+    // the rows this warp merges (k = rank + ncl * (warp + kSampleWarps * t)):
+    // target rows 0..K, then draft rows 0..K-1; the logit at the drafted
+    // token of each such row
+    int my_k[2];
+    float g[2] = {-INFINITY, -INFINITY};
+    bool g_ok[2] = {false, false};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        my_k[t] = (int)rank + ncl * (warp + kSampleWarps * t);
+        if (!shape || my_k[t] >= nrows)
+            my_k[t] = -1;
+        else if (my_k[t] != K) {
+            const int j = my_k[t] < K ? my_k[t] : my_k[t] - K - 1;
+            const int64_t dj = draft_index(p.draft_stride, p.cu, i, j);
+            const int xj = __ldg(p.tokens + dj);
+            if (xj >= 0 && xj < p.V) {
+                g_ok[t] = true;
+                g[t] = my_k[t] < K ? Elem<T>::ld_global(tbase + (t0 + j) * p.V, xj)
+                                   : Elem<T>::ld_global(dbase + dj * p.V, xj);
+            }
+        }
+    }
+    const float uf = __ldg(p.u_final + i);
+
+    pdl_wait();  // kernel 1 has completed and its writes are visible
+    if (__ldcg(p.cu_flag) == 0u || !shape)
+        return;  // malformed offsets: kernel 1 poisoned every output (same in every CTA)
+    cluster_arrive_relaxed();  // (0) this CTA has started
+    // an expired wait of kernel 1 only poisons; its flag is read now, off the
+    // critical path
+    const bool timeout = warp == 0 && (read_status(p.status) & ST_TIMEOUT);
+
+    // ---- (m, s) and p(x) of the request's rows, one or two rows per warp of
+    // the cluster, sent to every CTA
+    float mm[2] = {-INFINITY, -INFINITY}, px[2] = {0.f, 0.f};
+    ff sm[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (my_k[t] < 0)
+            continue;
+        const int k = my_k[t];
+        const int64_t rg = k <= K ? t0 + k : p.g.max_rows + cu_i + (k - K - 1);
+        int wf, wl;
+        row_span(p.g, rg, wf, wl);
+        for (int w = wf + lane; w <= wl; w += 32) {
+            const Partial pt = load_partial(p.part + rg + w);
+            lse_combine(mm[t], sm[t], pt.m, {pt.s_hi, pt.s_lo}, p.c);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float mo = __shfl_xor_sync(0xffffffffu, mm[t], o);
+            const ff so = ff_shfl_xor(sm[t], o);
+            lse_combine(mm[t], sm[t], mo, so, p.c);
+        }
+        px[t] = g_ok[t] && row_ok(mm[t], sm[t]) ? softmax_at(g[t], mm[t], sm[t], p.c) : 0.f;
+    }
+    cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+        if (my_k[t] >= 0 && lane < ncl)
+            st_cluster_row(row_m, row_s, row_p, my_k[t], (uint32_t)lane, mm[t], sm[t], px[t]);
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
+
+    // ---- accept test and first rejection (warp 0; identical in every CTA)
+    if (warp == 0) {
+        bool bad_tok = act && (x < 0 || x >= p.V), bad_nf = false, acc = true;
+        float pp = 0.f, qq = 0.f;
+        if (act && !bad_tok) {
+            if (!row_ok(row_m[lane], row_s[lane]) ||
+                !row_ok(row_m[K + 1 + lane], row_s[K + 1 + lane])) {
+                bad_nf = true;
+            } else {
+                pp = row_p[lane];
+                qq = row_p[K + 1 + lane];
+                const float ratio = qq > 0.f ? __fdiv_rn(pp, qq) : (pp > 0.f ? INFINITY : 0.f);
+                acc = u < ratio;
+            }
+        }
+        if (lane == 0 && !row_ok(row_m[K], row_s[K]))
+            bad_nf = true;
+        const unsigned nf = __ballot_sync(0xffffffffu, bad_nf);
+        const unsigned bt = __ballot_sync(0xffffffffu, bad_tok);
+        const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
+        // bad depends only on the request's data, so every CTA of the cluster
+        // takes the same branch; an expired wait only poisons (best effort)
+        const bool bad = nf || bt;
+        const int a = rej ? __ffs(rej) - 1 : K;
+        if (rank == 0) {  // the request's outputs, written once
+            if (bad || timeout) {
+                if (lane == 0)
+                    set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
+                for (int jj = lane; jj <= K; jj += 32)
+                    p.out_tokens[t0 + jj] = -1;
+                if (lane == 0)
+                    p.out_len[i] = -1;
+            } else {
+                if (act && p.out_p)
+                    p.out_p[di] = pp;
+                if (act && p.out_q)
+                    p.out_q[di] = qq;
+                for (int jj = lane; jj <= K; jj += 32) {
+                    if (jj < a)
+                        p.out_tokens[t0 + jj] = x;  // jj == lane since a <= 32
+                    else if (jj > a)
+                        p.out_tokens[t0 + jj] = -1;
+                }
+                if (lane == 0)
+                    p.out_len[i] = a;
+            }
+        }
+        if (lane == 0) {
+            s_a = a;
+            s_bad = bad;
+            // the final draw's constants, once for the CTA
+            DrawCtx d0;
+            d0.resid = a < K;
+            d0.c = p.c;
+            const float mt = row_m[a];
+            d0.mct = mt * p.c;
+            d0.sc_t = ff_recip_scaled(mc_correction(mt, d0.mct, p.c), row_s[a]);
+            d0.mcd = 0.f;
+            d0.sc_d = 0.f;
+            if (d0.resid) {
+                const float md = row_m[K + 1 + a];
+                d0.mcd = md * p.c;
+                d0.sc_d = ff_recip_scaled(mc_correction(md, d0.mcd, p.c), row_s[K + 1 + a]);
+            }
+            s_d = d0;
+        }
+    }
+    __syncthreads();
+    if (s_bad)
+        return;  // same decision in every CTA of the cluster; no more cluster traffic
+
+    // ---- final draw: this CTA weighs its range of the vocabulary
+    const int a = s_a;
+    const int64_t trow_i = t0 + a;
+    const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
+    DrawCtx d = s_d;
+    const T *trow = tbase + trow_i * p.V;
+    const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
+    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
+    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+    int weighed = -1;  // slice staged in shared memory
+    uint32_t phase = 0;
+
+    // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
+    // second pass over p_a (the same decision in every CTA)
+    int slot = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        ff mine{0.f, 0.f};
+        for (int sl = 0; sl < nsl; ++sl) {
+            const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+            const ff ss = weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
+                                         wred, &s_expired);
+            weighed = sl;
+            if (tid == 0)
+                slice_tot[sl] = ss;
+            mine = ff_add(mine, ss);
+        }
+        if (tid < ncl)
+            st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
+        cluster_arrive_release();
+        cluster_wait_acquire();  // (2 + pass) every CTA holds every range sum
+        slot = pass;
+        // S and the range holding u*S, by warp 0 (lane r holds range r): an
+        // inclusive float-float scan in range order, the same in every CTA.
+        // `past` marks u*S at or beyond the end after rounding: then the
+        // last weight > 0 wins.
+        if (warp == 0) {
+            const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
+            ff incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff n = ff_shfl_up(incl, o);
+                if (lane >= o)
+                    incl = ff_add(n, incl);
+            }
+            const ff S = {__shfl_sync(0xffffffffu, incl.hi, 31),
+                          __shfl_sync(0xffffffffu, incl.lo, 31)};
+            const ff target = ff_mul(S, uf);
+            const unsigned over = __ballot_sync(0xffffffffu, lane < ncl && ff_gt(incl, target));
+            const unsigned mass = __ballot_sync(0xffffffffu, lane < ncl && v.hi > 0.f);
+            const int cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
+            ff excl = ff_shfl_up(incl, 1);
+            if (lane == 0)
+                excl = {0.f, 0.f};
+            const int src = cs < 0 ? 0 : cs;
+            const ff base = {__shfl_sync(0xffffffffu, excl.hi, src),
+                             __shfl_sync(0xffffffffu, excl.lo, src)};
+            if (lane == 0) {
+                s_cs = cs;
+                s_past = over == 0u;
+                s_base = base;
+                s_target = target;
+                s_redo = !(S.hi > 0.f);
+            }
+        }
+        __syncthreads();
+        if (!(d.resid && s_redo))
+            break;
+        d.resid = false;  // all-zero residual: draw from p_a instead
+    }
+    // no shared memory of another CTA is touched after this point
+    const int cs = s_cs;
+    bool past = s_past != 0;
+    ff base = s_base;
+    const ff target = s_target;
+    if ((int)rank != cs) {
+        if (cs < 0 && rank == 0 && tid == 0) {  // no mass at all (never with finite rows)
+            set_status(p.status, ST_NONFINITE);
+            p.out_tokens[trow_i] = -1;
+        }
+        return;
+    }
+
+    // ---- owner CTA: the slice, then the thread piece, then the element
+    int sl = -1;
+    {
+        ff b2 = base;
+        for (int s2 = 0; s2 < nsl && !past; ++s2) {
+            const ff next = ff_add(b2, slice_tot[s2]);
+            if (ff_gt(next, target)) {
+                sl = s2;
+                break;
+            }
+            b2 = next;
+        }
+        if (sl >= 0) {
+            base = b2;
+        } else {  // the last slice with mass
+            past = true;
+            ff bl = base;
+            b2 = base;
+            sl = nsl - 1;
+            for (int s2 = 0; s2 < nsl; ++s2) {
+                if (slice_tot[s2].hi > 0.f) {
+                    sl = s2;
+                    bl = b2;
+                }
+                b2 = ff_add(b2, slice_tot[s2]);
+            }
+            base = bl;
+        }
+    }
+    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+    if (sl != weighed)
+        weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
+    // scan of the piece sums (float-float, fixed order).  A piece's lower end
+    // is the previous piece's upper end bit for bit, so the pieces tile the
+    // slice with no gap and no overlap.
+    ff incl{piece[tid], 0.f};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(incl, o);
+        if (lane >= o)
+            incl = ff_add(n, incl);
+    }
+    ff excl = ff_shfl_up(incl, 1);
+    if (lane == 0)
+        excl = {0.f, 0.f};
+    if (tid == 0) {
+        s_hit = INT_MAX;
+        s_last = -1;
+    }
+    if (lane == 31)
+        s_excl[warp] = incl;
+    __syncthreads();
+    ff wbase = base;
+    for (int q = 0; q < warp; ++q)
+        wbase = ff_add(wbase, s_excl[q]);
+    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
+    if (!past && ff_le(lo, target) && ff_gt(hi, target))
+        atomicMin(&s_hit, tid);
+    __syncthreads();
+    // the piece walk repeats the piece sum's additions, so it meets the same
+    // running sums; rem may round up to the piece total: then the piece's
+    // last element with weight > 0
+    constexpr int E = Elem<T>::kPerVec;
+    const int nv = (len + E - 1) / E;
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    if (s_hit == tid) {
+        const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+        s_last = piece_find<T>(d, tb, db, len, v0, v1, rem);
+    } else if (s_hit == INT_MAX) {  // past the end after rounding: the last element with mass
+        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
+        if (lp >= 0)
+            atomicMax(&s_last, lp);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int res = s_last;
+        int y = res >= 0 ? c0 + res : -1;
+        if (y < 0)
+            set_status(p.status, ST_NONFINITE);
+        if (timeout || s_expired) {  // a copy gave up: the data may be stale
+            y = -1;
+            p.out_len[i] = -1;
+            for (int jj = 0; jj <= K; ++jj)
+                p.out_tokens[t0 + jj] = -1;
+        }
+        p.out_tokens[trow_i] = y;
+    }
+}
+
+}  // namespace sv

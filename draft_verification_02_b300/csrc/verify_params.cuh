@@ -1,0 +1,126 @@
+// verify_params.cuh - what the two verification kernels share: their
+// parameter blocks and small device helpers (PDL control, 2^x, bf16
+// unpacking, the draft index, the rounding fix of fl(m c)).
+#pragma once
+
+#include <algorithm>
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// parameters
+// ---------------------------------------------------------------------------
+
+struct Geometry {  // the unit split of kernel 1, needed by kernel 2 to find partials
+    int64_t max_rows;  // target rows (host bound)
+    int64_t U;         // units
+    int cpr;           // units per row
+    int Q;             // elements per unit (the last unit of a row may be shorter)
+    int P;             // warp workers
+};
+
+struct StreamParams {
+    const void *target;
+    const void *draft;
+    const int32_t *cu;
+    int32_t *out_tokens;
+    int32_t *out_len;
+    int B, V;
+    int64_t draft_slots;  // draft rows read (packed index space); 0 at T = 0
+    int draft_stride;
+    Geometry g;
+    int tma;
+    int piece_smem;  // bytes per ring slot (multiple of 128)
+    float c;         // log2(e) / T
+    uint32_t *status;
+    uint32_t *cu_flag;
+    Partial *part;
+};
+
+struct FinishParams {
+    const void *target;
+    const void *draft;
+    const int32_t *tokens;
+    const int32_t *cu;
+    const float *u_accept;
+    const float *u_final;
+    int32_t *out_tokens;
+    int32_t *out_len;
+    float *out_p;
+    float *out_q;
+    int B, V;
+    int64_t draft_rows;  // rows the draft side may index
+    int draft_stride;
+    Geometry g;
+    int ncl;    // CTAs per request (cluster size) in the final draw: 8 or 16
+    int R;      // vocabulary entries per cluster CTA in the final draw
+    int slice;  // entries of one row weighed at a time (multiple of 16 bytes)
+    int pv;          // 16-byte vectors per thread piece of a slice (odd)
+    int stage_smem;  // bytes per staged row slice (multiple of 128)
+    int tma;         // rows 16-byte aligned: TMA bulk copies
+    float c;
+    uint32_t *status;
+    const uint32_t *cu_flag;
+    const Partial *part;
+};
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// 2^x on the SFU (PTX ex2.approx.ftz.f32); results below 2^-126 flush to 0.
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Owner warp of unit u when warp w owns units [w*U/P, (w+1)*U/P).
+__device__ __forceinline__ int owner_of(int64_t u, const Geometry &g)
+{
+    return (int)(((u + 1) * (int64_t)g.P - 1) / g.U);
+}
+
+// The unit sums use exp2(x*c - fl(m*c)) = exp2((x - m)*c) * 2^-(fl(m*c) - m*c);
+// this returns the factor 2^(fl(m*c) - m*c) that undoes the rounding.  The
+// rounding error fl(m*c) - m*c is exact as -fma(m, c, -fl(m*c)) and below
+// 2^-17 in magnitude, so 1 + delta*ln2 is the factor to fp32 precision.
+__device__ __forceinline__ float mc_correction(float m, float mc, float c)
+{
+    const float delta = -fmaf(m, c, -mc);
+    return fmaf(delta, 0.69314718f, 1.0f);
+}
+
+__device__ __forceinline__ int64_t draft_index(int draft_stride, const int32_t *cu, int i, int j)
+{
+    return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)__ldg(cu + i) + j;
+}
+
+}  // namespace sv
