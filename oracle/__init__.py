@@ -68,6 +68,8 @@ def load(path: str | None = None):
         lib.oracle_dcut_cost.argtypes = [_i32]
         lib.oracle_dcut_cost.restype = _f64
         lib.oracle_dcut_schedule_cost.argtypes = [_p, _p, _i32, _i32, _f64, _p, _p, _p]
+        lib.oracle_draft_confidence.argtypes = [_p, ctypes.c_int, _p, _p, _i32, _i32, _i64, _f64,
+                                                _p]
         if path is None:
             _lib = lib
         return lib
@@ -264,3 +266,17 @@ def dcut_schedule_cost(conf, kmax, max_cost: float, lib=None):
     st = (lib or load()).oracle_dcut_schedule_cost(_ptr(c), _ptr(km), B, Kmax, float(max_cost),
                                                    _ptr(depth), _ptr(cu), _ptr(benefit))
     return VerifyResult(status=st, depth=depth[:B], cu=cu, benefit=benefit[:B])
+
+
+def draft_confidence(draft, tokens, kmax, temperature: float, lib=None):
+    """q_{i,j}(x_{i,j}) for padded draft rows [B*Kmax, V]; 0 past kmax[i]."""
+    d, dt = _logits(draft)
+    tok = _np(tokens, np.int32)
+    km = _np(kmax, np.int32)
+    B = km.size
+    Kmax = tok.size // B if B else 0
+    V = d.shape[-1]
+    out = np.full(max(B * Kmax, 1), -7.0, np.float32)
+    st = (lib or load()).oracle_draft_confidence(_ptr(d), dt, _ptr(tok), _ptr(km), B, Kmax, V,
+                                                 float(temperature), _ptr(out))
+    return st, out[:B * Kmax].reshape(B, Kmax) if B else out[:0]

@@ -697,3 +697,59 @@ int oracle_dcut_schedule_cost(const float *conf, const int32_t *kmax, int32_t B,
     free(cand);
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* prefix confidence of drafted tokens                                       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * D-cut allocates depth from per-request prefix confidence ("Tencent Hunyuan
+ * Turns Speculative Decoding Into a Full Open-Source Stack", "What problem
+ * does it solve", inference layer).  Reading: the confidence of drafted
+ * token x_{i,j} is the drafter's own probability of it, q_{i,j}(x_{i,j}) =
+ * softmax(draft row (i, j) / T)(x_{i,j}); at T = 0 the drafter is greedy and
+ * the confidence is 1 when x_{i,j} is the row's lowest-index maximum, else 0.
+ * Rows are padded, row i*Kmax + j; entries j >= kmax[i] are 0.  A failing
+ * row (NaN / +inf / all masked, or a token outside [0, V)) gets NaN and the
+ * first error is returned.
+ */
+int oracle_draft_confidence(const void *draft, int dtype, const int32_t *tokens,
+                            const int32_t *kmax, int32_t B, int32_t Kmax, int64_t V, double T,
+                            float *out_conf)
+{
+    if (B < 0 || Kmax < 0 || Kmax > ORC_MAX_DRAFT || V <= 0 || !(T >= 0) || isinf(T) ||
+        (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_ERR_INVALID_ARG;
+    int first_err = ORC_OK;
+    for (int32_t i = 0; i < B; ++i) {
+        if (kmax[i] < 0 || kmax[i] > Kmax)
+            return ORC_ERR_INVALID_ARG;
+        for (int32_t j = 0; j < Kmax; ++j) {
+            int64_t r = (int64_t)i * Kmax + j;
+            if (j >= kmax[i]) {
+                out_conf[r] = 0.0f;
+                continue;
+            }
+            int32_t x = tokens[r];
+            int err = ORC_OK;
+            double c = 0.0;
+            if (x < 0 || x >= V) {
+                err = ORC_ERR_INVALID_ARG;
+            } else if (T == 0.0) {
+                int32_t g;
+                err = oracle_argmax_row(draft, dtype, r, V, &g);
+                c = (err == ORC_OK && g == x) ? 1.0 : 0.0;
+            } else {
+                err = softmax_at(draft, dtype, r, V, T, x, &c);
+            }
+            if (err != ORC_OK) {
+                out_conf[r] = NAN;
+                if (first_err == ORC_OK)
+                    first_err = err;
+                continue;
+            }
+            out_conf[r] = (float)c;
+        }
+    }
+    return first_err;
+}

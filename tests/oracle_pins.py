@@ -668,3 +668,52 @@ def pin_dcut_cost_errors(lib):
 
 ALL_PINS += [pin_dcut_cost_table, pin_dcut_cost_golden, pin_dcut_cost_invariants,
              pin_dcut_cost_errors]
+
+
+# ---------------------------------------------------------------------------
+# prefix confidence of drafted tokens
+# ---------------------------------------------------------------------------
+
+
+def pin_draft_confidence(lib):
+    """q(x) against scipy's softmax in fp64 (f32 and bf16 rows); T = 0 against
+    numpy's first-occurrence argmax; zeros past kmax; errors."""
+    rng = np.random.default_rng(21)
+    B, Kmax, V = 5, 4, 37
+    l = (rng.standard_normal((B * Kmax, V)) * 2).astype(np.float32)
+    tok = rng.integers(0, V, size=B * Kmax).astype(np.int32)
+    kmax = np.array([4, 0, 2, 3, 1], np.int32)
+    for T in (0.6, 1.0, 1.7):
+        for rows, exact in ((l, l), (_to_bf16_bits(l), None)):
+            if exact is None:
+                exact = (rows.astype(np.uint32) << 16).view(np.float32)
+            st, c = O.draft_confidence(rows, tok, kmax, T, lib=lib)
+            assert st == O.OK
+            for i in range(B):
+                for j in range(Kmax):
+                    r = i * Kmax + j
+                    want = _ref_softmax(exact[r], T)[tok[r]] if j < kmax[i] else 0.0
+                    assert abs(c[i, j] - want) <= 1e-6 * max(want, 1e-30), (T, i, j, c[i, j], want)
+    ties = rng.integers(-3, 3, size=(B * Kmax, V)).astype(np.float32)  # many ties
+    g = np.argmax(ties, axis=1)
+    tok2 = np.where(rng.random(B * Kmax) < 0.5, g, (g + 1) % V).astype(np.int32)
+    st, c = O.draft_confidence(ties, tok2, kmax, 0.0, lib=lib)
+    assert st == O.OK
+    for i in range(B):
+        for j in range(Kmax):
+            r = i * Kmax + j
+            want = (1.0 if tok2[r] == g[r] else 0.0) if j < kmax[i] else 0.0
+            assert c[i, j] == want, (i, j)
+    bad = l.copy()
+    bad[2 * Kmax + 1, 5] = np.nan  # request 2, position 1 (inside kmax = 2)
+    st, c = O.draft_confidence(bad, tok, kmax, 1.0, lib=lib)
+    assert st == O.ERR_NONFINITE and np.isnan(c[2, 1]) and not np.isnan(c[2, 0])
+    tok3 = tok.copy()
+    tok3[0] = V
+    st, c = O.draft_confidence(l, tok3, kmax, 1.0, lib=lib)
+    assert st == O.ERR_INVALID_ARG and np.isnan(c[0, 0])
+    assert O.draft_confidence(l, tok, np.array([4, 0, 2, 3, 5], np.int32), 1.0,
+                              lib=lib)[0] == O.ERR_INVALID_ARG
+
+
+ALL_PINS += [pin_draft_confidence]

@@ -53,6 +53,10 @@ MUTANTS = [
      "if (total + c <= max_cost) {", "if (total + c > max_cost) break; {"),
     ("cost variant benefit forgets the depth factor",
      "double b = P * (double)d / oracle_dcut_cost(d);", "double b = P / oracle_dcut_cost(d);"),
+    ("confidence reads the wrong row", "err = softmax_at(draft, dtype, r, V, T, x, &c);",
+     "err = softmax_at(draft, dtype, r > 0 ? r - 1 : r, V, T, x, &c);"),
+    ("greedy confidence ignores the argmax", "c = (err == ORC_OK && g == x) ? 1.0 : 0.0;",
+     "c = 1.0;"),
     ("cost variant keeps the last maximising depth", "if (b > best) { /* strict",
      "if (b >= best) { /* strict"),
     ("cost variant sorts ascending",
