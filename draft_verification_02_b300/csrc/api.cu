@@ -235,6 +235,36 @@ int dcut_allocate_cost(const float *conf, const int32_t *kmax, int32_t B, int32_
     return cuda_status(sv::launch_dcut_cost(a, (cudaStream_t)stream, tr));
 }
 
+int spec_draft_confidence(const void *draft_logits, int dtype, const int32_t *draft_tokens,
+                          const int32_t *kmax, int32_t B, int32_t Kmax, int32_t V,
+                          float temperature, float *out_conf, void *workspace, size_t ws_bytes,
+                          spec_stream_t stream)
+{
+    if (!valid_dtype(dtype) || B < 0 || B > SPEC_MAX_BATCH || Kmax < 0 ||
+        Kmax > SPEC_MAX_DRAFT || V < 1 || V > sv::kMaxVocab || !(temperature >= 0.f) ||
+        std::isinf(temperature))
+        return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)B * Kmax == 0)
+        return SPEC_OK;
+    if (!draft_logits || !draft_tokens || !kmax || !out_conf)
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(B, (int64_t)B * (Kmax + 1), V))
+        return SPEC_ERR_WORKSPACE;
+    sv::ConfArgs a{};
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.tokens = draft_tokens;
+    a.kmax = kmax;
+    a.B = B;
+    a.Kmax = Kmax;
+    a.V = V;
+    a.temperature = (double)temperature;
+    a.out_conf = out_conf;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_confidence(a, (cudaStream_t)stream, tr));
+}
+
 int spec_get_device_status(void *workspace, spec_stream_t stream)
 {
     if (!workspace)

@@ -327,7 +327,10 @@ __device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, c
     const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
     const float ps = piece_sum<T>(d, tb, db, len, v0, v1);
     piece[tid] = ps;
-    const ff ws = warp_sum_ff({ps, 0.f});
+    ff ws{ps, 0.f};
+#pragma unroll 1
+    for (int o = 16; o > 0; o >>= 1)  // warp sum, the same bits in every lane
+        ws = ff_add(ws, ff_shfl_xor(ws, o));
     __syncthreads();  // piece[] complete; wred free
     if (lane == 0)
         wred[warp] = ws;
@@ -399,15 +402,18 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         x = __ldg(p.tokens + di);
         u = __ldg(p.u_accept + di);
     }
-    // the rows this warp merges (k = rank + ncl * (warp + kSampleWarps * t)):
-    // target rows 0..K, then draft rows 0..K-1; the logit at the drafted
-    // token of each such row
+    // the rows this warp merges: with at most one row per warp of a CTA,
+    // every CTA merges all of them (row k = warp), else the rows are spread
+    // over the cluster (k = rank + ncl * (warp + kSampleWarps * t)) and sent
+    // to every CTA.  Target rows 0..K, then draft rows 0..K-1; the logit at
+    // the drafted token of each such row.
+    const bool local = nrows <= kSampleWarps;
     int my_k[2];
     float g[2] = {-INFINITY, -INFINITY};
     bool g_ok[2] = {false, false};
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-        my_k[t] = (int)rank + ncl * (warp + kSampleWarps * t);
+        my_k[t] = local ? (t == 0 ? warp : nrows) : (int)rank + ncl * (warp + kSampleWarps * t);
         if (!shape || my_k[t] >= nrows)
             my_k[t] = -1;
         else if (my_k[t] != K) {
@@ -447,7 +453,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
             const Partial pt = load_partial(p.part + rg + w);
             lse_combine(mm[t], sm[t], pt.m, {pt.s_hi, pt.s_lo}, p.c);
         }
-#pragma unroll
+#pragma unroll 1
         for (int o = 16; o > 0; o >>= 1) {
             const float mo = __shfl_xor_sync(0xffffffffu, mm[t], o);
             const ff so = ff_shfl_xor(sm[t], o);
@@ -455,13 +461,23 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         }
         px[t] = g_ok[t] && row_ok(mm[t], sm[t]) ? softmax_at(g[t], mm[t], sm[t], p.c) : 0.f;
     }
-    cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
+    if (local) {  // every CTA merged every row itself
+        if (my_k[0] >= 0 && lane == 0) {
+            row_m[my_k[0]] = mm[0];
+            row_s[my_k[0]] = sm[0];
+            row_p[my_k[0]] = px[0];
+        }
+        __syncthreads();
+        cluster_wait_acquire();  // (0) complete (long since)
+    } else {
+        cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
 #pragma unroll
-    for (int t = 0; t < 2; ++t)
-        if (my_k[t] >= 0 && lane < ncl)
-            st_cluster_row(row_m, row_s, row_p, my_k[t], (uint32_t)lane, mm[t], sm[t], px[t]);
-    cluster_arrive_release();
-    cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
+        for (int t = 0; t < 2; ++t)
+            if (my_k[t] >= 0 && lane < ncl)
+                st_cluster_row(row_m, row_s, row_p, my_k[t], (uint32_t)lane, mm[t], sm[t], px[t]);
+        cluster_arrive_release();
+        cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
+    }
 
     // ---- accept test and first rejection (warp 0; identical in every CTA)
     if (warp == 0) {
@@ -572,7 +588,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         if (warp == 0) {
             const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
             ff incl = v;
-#pragma unroll
+#pragma unroll 1
             for (int o = 1; o < 32; o <<= 1) {
                 const ff n = ff_shfl_up(incl, o);
                 if (lane >= o)
@@ -652,7 +668,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     // is the previous piece's upper end bit for bit, so the pieces tile the
     // slice with no gap and no overlap.
     ff incl{piece[tid], 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
         const ff n = ff_shfl_up(incl, o);
         if (lane >= o)
@@ -702,6 +718,91 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
                 p.out_tokens[t0 + jj] = -1;
         }
         p.out_tokens[trow_i] = y;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// prefix confidence of drafted tokens
+// ---------------------------------------------------------------------------
+
+struct ConfParams {
+    const void *draft;  // [B*Kmax][V], row i*Kmax + j
+    const int32_t *tokens;
+    const int32_t *kmax;
+    int B, Kmax, V;
+    Geometry g;  // the streaming pass over the B*Kmax rows
+    float c;     // log2(e) / T (T > 0)
+    float *out_conf;
+    uint32_t *status;
+    const Partial *part;
+};
+
+// One warp per draft row: conf = q(x) = 2^((g - m) c) / s from the row's
+// merged partials (T > 0), or 1 when x is the row's lowest-index maximum
+// (T = 0); 0 past kmax[i].  Launched as a programmatic dependent of the
+// streaming pass; the token and the logit at it are read before waiting.
+template <typename T, bool GREEDY>
+__global__ void __launch_bounds__(kFinishThreads) confidence_kernel(const ConfParams p)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t r = (int64_t)blockIdx.x * kFinishWarps + warp;
+    const int64_t nrow = (int64_t)p.B * p.Kmax;
+    bool live = false, bad_k = false, bad_x = false;
+    int x = -1;
+    float gx = 0.f;
+    if (r < nrow) {
+        const int i = (int)(r / p.Kmax), j = (int)(r - (int64_t)i * p.Kmax);
+        const int km = __ldg(p.kmax + i);
+        bad_k = km < 0 || km > p.Kmax;
+        live = !bad_k && j < km;
+        if (live) {
+            x = __ldg(p.tokens + r);
+            bad_x = x < 0 || x >= p.V;
+            if (!bad_x && !GREEDY)
+                gx = Elem<T>::ld_global(reinterpret_cast<const T *>(p.draft) + r * p.V, x);
+        }
+    }
+    pdl_wait();  // the streaming pass has completed and its writes are visible
+    if (r >= nrow)
+        return;
+    float conf = 0.f;
+    uint32_t err = 0;
+    if (bad_k || bad_x) {
+        err = ST_INVALID;
+    } else if (live) {
+        if constexpr (GREEDY) {
+            const int gi = merge_argmax_row(p.part, p.g, r);
+            if (gi < 0)
+                err = ST_NONFINITE;
+            else
+                conf = gi == x ? 1.f : 0.f;
+        } else {
+            int wf, wl;
+            row_span(p.g, r, wf, wl);
+            float m = -INFINITY;
+            ff s{0.f, 0.f};
+            for (int w = wf + lane; w <= wl; w += 32) {
+                const Partial q = load_partial(p.part + r + w);
+                lse_combine(m, s, q.m, {q.s_hi, q.s_lo}, p.c);
+            }
+#pragma unroll 1
+            for (int o = 16; o > 0; o >>= 1) {
+                const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+                const ff so = ff_shfl_xor(s, o);
+                lse_combine(m, s, mo, so, p.c);
+            }
+            if (row_ok(m, s))
+                conf = softmax_at(gx, m, s, p.c);
+            else
+                err = ST_NONFINITE;
+        }
+    }
+    if (lane == 0) {
+        if (err) {
+            set_status(p.status, err);
+            conf = __int_as_float(0x7fc00000);
+        }
+        p.out_conf[r] = conf;
     }
 }
 

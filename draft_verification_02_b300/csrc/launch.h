@@ -68,4 +68,21 @@ struct DcutCostArgs {
 
 cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t stream, Tracer &tr);
 
+struct ConfArgs {
+    const void *draft;  // [B*Kmax][V]
+    int dtype;
+    const int32_t *tokens;
+    const int32_t *kmax;
+    int B;
+    int Kmax;
+    int V;
+    double temperature;  // 0 = greedy
+    float *out_conf;
+    void *ws;
+};
+
+// Enqueue the streaming pass over the B*Kmax draft rows and the per-row
+// confidence kernel (2 launches).
+cudaError_t launch_confidence(const ConfArgs &a, cudaStream_t stream, Tracer &tr);
+
 }  // namespace sv

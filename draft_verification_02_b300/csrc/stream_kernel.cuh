@@ -414,8 +414,9 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
             advance(i_rg, i_q);
         }
     // CTA 0 validates the offsets for both kernels (and every CTA does when
-    // it maps padded rows through them).
-    if (padded || blockIdx.x == 0) {
+    // it maps padded rows through them).  Without offsets (p.cu == nullptr)
+    // every row is real.
+    if (p.cu != nullptr && (padded || blockIdx.x == 0)) {
         int bad = 0;
         for (int k = threadIdx.x; k <= B; k += kStreamThreads) {
             const int v = __ldg(p.cu + k);
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
             return;
         }
     }
-    {
+    if (p.cu != nullptr) {
         int v = lane == 0 ? __ldg(p.cu + B) : 0;
         v = __shfl_sync(0xffffffffu, v, 0);
         nd = min(nd, (int64_t)v);

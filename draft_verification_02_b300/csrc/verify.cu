@@ -246,6 +246,82 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     return cudaSuccess;
 }
 
+template <typename T, bool GREEDY>
+static cudaError_t launch_conf_typed(const ConfArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const int e = (int)sizeof(T);
+    const int64_t rows = (int64_t)a.B * a.Kmax;
+    const WsLayout L = ws_layout(a.B, (int64_t)a.B * (a.Kmax + 1), a.V);
+    unsigned char *ws = static_cast<unsigned char *>(a.ws);
+    const int ctas_max = sm_count() * SV_STREAM_CTAS_PER_SM;
+    const Geometry g = plan(rows, rows, a.V, e, std::min(kMaxWorkers, ctas_max * kStreamWarps));
+    const bool tma = ((int64_t)a.V * e) % 16 == 0 && reinterpret_cast<uintptr_t>(a.draft) % 16 == 0;
+    const double c = GREEDY ? 0.0 : 1.4426950408889634074 / a.temperature;  // log2(e) / T
+
+    StreamParams sp{};
+    sp.target = a.draft;  // every draft row is read as a row of the pass
+    sp.draft = nullptr;
+    sp.cu = nullptr;      // no offsets: every row is real
+    sp.B = a.B;
+    sp.V = a.V;
+    sp.draft_slots = 0;
+    sp.draft_stride = 0;
+    sp.g = g;
+    sp.tma = tma;
+    sp.piece_smem = (int)align_up((size_t)g.Q * e, 128);
+    sp.c = (float)c;
+    sp.status = reinterpret_cast<uint32_t *>(ws + L.status);
+    sp.cu_flag = sp.status + 1;
+    sp.part = reinterpret_cast<Partial *>(ws + L.part1);
+
+    ConfParams cp{};
+    cp.draft = a.draft;
+    cp.tokens = a.tokens;
+    cp.kmax = a.kmax;
+    cp.B = a.B;
+    cp.Kmax = a.Kmax;
+    cp.V = a.V;
+    cp.g = g;
+    cp.c = sp.c;
+    cp.out_conf = a.out_conf;
+    cp.status = sp.status;
+    cp.part = sp.part;
+
+    cudaError_t err = prepare_stream<T, GREEDY>();
+    if (err != cudaSuccess)
+        return err;
+    const int grid1 = (g.P + kStreamWarps - 1) / kStreamWarps;
+    tr.begin(s);
+    stream_kernel<T, GREEDY><<<grid1, kStreamThreads, (size_t)kStreamWarps * kRing * sp.piece_smem,
+                              s>>>(sp);
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)((rows + kFinishWarps - 1) / kFinishWarps));
+    cfg.blockDim = dim3(kFinishThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((err = cudaLaunchKernelEx(&cfg, confidence_kernel<T, GREEDY>, cp)) != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+cudaError_t launch_confidence(const ConfArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const bool greedy = a.temperature == 0.0;
+    if (a.dtype == 0)
+        return greedy ? launch_conf_typed<float, true>(a, s, tr)
+                      : launch_conf_typed<float, false>(a, s, tr);
+    return greedy ? launch_conf_typed<uint16_t, true>(a, s, tr)
+                  : launch_conf_typed<uint16_t, false>(a, s, tr);
+}
+
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
 {
     const bool greedy = a.temperature == 0.0;

@@ -31,7 +31,7 @@ SPEC_DCUT_MAX_CANDIDATES = 8192
 EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
            "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
-           "spec_verify_sample_static", "dcut_allocate_cost")
+           "spec_verify_sample_static", "dcut_allocate_cost", "spec_draft_confidence")
 SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -65,6 +65,8 @@ def _load():
     lib.dcut_allocate.argtypes = [P, P, I32, I32, I32, F32, P, P, P, P, SZ, P]
     lib.dcut_allocate_cost.argtypes = [P, P, I32, I32, ctypes.c_double, P, P, P, P, SZ, P]
     lib.dcut_allocate_cost.restype = INT
+    lib.spec_draft_confidence.argtypes = [P, INT, P, P, I32, I32, I32, F32, P, P, SZ, P]
+    lib.spec_draft_confidence.restype = INT
     lib.dcut_allocate.restype = INT
     lib.spec_get_device_status.argtypes = [P, P]
     lib.spec_get_device_status.restype = INT
@@ -233,6 +235,20 @@ def dcut_allocate_cost(conf, kmax, B: int, Kmax: int, max_cost: float, out_depth
         _dev(out_depth, "out_depth", torch.int32, B, allow_none=B == 0),
         _dev(out_cu, "out_cu", torch.int32, B + 1),
         _dev(out_benefit, "out_benefit", torch.float64, B, allow_none=True),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_draft_confidence(draft_logits, draft_tokens, kmax, B: int, Kmax: int, V: int,
+                          temperature: float, out_conf, workspace, stream=None) -> int:
+    n = B * Kmax
+    if n == 0:
+        return SPEC_OK
+    return LIB.spec_draft_confidence(
+        _dev(draft_logits, "draft_logits", min_numel=n * V), dtype_code(draft_logits),
+        _dev(draft_tokens, "draft_tokens", torch.int32, n),
+        _dev(kmax, "kmax", torch.int32, B), B, Kmax, V, float(temperature),
+        _dev(out_conf, "out_conf", torch.float32, n),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
 

@@ -199,6 +199,33 @@ int dcut_allocate_cost(const float *conf, const int32_t *kmax, int32_t B, int32_
                        spec_stream_t stream);
 
 /*
+ * Prefix confidence of drafted tokens, the input D-cut ranks: D-cut moves
+ * verification depth by per-request prefix confidence ("Tencent Hunyuan
+ * Turns Speculative Decoding Into a Full Open-Source Stack", "What problem
+ * does it solve", inference layer).  This library's reading: the confidence
+ * of drafted token x_{i,j} is the drafter's own probability of it,
+ *   out_conf[i*Kmax + j] = softmax(draft row i*Kmax + j / T)(x_{i,j})   j < kmax[i]
+ *   out_conf[i*Kmax + j] = 0                                            j >= kmax[i]
+ * and at T == 0 (a greedy drafter) 1 when x_{i,j} is the row's lowest-index
+ * maximum, else 0.  The output feeds dcut_allocate's conf directly (same
+ * [B][Kmax] layout).
+ *
+ *   draft_logits  [B*Kmax][V] f32 or bf16, padded: row i*Kmax + j (every row
+ *                 is read, also those past kmax[i])
+ *   draft_tokens  int32 [B*Kmax], kmax int32 [B] (device)
+ *   out_conf      float [B*Kmax]
+ * A workspace of spec_workspace_size(B, B * (Kmax + 1), V) bytes suffices.
+ * A failing row (NaN / +inf / all masked, or a token outside [0, V)) gets
+ * NaN and sets the device status; kmax outside [0, Kmax] is
+ * SPEC_ERR_INVALID_ARG on the device.  Two kernel launches: the streaming
+ * pass over the B*Kmax rows and a per-row kernel, its programmatic dependent.
+ */
+int spec_draft_confidence(const void *draft_logits, int dtype, const int32_t *draft_tokens,
+                          const int32_t *kmax, int32_t B, int32_t Kmax, int32_t V,
+                          float temperature, float *out_conf, void *workspace, size_t ws_bytes,
+                          spec_stream_t stream);
+
+/*
  * spec_verify_sample without a workspace, for callers that cannot allocate
  * device memory: an engine whose memory pool already owns all of HBM (for
  * its KV cache), a plugin whose host runtime forbids allocations outside its
