@@ -70,6 +70,9 @@ def load(path: str | None = None):
         lib.oracle_dcut_schedule_cost.argtypes = [_p, _p, _i32, _i32, _f64, _p, _p, _p]
         lib.oracle_draft_confidence.argtypes = [_p, ctypes.c_int, _p, _p, _i32, _i32, _i64, _f64,
                                                 _p]
+        lib.oracle_draft_sample.argtypes = [_p, ctypes.c_int, _p, _i32, _i32, _i64, _f64, _p, _p,
+                                            _p]
+        lib.oracle_acceptance_stats.argtypes = [_p, _p, _i32, _i32, _p, _p, _p]
         if path is None:
             _lib = lib
         return lib
@@ -280,3 +283,29 @@ def draft_confidence(draft, tokens, kmax, temperature: float, lib=None):
     st = (lib or load()).oracle_draft_confidence(_ptr(d), dt, _ptr(tok), _ptr(km), B, Kmax, V,
                                                  float(temperature), _ptr(out))
     return st, out[:B * Kmax].reshape(B, Kmax) if B else out[:0]
+
+
+def draft_sample(draft, kmax, Kmax: int, temperature: float, u, lib=None):
+    """Drafted tokens x ~ q (inverse CDF at u) for padded rows; -1 past kmax."""
+    d, dt = _logits(draft)
+    km = _np(kmax, np.int32)
+    uu = _np(u, np.float32)
+    B = km.size
+    V = d.shape[-1]
+    tok = np.full(max(B * Kmax, 1), -7, np.int32)
+    conf = np.full(max(B * Kmax, 1), -7.0, np.float32)
+    st = (lib or load()).oracle_draft_sample(_ptr(d), dt, _ptr(km), B, Kmax, V,
+                                             float(temperature), _ptr(uu), _ptr(tok), _ptr(conf))
+    return st, tok[:B * Kmax], conf[:B * Kmax]
+
+
+def acceptance_stats(accept_len, cu_draft, Kmax: int, lib=None):
+    a = _np(accept_len, np.int32)
+    cu = _np(cu_draft, np.int32)
+    B = a.size
+    reached = np.full(max(Kmax, 1), -7, np.int32)
+    accepted = np.full(max(Kmax, 1), -7, np.int32)
+    mean = _f64(-1.0)
+    st = (lib or load()).oracle_acceptance_stats(_ptr(a), _ptr(cu), B, Kmax, _ptr(reached),
+                                                 _ptr(accepted), ctypes.byref(mean))
+    return st, reached[:Kmax], accepted[:Kmax], mean.value

@@ -753,3 +753,110 @@ int oracle_draft_confidence(const void *draft, int dtype, const int32_t *tokens,
     }
     return first_err;
 }
+
+/* ------------------------------------------------------------------------ */
+/* drafted tokens and acceptance statistics                                  */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The step before verification: the drafter proposes its tokens
+ * ("Tencent Hunyuan Turns Speculative Decoding Into a Full Open-Source
+ * Stack", "What problem does it solve": a lightweight drafter proposes the
+ * candidate sequence).  Reading: for a drafter that samples, x_{i,j} is the
+ * inverse CDF of q_{i,j} = softmax(draft row (i, j) / T) at the uniform
+ * u[i*Kmax + j] (smallest v with C(v) > u * S, as for the final draw);
+ * greedy (T = 0) takes the lowest-index maximum.  out_conf = q(x) (1 at
+ * T = 0).  Rows j >= kmax[i] give token -1 and conf 0; a failing row gives
+ * -1 and NaN and the first error is returned.
+ */
+int oracle_draft_sample(const void *draft, int dtype, const int32_t *kmax, int32_t B,
+                        int32_t Kmax, int64_t V, double T, const float *u, int32_t *out_tokens,
+                        float *out_conf)
+{
+    if (B < 0 || Kmax < 0 || Kmax > ORC_MAX_DRAFT || V <= 0 || V > INT32_MAX || !(T >= 0) ||
+        isinf(T) || (dtype != ORC_F32 && dtype != ORC_BF16))
+        return ORC_ERR_INVALID_ARG;
+    double *w = (double *)malloc((size_t)V * sizeof(double));
+    if (!w)
+        return ORC_ERR_INVALID_ARG;
+    int first_err = ORC_OK;
+    for (int32_t i = 0; i < B; ++i) {
+        if (kmax[i] < 0 || kmax[i] > Kmax) {
+            free(w);
+            return ORC_ERR_INVALID_ARG;
+        }
+        for (int32_t j = 0; j < Kmax; ++j) {
+            int64_t r = (int64_t)i * Kmax + j;
+            out_tokens[r] = -1;
+            out_conf[r] = 0.0f;
+            if (j >= kmax[i])
+                continue;
+            int err;
+            if (T == 0.0) {
+                int32_t g;
+                err = oracle_argmax_row(draft, dtype, r, V, &g);
+                if (err == ORC_OK) {
+                    out_tokens[r] = g;
+                    out_conf[r] = 1.0f;
+                }
+            } else {
+                err = oracle_softmax_row(draft, dtype, r, V, T, w);
+                if (err == ORC_OK) {
+                    int64_t x = oracle_inverse_cdf(w, V, (double)u[r], NULL, NULL);
+                    if (x < 0) {
+                        err = ORC_ERR_NONFINITE;
+                    } else {
+                        out_tokens[r] = (int32_t)x;
+                        out_conf[r] = (float)w[x];
+                    }
+                }
+            }
+            if (err != ORC_OK) {
+                out_conf[r] = NAN;
+                if (first_err == ORC_OK)
+                    first_err = err;
+            }
+        }
+    }
+    free(w);
+    return first_err;
+}
+
+/*
+ * The statistics the pages report for a drafter (mean accepted length;
+ * per-position acceptance: the French/Russian page's numbers at T = 0 and by
+ * position; the online evaluation reads both from the serving engine,
+ * "Tencent Hunyuan Turns Speculative Decoding ...", "Five angles worth a
+ * closer look", item 4), from one verification call's outputs:
+ *   reached[j]  = #{ i : K_i > j and a_i >= j }   (position j was tested)
+ *   accepted[j] = #{ i : a_i > j }                 (and accepted)
+ *   mean accepted length = sum a_i / #requests
+ * over requests whose a_i >= 0 (poisoned requests are left out), j < Kmax.
+ */
+int oracle_acceptance_stats(const int32_t *accept_len, const int32_t *cu, int32_t B,
+                            int32_t Kmax, int32_t *out_reached, int32_t *out_accepted,
+                            double *out_mean)
+{
+    if (B < 0 || Kmax < 0 || Kmax > ORC_MAX_DRAFT)
+        return ORC_ERR_INVALID_ARG;
+    for (int32_t j = 0; j < Kmax; ++j)
+        out_reached[j] = out_accepted[j] = 0;
+    int64_t total = 0, n = 0;
+    for (int32_t i = 0; i < B; ++i) {
+        int32_t a = accept_len[i], k = cu[i + 1] - cu[i];
+        if (a < 0)
+            continue;
+        if (a > k || k > Kmax)
+            return ORC_ERR_INVALID_ARG;
+        total += a;
+        ++n;
+        for (int32_t j = 0; j < k; ++j) {
+            if (a >= j)
+                out_reached[j] += 1;
+            if (a > j)
+                out_accepted[j] += 1;
+        }
+    }
+    *out_mean = n > 0 ? (double)total / (double)n : 0.0;
+    return ORC_OK;
+}

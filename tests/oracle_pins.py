@@ -717,3 +717,81 @@ def pin_draft_confidence(lib):
 
 
 ALL_PINS += [pin_draft_confidence]
+
+
+# ---------------------------------------------------------------------------
+# drafted tokens and acceptance statistics
+# ---------------------------------------------------------------------------
+
+
+def pin_draft_sample(lib):
+    """x = searchsorted(cumsum(scipy softmax), u*S, 'right') on random rows
+    (f32, bf16); conf = q(x); T = 0: numpy's first-occurrence argmax; rows
+    past kmax give -1; errors."""
+    rng = np.random.default_rng(31)
+    B, Kmax, V = 6, 3, 41
+    l = (rng.standard_normal((B * Kmax, V)) * 2).astype(np.float32)
+    l[rng.random(l.shape) < 0.2] = -np.inf  # masked entries never drawn
+    kmax = np.array([3, 1, 0, 2, 3, 3], np.int32)
+    u = rng.random(B * Kmax).astype(np.float32)
+    for T in (0.7, 1.0):
+        for rows, exact in ((l, l), (_to_bf16_bits(l), None)):
+            if exact is None:
+                exact = (rows.astype(np.uint32) << 16).view(np.float32)
+            st, tok, conf = O.draft_sample(rows, kmax, Kmax, T, u, lib=lib)
+            assert st == O.OK
+            for i in range(B):
+                for j in range(Kmax):
+                    r = i * Kmax + j
+                    if j >= kmax[i]:
+                        assert tok[r] == -1 and conf[r] == 0.0
+                        continue
+                    q = _ref_softmax(exact[r], T)
+                    C = np.cumsum(q)
+                    want = int(np.searchsorted(C, float(u[r]) * C[-1], side="right"))
+                    assert tok[r] == want, (T, i, j, tok[r], want)
+                    assert abs(conf[r] - q[want]) <= 1e-6 * q[want]
+    g = np.argmax(l, axis=1)
+    st, tok, conf = O.draft_sample(l, kmax, Kmax, 0.0, u, lib=lib)
+    assert st == O.OK
+    for i in range(B):
+        for j in range(Kmax):
+            r = i * Kmax + j
+            assert tok[r] == (g[r] if j < kmax[i] else -1)
+    bad = l.copy()
+    bad[1, 3] = np.inf  # request 0, position 1
+    st, tok, conf = O.draft_sample(bad, kmax, Kmax, 1.0, u, lib=lib)
+    assert st == O.ERR_NONFINITE and tok[1] == -1 and np.isnan(conf[1]) and tok[0] >= 0
+
+
+def pin_draft_sample_chi_square(lib):
+    """The drawn tokens follow softmax(l / T): Pearson chi-square, alpha 1e-3."""
+    rng = np.random.default_rng(32)
+    row = np.array([0.3, -1.2, 2.0, 0.0, 1.1, -0.4, 0.7, -2.0], np.float32)
+    n = 200_000
+    rows = np.tile(row, (n, 1))
+    u = rng.random(n).astype(np.float32)
+    for T in (0.7, 1.0):
+        st, tok, _ = O.draft_sample(rows, np.ones(n, np.int32), 1, T, u, lib=lib)
+        assert st == O.OK
+        ok, chi2, dof = _chi2_ok(np.bincount(tok, minlength=8), _ref_softmax(row, T))
+        assert ok, (T, chi2, dof)
+
+
+def pin_acceptance_stats(lib):
+    g = _golden("acceptance_stats.json")
+    k = np.array(g["k"], np.int32)
+    cu = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
+    st, reached, accepted, mean = O.acceptance_stats(np.array(g["accept_len"], np.int32), cu,
+                                                     g["Kmax"], lib=lib)
+    assert st == O.OK
+    assert reached.tolist() == g["expected_reached"], reached
+    assert accepted.tolist() == g["expected_accepted"], accepted
+    assert abs(mean - g["expected_mean"]) < 1e-15
+    # a length beyond its request's K is an error
+    bad = np.array(g["accept_len"], np.int32)
+    bad[1] = 3
+    assert O.acceptance_stats(bad, cu, g["Kmax"], lib=lib)[0] == O.ERR_INVALID_ARG
+
+
+ALL_PINS += [pin_draft_sample, pin_draft_sample_chi_square, pin_acceptance_stats]

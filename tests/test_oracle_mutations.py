@@ -57,6 +57,14 @@ MUTANTS = [
      "err = softmax_at(draft, dtype, r > 0 ? r - 1 : r, V, T, x, &c);"),
     ("greedy confidence ignores the argmax", "c = (err == ORC_OK && g == x) ? 1.0 : 0.0;",
      "c = 1.0;"),
+    ("draft sample reads the next row", "err = oracle_softmax_row(draft, dtype, r, V, T, w);",
+     "err = oracle_softmax_row(draft, dtype, r + 1 < (int64_t)B * Kmax ? r + 1 : r, V, T, w);"),
+    ("draft sample conf of the wrong entry", "out_conf[r] = (float)w[x];",
+     "out_conf[r] = (float)w[x > 0 ? x - 1 : x];"),
+    ("acceptance counts an untested position", "            if (a >= j)\n                out_reached[j] += 1;",
+     "            if (a >= j - 1)\n                out_reached[j] += 1;"),
+    ("acceptance mean over every request", "    *out_mean = n > 0 ? (double)total / (double)n : 0.0;",
+     "    *out_mean = B > 0 ? (double)total / (double)B : 0.0;"),
     ("cost variant keeps the last maximising depth", "if (b > best) { /* strict",
      "if (b >= best) { /* strict"),
     ("cost variant sorts ascending",
