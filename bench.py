@@ -2,6 +2,7 @@
 """Benchmark of batched draft verification (+ D-cut) on B300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mtp|block|block_greedy|dcut|tiny]
+    python bench.py --workload draft|draft_greedy   (the drafter's step: spec_draft_sample)
     python bench.py --impl reference ...     (the CPU oracle, timed on the host cores)
 
 One step = one pass of the whole verification path over one batch whose
@@ -46,12 +47,23 @@ WORKLOADS = {  # name -> (workload, temperature)
     "block_greedy": (W.BLOCK, 0.0),
     "dcut": (W.DCUT, 1.0),
     "tiny": (W.TINY, 1.0),
+    # the drafter's step of the block workload: draw 16 tokens per request from
+    # the padded drafter rows (spec_draft_sample); its own metric
+    "draft": (W.BLOCK, 0.7),
+    "draft_greedy": (W.BLOCK, 0.0),
 }
-# the sources of the streaming kernel (the roofline's kernel): a recorded ncu
-# traffic figure holds only while these hash the same
-KERNEL_SOURCES = ["draft_verification_02_b300/csrc/stream_kernel.cuh",
-                  "draft_verification_02_b300/csrc/verify_params.cuh",
-                  "draft_verification_02_b300/csrc/common.cuh"]
+DRAFT_WORKLOADS = ("draft", "draft_greedy")
+DRAFT_METRIC = "drafted positions/sec and achieved HBM GB/s (fraction of peak) at 1 B300"
+# the sources of each roofline kernel: a recorded ncu traffic figure holds
+# only while these hash the same
+KERNEL_SOURCES = {
+    "stream_kernel": ["draft_verification_02_b300/csrc/stream_kernel.cuh",
+                      "draft_verification_02_b300/csrc/verify_params.cuh",
+                      "draft_verification_02_b300/csrc/common.cuh"],
+    "draft_sample_kernel": ["draft_verification_02_b300/csrc/finish_kernel.cuh",
+                            "draft_verification_02_b300/csrc/verify_params.cuh",
+                            "draft_verification_02_b300/csrc/common.cuh"],
+}
 
 
 def parse_args(argv=None):
@@ -134,9 +146,9 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(kernel: str = "stream_kernel") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -148,7 +160,7 @@ def recorded_traffic(workload: str, kernel: str):
     valid only while the kernel sources still hash the same."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     try:
-        want = kernel_source_hash()
+        want = kernel_source_hash(kernel)
         with open(path) as f:
             for line in f:
                 p = line.split()
@@ -614,6 +626,287 @@ def run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist)
 
 
 # ---------------------------------------------------------------------------
+# the drafter's step: spec_draft_sample over B*Kmax padded drafter rows
+# ---------------------------------------------------------------------------
+
+
+def draft_inputs(w, T, device, rep):
+    """Drafter logits [B*K][V] (the block workload's draft rows, every request
+    drafting K tokens), kmax and the per-row uniforms u_draft."""
+    b = W.make_verify_batch(w, T, device, rep=rep)
+    g = torch.Generator().manual_seed(w.seed * 7919 + rep)
+    u = torch.rand(w.B * w.k, generator=g, dtype=torch.float32).to(device)
+    kmax = torch.full((w.B,), w.k, dtype=torch.int32, device=device)
+    return {"draft": b.draft_logits, "kmax": kmax, "u": u}
+
+
+def oracle_draft_rows(orc, d, u, T, rows):
+    """The oracle's draws for the given rows (each row drawn on its own)."""
+    n = len(rows)
+    st, tok, conf = orc.draft_sample(d[rows], np.ones(n, np.int32), 1, T, u[rows])
+    if st != orc.OK:
+        raise RuntimeError(f"oracle status {st}")
+    return n
+
+
+def oracle_draft_rate(d, u, T, seconds, threads, rows_per_call=4):
+    import oracle as orc
+    orc.load()
+    n_rows = d.shape[0]
+    done = 0
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        i = 0
+        while True:
+            chunks = [[(i + k * rows_per_call + j) % n_rows for j in range(rows_per_call)]
+                      for k in range(threads)]
+            i += threads * rows_per_call
+            done += sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r), chunks))
+            if time.perf_counter() - t0 >= seconds:
+                break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def host_draft(x):
+    x = x.detach().cpu().contiguous()
+    if x.dtype == torch.bfloat16:
+        return x.view(torch.int16).numpy().view(np.uint16)
+    return x.numpy()
+
+
+def run_draft(args, dist):
+    from draft_verification_02_b300 import specverify as sv
+    from draft_verification_02_b300.verifier import Verifier
+
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    sampler = ClockSampler(device, enabled=not args.no_clocks)
+    dist.init("nccl")
+    w, T = WORKLOADS[args.workload]
+    Kmax, n_rows = w.k, w.B * w.k
+    v = Verifier(w.B, w.B * (Kmax + 1), w.V, device=device)
+    e = 4 if w.dtype == "f32" else 2
+    alg_bytes = n_rows * w.V * e  # every drafter row read once
+
+    def make_set(rep):
+        s = draft_inputs(w, T, device, rep)
+        s["tokens"] = torch.empty(n_rows, dtype=torch.int32, device=device)
+        s["conf"] = torch.empty(n_rows, dtype=torch.float32, device=device)
+        return s
+
+    first = make_set(rank_seed_offset(dist.rank))
+    n_sets = max(2, min(64, math.ceil(2.2 * l2_bytes(device) / alg_bytes)))
+    sets = [first] + [make_set(rank_seed_offset(dist.rank) + r) for r in range(1, n_sets)]
+
+    def step(s, trace=None):
+        if trace is not None:
+            sv.spec_set_trace(trace)
+        st = sv.spec_draft_sample(s["draft"], s["kmax"], w.B, Kmax, w.V, T,
+                                  None if T == 0 else s["u"], s["tokens"], s["conf"],
+                                  v.workspace)
+        if trace is not None:
+            sv.spec_set_trace(None)
+        return st
+
+    n0 = sv.spec_kernel_launch_count()
+    for k in range(max(1, args.warmup)):
+        sv.check(step(sets[k % n_sets]), "warm-up step")
+    torch.cuda.synchronize(device)
+    launches_per_step = (sv.spec_kernel_launch_count() - n0) // max(1, args.warmup)
+    sv.check(v.device_status(), "device status after warm-up")
+
+    K = args.steps
+    G = max(1, min(K, args.graph_steps))
+    stream = torch.cuda.Stream(device)
+
+    # T > 0: one kernel reads and draws (draft_sample_kernel); T = 0: the
+    # streaming pass, then the per-row argmax merge
+    kernels = ["draft_sample_kernel"] if T > 0 else ["stream_kernel", "draft_greedy_kernel"]
+
+    def capture(n_steps, offset, traced):
+        evs = []
+        for _ in range(n_steps):
+            ev = ([torch.cuda.Event(enable_timing=True) for _ in range(len(kernels) + 1)]
+                  if traced else None)
+            for x in ev or []:
+                x.record()
+            evs.append(ev)
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n_steps):
+                step(sets[(offset + k) % n_sets], evs[k])
+        return g, evs
+
+    g_main = capture(G, 0, False)[0]
+    n_rep, rem = divmod(K, G)
+    g_rem = capture(rem, n_rep * G, False)[0] if rem else None
+    g_traced, ev_tr = capture(G, 0, True)
+    g_main.replay()
+    g_traced.replay()
+    torch.cuda.synchronize(device)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler.wait_first_sample(timeout=60.0)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n_rep):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    dist.barrier()
+    with torch.cuda.stream(stream):
+        g_traced.replay()
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    elapsed_ms_max = dist.max(start.elapsed_time(end), device)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    sv.check(v.device_status(), "device status after the timed region")
+    kernel_us = {name: statistics.mean(ev_tr[k][q].elapsed_time(ev_tr[k][q + 1]) * 1e3
+                                       for k in range(G))
+                 for q, name in enumerate(kernels)}
+    roof_kernel = kernels[0]  # the kernel that reads the rows
+    stream_us = kernel_us[roof_kernel]
+
+    value = dist.sum(n_rows * K, device) / (elapsed_ms_max / 1e3)
+    ms_per_step = elapsed_ms_max / K
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg_bytes / (stream_us / 1e6) / 1e9
+    step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+
+    # end to end: drafter logits and uniforms from pinned host memory, tokens
+    # and q(x) read back, through the same public call
+    e2e = None
+    if not args.no_e2e:
+        steps = max(1, min(args.e2e_steps, K))
+        host = [{n: sets[k][n].cpu().pin_memory() for n in ("draft", "kmax", "u")}
+                for k in range(min(n_sets, 3))]
+        out_t = torch.empty(n_rows, dtype=torch.int32).pin_memory()
+        out_c = torch.empty(n_rows, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+        d2h = out_t.numel() * 4 + out_c.numel() * 4
+        cs = torch.cuda.current_stream(device)
+
+        def one(k):
+            s, hs = sets[k % len(host)], host[k % len(host)]
+            for n in ("draft", "kmax", "u"):
+                s[n].copy_(hs[n], non_blocking=True)
+            sv.check(step(s), "draft step")
+            out_t.copy_(s["tokens"], non_blocking=True)
+            out_c.copy_(s["conf"], non_blocking=True)
+
+        for k in range(3):
+            one(k)
+        torch.cuda.synchronize(device)
+        dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cs)
+        for k in range(steps):
+            one(k)
+        e1.record(cs)
+        torch.cuda.synchronize(device)
+        dist.barrier()
+        ms = dist.max(e0.elapsed_time(e1), device)
+        e2e = {"value": dist.sum(n_rows * steps, device) / (ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": steps,
+               "ms_per_step": ms / steps}
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, n, el = oracle_draft_rate(host_draft(first["draft"]), host_draft(first["u"]), T,
+                                        args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} drafter rows of input set 0 ({workload_desc(w, T)}), drawn by "
+                         f"the oracle 4 rows per call on {threads} host threads, {el:.1f} s"}
+
+    line = {
+        "metric": DRAFT_METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {
+            "workload": f"drafter step of {workload_desc(w, T)}: {n_rows} rows, Kmax={Kmax}",
+            "B": w.B, "Kmax": Kmax, "V": w.V, "logits_dtype": w.dtype, "temperature": T,
+            "drafted_positions_per_step": n_rows,
+            "l2": f"inputs rotate through {n_sets} independent sets "
+                  f"({n_sets * alg_bytes / 1e6:.0f} MB > 2x L2 of {l2_bytes(device) / 1e6:.0f} MB)",
+            "timing": f"CUDA graphs of {G} steps replayed, CUDA events on the launching stream;"
+                      " per-kernel times from a traced replay",
+            "parallelism": f"{dist.world} GPU(s), independent batches per GPU",
+        },
+        "hbm_gbs_step": step_gbs,
+        "hbm_frac_step": step_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": achieved,
+                     "peak": peak, "peak_kind": f"of {peak_kind}", "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": recorded_traffic(args.workload, roof_kernel),
+                     "algorithmic_bytes_per_launch": alg_bytes, "launch_us_mean": stream_us},
+        "kernels_us": dict(kernel_us, note="from one traced replay of the step graph after "
+                                           "the timed region (events between kernels)"),
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def run_reference_draft(args, dist):
+    import oracle as orc
+    orc.load()
+    w, T = WORKLOADS[args.workload]
+    s = draft_inputs(w, T, "cpu", 0)
+    d, u = host_draft(s["draft"]), host_draft(s["u"])
+    n_rows = d.shape[0]
+    threads = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle_draft_rows(orc, d, u, T, [0])
+    t_row = max(time.perf_counter() - t0, 1e-5)
+    per_step = args.reference_seconds / max(1, args.steps + args.warmup)
+    n = int(max(threads, min(n_rows, per_step * threads / t_row)))
+    ex = ThreadPoolExecutor(threads)
+
+    def one(k):
+        rows = [(k * n + j) % n_rows for j in range(n)]
+        chunks = [rows[c::threads] for c in range(threads) if rows[c::threads]]
+        return sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r), chunks))
+
+    for k in range(args.warmup):
+        one(k)
+    done = 0
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        done += one(k)
+    el = time.perf_counter() - t0
+    ex.shutdown()
+    value = done / el
+    desc = f"drafter step of {workload_desc(w, T)}: {n_rows} rows"
+    print(json.dumps({
+        "impl": "reference", "metric": DRAFT_METRIC, "value": value, "unit": UNIT,
+        "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": el * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "B": w.B, "Kmax": w.k, "V": w.V, "logits_dtype": w.dtype,
+                   "temperature": T, "sample_per_step": f"{n} of {n_rows} rows"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{n} drafter rows per step of {desc}, on {threads} host "
+                                   "threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 
@@ -621,6 +914,8 @@ def run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist)
 def run_reference(args, dist):
     if dist.rank != 0:
         return  # the other ranks exit without work
+    if args.workload in DRAFT_WORKLOADS:
+        return run_reference_draft(args, dist)
     import oracle as orc
     orc.load()
     w, T = WORKLOADS[args.workload]
@@ -675,6 +970,8 @@ def main(argv=None):
     dist = Dist()
     if args.impl == "reference":
         run_reference(args, dist)
+    elif args.workload in DRAFT_WORKLOADS:
+        run_draft(args, dist)
     else:
         run_ours(args, dist)
 

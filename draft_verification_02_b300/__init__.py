@@ -10,7 +10,7 @@ _BINDING_NAMES = {
     "spec_workspace_size", "spec_workspace_init", "spec_verify_greedy", "spec_verify_sample",
     "dcut_allocate", "spec_get_device_status", "spec_status_string", "spec_set_trace",
     "spec_kernel_launch_count", "spec_verify_sample_static", "dcut_allocate_cost",
-    "spec_draft_confidence",
+    "spec_draft_confidence", "spec_draft_sample", "spec_acceptance_stats",
     "SpecError", "check",
 }
 

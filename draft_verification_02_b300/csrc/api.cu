@@ -265,6 +265,61 @@ int spec_draft_confidence(const void *draft_logits, int dtype, const int32_t *dr
     return cuda_status(sv::launch_confidence(a, (cudaStream_t)stream, tr));
 }
 
+int spec_draft_sample(const void *draft_logits, int dtype, const int32_t *kmax, int32_t B,
+                      int32_t Kmax, int32_t V, float temperature, const float *u_draft,
+                      int32_t *out_tokens, float *out_conf, void *workspace, size_t ws_bytes,
+                      spec_stream_t stream)
+{
+    if (!valid_dtype(dtype) || B < 0 || B > SPEC_MAX_BATCH || Kmax < 0 ||
+        Kmax > SPEC_MAX_DRAFT || V < 1 || V > sv::kMaxVocab || !(temperature >= 0.f) ||
+        std::isinf(temperature))
+        return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)B * Kmax == 0)
+        return SPEC_OK;
+    if (!draft_logits || !kmax || !out_tokens || !out_conf || (temperature > 0.f && !u_draft))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(B, (int64_t)B * (Kmax + 1), V))
+        return SPEC_ERR_WORKSPACE;
+    sv::DraftArgs a{};
+    a.draft = draft_logits;
+    a.dtype = dtype;
+    a.kmax = kmax;
+    a.B = B;
+    a.Kmax = Kmax;
+    a.V = V;
+    a.temperature = (double)temperature;
+    a.u = u_draft;
+    a.out_tokens = out_tokens;
+    a.out_conf = out_conf;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_draft(a, (cudaStream_t)stream, tr));
+}
+
+int spec_acceptance_stats(const int32_t *accept_len, const int32_t *cu_draft, int32_t B,
+                          int32_t Kmax, int32_t *out_reached, int32_t *out_accepted,
+                          float *out_mean, void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (B < 0 || B > SPEC_MAX_BATCH || Kmax < 0 || Kmax > SPEC_MAX_DRAFT)
+        return SPEC_ERR_INVALID_ARG;
+    if ((B > 0 && (!accept_len || !cu_draft)) || (Kmax > 0 && (!out_reached || !out_accepted)) ||
+        !out_mean)
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < spec_workspace_size(0, 0, 0))
+        return SPEC_ERR_WORKSPACE;
+    sv::StatsArgs a{};
+    a.accept_len = accept_len;
+    a.cu = cu_draft;
+    a.B = B;
+    a.Kmax = Kmax;
+    a.out_reached = out_reached;
+    a.out_accepted = out_accepted;
+    a.out_mean = out_mean;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_acceptance_stats(a, (cudaStream_t)stream, tr));
+}
+
 int spec_get_device_status(void *workspace, spec_stream_t stream)
 {
     if (!workspace)

@@ -288,17 +288,18 @@ __device__ __forceinline__ int piece_find(const DrawCtx d, const T *tb, const T 
 // aligned), then every thread sums its contiguous piece (kept in piece[]
 // for the search) and the pieces are added as float-float pairs in a fixed
 // order.  Once any copy of this call has timed out nothing more is copied.
+// With copy == false the slice is already staged.
 template <typename T>
 __device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, const T *trow,
                                        const T *drow, int c0, int len, T *tb, T *db,
                                        uint64_t *bar, uint32_t *phase, float *piece, ff *wred,
-                                       int *expired)
+                                       int *expired, bool copy = true)
 {
     constexpr int E = Elem<T>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // earlier readers of the buffers, piece and wred are done
     const bool stop = __syncthreads_or(tid == 0 && (read_status(p.status) & ST_TIMEOUT));
-    if (!stop && len > 0) {
+    if (copy && !stop && len > 0) {
         if (p.tma) {
             if (tid == 0) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -353,6 +354,193 @@ __device__ __forceinline__ void st_cluster_row(float *row_m, ff *row_s, float *r
     asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(rs), "f"(s.hi), "f"(s.lo)
                  : "memory");
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(rp), "f"(px) : "memory");
+}
+
+// Shared-memory state of one CTA's part in a cluster draw.
+template <typename T>
+struct DrawShared {
+    T *tb, *db;  // staged slices of the two rows
+    uint64_t *bar;
+    float *piece;
+    ff *wred, *slice_tot, *s_excl;
+    ff (*cl_sum)[kCluster];  // written by every CTA of the cluster
+    int *s_hit, *s_last, *s_cs, *s_past, *s_redo, *s_expired;
+    ff *s_base, *s_target;
+    ff *s_total;  // S, the sum of every weight (may be null)
+};
+
+// The final draw of one cluster: the CTAs split the vocabulary into ncl
+// ranges, weigh theirs (w = max(0, p - q) with d.resid, else the unnormalised
+// p), exchange the range sums through distributed shared memory, and the CTA
+// whose range holds u*S finds the token.  Returns, in every thread of that
+// CTA, the drawn index (or -1 if it found none); -2 in the other CTAs, -1 in
+// all CTAs when no range has mass.  Every CTA of the cluster must call it
+// (it contains cluster barriers); no shared memory of another CTA is touched
+// after it returns.  `staged`: the slice of this CTA's range already in the
+// target buffer (-1 none); phase0: the parity of the copy barrier's next
+// phase.
+template <typename T>
+__device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, const T *trow,
+                                          const T *drow, float uf, uint32_t rank, int ncl,
+                                          const DrawShared<T> &sh, int staged = -1,
+                                          uint32_t phase0 = 0)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    T *tb = sh.tb, *db = sh.db;
+    float *piece = sh.piece;
+    ff *wred = sh.wred, *slice_tot = sh.slice_tot, *s_excl = sh.s_excl;
+    ff(*cl_sum)[kCluster] = sh.cl_sum;
+    int &s_hit = *sh.s_hit, &s_last = *sh.s_last, &s_cs = *sh.s_cs, &s_past = *sh.s_past,
+        &s_redo = *sh.s_redo, &s_expired = *sh.s_expired;
+    ff &s_base = *sh.s_base, &s_target = *sh.s_target;
+    uint64_t &bar = *sh.bar;
+    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
+    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+    int weighed = -1;  // slice staged in shared memory
+    uint32_t phase = phase0;  // parity of the copy barrier's next phase
+
+    // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
+    // second pass over p_a (the same decision in every CTA)
+    int slot = 0;
+    for (int pass = 0; pass < 2; ++pass) {
+        ff mine{0.f, 0.f};
+        for (int sl = 0; sl < nsl; ++sl) {
+            const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+            const ff ss = weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
+                                         wred, &s_expired, !(pass == 0 && sl == 0 && staged == 0));
+            weighed = sl;
+            if (tid == 0)
+                slice_tot[sl] = ss;
+            mine = ff_add(mine, ss);
+        }
+        if (tid < ncl)
+            st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
+        cluster_arrive_release();
+        cluster_wait_acquire();  // (2 + pass) every CTA holds every range sum
+        slot = pass;
+        // S and the range holding u*S, by warp 0 (lane r holds range r): an
+        // inclusive float-float scan in range order, the same in every CTA.
+        // `past` marks u*S at or beyond the end after rounding: then the
+        // last weight > 0 wins.
+        if (warp == 0) {
+            const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
+            ff incl = v;
+#pragma unroll 1
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff n = ff_shfl_up(incl, o);
+                if (lane >= o)
+                    incl = ff_add(n, incl);
+            }
+            const ff S = {__shfl_sync(0xffffffffu, incl.hi, 31),
+                          __shfl_sync(0xffffffffu, incl.lo, 31)};
+            const ff target = ff_mul(S, uf);
+            const unsigned over = __ballot_sync(0xffffffffu, lane < ncl && ff_gt(incl, target));
+            const unsigned mass = __ballot_sync(0xffffffffu, lane < ncl && v.hi > 0.f);
+            const int cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
+            ff excl = ff_shfl_up(incl, 1);
+            if (lane == 0)
+                excl = {0.f, 0.f};
+            const int src = cs < 0 ? 0 : cs;
+            const ff base = {__shfl_sync(0xffffffffu, excl.hi, src),
+                             __shfl_sync(0xffffffffu, excl.lo, src)};
+            if (lane == 0) {
+                if (sh.s_total)
+                    *sh.s_total = S;
+                s_cs = cs;
+                s_past = over == 0u;
+                s_base = base;
+                s_target = target;
+                s_redo = !(S.hi > 0.f);
+            }
+        }
+        __syncthreads();
+        if (!(d.resid && s_redo))
+            break;
+        d.resid = false;  // all-zero residual: draw from p_a instead
+    }
+    // no shared memory of another CTA is touched after this point
+    const int cs = s_cs;
+    bool past = s_past != 0;
+    ff base = s_base;
+    const ff target = s_target;
+    if ((int)rank != cs)
+        return cs < 0 ? -1 : -2;  // -1: no mass at all (never with finite rows)
+
+    // ---- owner CTA: the slice, then the thread piece, then the element
+    int sl = -1;
+    {
+        ff b2 = base;
+        for (int s2 = 0; s2 < nsl && !past; ++s2) {
+            const ff next = ff_add(b2, slice_tot[s2]);
+            if (ff_gt(next, target)) {
+                sl = s2;
+                break;
+            }
+            b2 = next;
+        }
+        if (sl >= 0) {
+            base = b2;
+        } else {  // the last slice with mass
+            past = true;
+            ff bl = base;
+            b2 = base;
+            sl = nsl - 1;
+            for (int s2 = 0; s2 < nsl; ++s2) {
+                if (slice_tot[s2].hi > 0.f) {
+                    sl = s2;
+                    bl = b2;
+                }
+                b2 = ff_add(b2, slice_tot[s2]);
+            }
+            base = bl;
+        }
+    }
+    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+    if (sl != weighed)
+        weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
+    // scan of the piece sums (float-float, fixed order).  A piece's lower end
+    // is the previous piece's upper end bit for bit, so the pieces tile the
+    // slice with no gap and no overlap.
+    ff incl{piece[tid], 0.f};
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(incl, o);
+        if (lane >= o)
+            incl = ff_add(n, incl);
+    }
+    ff excl = ff_shfl_up(incl, 1);
+    if (lane == 0)
+        excl = {0.f, 0.f};
+    if (tid == 0) {
+        s_hit = INT_MAX;
+        s_last = -1;
+    }
+    if (lane == 31)
+        s_excl[warp] = incl;
+    __syncthreads();
+    ff wbase = base;
+    for (int q = 0; q < warp; ++q)
+        wbase = ff_add(wbase, s_excl[q]);
+    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
+    if (!past && ff_le(lo, target) && ff_gt(hi, target))
+        atomicMin(&s_hit, tid);
+    __syncthreads();
+    // the piece walk repeats the piece sum's additions, so it meets the same
+    // running sums; rem may round up to the piece total: then the piece's
+    // last element with weight > 0
+    constexpr int E = Elem<T>::kPerVec;
+    const int nv = (len + E - 1) / E;
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    if (s_hit == tid) {
+        const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+        s_last = piece_find<T>(d, tb, db, len, v0, v1, rem);
+    } else if (s_hit == INT_MAX) {  // past the end after rounding: the last element with mass
+        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
+        if (lp >= 0)
+            atomicMax(&s_last, lp);
+    }
+    __syncthreads();
+    return s_last >= 0 ? c0 + s_last : -1;
 }
 
 template <typename T>
@@ -557,158 +745,14 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     DrawCtx d = s_d;
     const T *trow = tbase + trow_i * p.V;
     const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
-    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
-    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
-    int weighed = -1;  // slice staged in shared memory
-    uint32_t phase = 0;
-
-    // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
-    // second pass over p_a (the same decision in every CTA)
-    int slot = 0;
-    for (int pass = 0; pass < 2; ++pass) {
-        ff mine{0.f, 0.f};
-        for (int sl = 0; sl < nsl; ++sl) {
-            const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-            const ff ss = weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
-                                         wred, &s_expired);
-            weighed = sl;
-            if (tid == 0)
-                slice_tot[sl] = ss;
-            mine = ff_add(mine, ss);
-        }
-        if (tid < ncl)
-            st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
-        cluster_arrive_release();
-        cluster_wait_acquire();  // (2 + pass) every CTA holds every range sum
-        slot = pass;
-        // S and the range holding u*S, by warp 0 (lane r holds range r): an
-        // inclusive float-float scan in range order, the same in every CTA.
-        // `past` marks u*S at or beyond the end after rounding: then the
-        // last weight > 0 wins.
-        if (warp == 0) {
-            const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
-            ff incl = v;
-#pragma unroll 1
-            for (int o = 1; o < 32; o <<= 1) {
-                const ff n = ff_shfl_up(incl, o);
-                if (lane >= o)
-                    incl = ff_add(n, incl);
-            }
-            const ff S = {__shfl_sync(0xffffffffu, incl.hi, 31),
-                          __shfl_sync(0xffffffffu, incl.lo, 31)};
-            const ff target = ff_mul(S, uf);
-            const unsigned over = __ballot_sync(0xffffffffu, lane < ncl && ff_gt(incl, target));
-            const unsigned mass = __ballot_sync(0xffffffffu, lane < ncl && v.hi > 0.f);
-            const int cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
-            ff excl = ff_shfl_up(incl, 1);
-            if (lane == 0)
-                excl = {0.f, 0.f};
-            const int src = cs < 0 ? 0 : cs;
-            const ff base = {__shfl_sync(0xffffffffu, excl.hi, src),
-                             __shfl_sync(0xffffffffu, excl.lo, src)};
-            if (lane == 0) {
-                s_cs = cs;
-                s_past = over == 0u;
-                s_base = base;
-                s_target = target;
-                s_redo = !(S.hi > 0.f);
-            }
-        }
-        __syncthreads();
-        if (!(d.resid && s_redo))
-            break;
-        d.resid = false;  // all-zero residual: draw from p_a instead
-    }
-    // no shared memory of another CTA is touched after this point
-    const int cs = s_cs;
-    bool past = s_past != 0;
-    ff base = s_base;
-    const ff target = s_target;
-    if ((int)rank != cs) {
-        if (cs < 0 && rank == 0 && tid == 0) {  // no mass at all (never with finite rows)
-            set_status(p.status, ST_NONFINITE);
-            p.out_tokens[trow_i] = -1;
-        }
-        return;
-    }
-
-    // ---- owner CTA: the slice, then the thread piece, then the element
-    int sl = -1;
-    {
-        ff b2 = base;
-        for (int s2 = 0; s2 < nsl && !past; ++s2) {
-            const ff next = ff_add(b2, slice_tot[s2]);
-            if (ff_gt(next, target)) {
-                sl = s2;
-                break;
-            }
-            b2 = next;
-        }
-        if (sl >= 0) {
-            base = b2;
-        } else {  // the last slice with mass
-            past = true;
-            ff bl = base;
-            b2 = base;
-            sl = nsl - 1;
-            for (int s2 = 0; s2 < nsl; ++s2) {
-                if (slice_tot[s2].hi > 0.f) {
-                    sl = s2;
-                    bl = b2;
-                }
-                b2 = ff_add(b2, slice_tot[s2]);
-            }
-            base = bl;
-        }
-    }
-    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-    if (sl != weighed)
-        weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
-    // scan of the piece sums (float-float, fixed order).  A piece's lower end
-    // is the previous piece's upper end bit for bit, so the pieces tile the
-    // slice with no gap and no overlap.
-    ff incl{piece[tid], 0.f};
-#pragma unroll 1
-    for (int o = 1; o < 32; o <<= 1) {
-        const ff n = ff_shfl_up(incl, o);
-        if (lane >= o)
-            incl = ff_add(n, incl);
-    }
-    ff excl = ff_shfl_up(incl, 1);
-    if (lane == 0)
-        excl = {0.f, 0.f};
+    const DrawShared<T> sh{tb,     db,     &bar,   piece,   wred,    slice_tot, s_excl,
+                           cl_sum, &s_hit, &s_last, &s_cs, &s_past, &s_redo, &s_expired,
+                           &s_base, &s_target, nullptr};
+    const int y0 = draw_token<T>(p, d, trow, drow, uf, rank, ncl, sh);
+    if (y0 == -2)
+        return;  // another CTA's range holds u*S
     if (tid == 0) {
-        s_hit = INT_MAX;
-        s_last = -1;
-    }
-    if (lane == 31)
-        s_excl[warp] = incl;
-    __syncthreads();
-    ff wbase = base;
-    for (int q = 0; q < warp; ++q)
-        wbase = ff_add(wbase, s_excl[q]);
-    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
-    if (!past && ff_le(lo, target) && ff_gt(hi, target))
-        atomicMin(&s_hit, tid);
-    __syncthreads();
-    // the piece walk repeats the piece sum's additions, so it meets the same
-    // running sums; rem may round up to the piece total: then the piece's
-    // last element with weight > 0
-    constexpr int E = Elem<T>::kPerVec;
-    const int nv = (len + E - 1) / E;
-    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
-    if (s_hit == tid) {
-        const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
-        s_last = piece_find<T>(d, tb, db, len, v0, v1, rem);
-    } else if (s_hit == INT_MAX) {  // past the end after rounding: the last element with mass
-        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
-        if (lp >= 0)
-            atomicMax(&s_last, lp);
-    }
-    __syncthreads();
-    if (tid == 0) {
-        const int res = s_last;
-        int y = res >= 0 ? c0 + res : -1;
+        int y = y0;
         if (y < 0)
             set_status(p.status, ST_NONFINITE);
         if (timeout || s_expired) {  // a copy gave up: the data may be stale
@@ -803,6 +847,258 @@ __global__ void __launch_bounds__(kFinishThreads) confidence_kernel(const ConfPa
             conf = __int_as_float(0x7fc00000);
         }
         p.out_conf[r] = conf;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// drafted tokens and acceptance statistics
+// ---------------------------------------------------------------------------
+
+// T > 0, one kernel, one read of each row: one cluster per padded draft row
+// r = i*Kmax + j.  Each CTA stages its range of the row in shared memory
+// (the same ranges and slices as the final draw of a verification) and takes
+// its maximum; the maxima are exchanged through distributed shared memory,
+// and with m known every CTA weighs its range, still in shared memory, by
+// the cluster draw: x = the inverse CDF of q at u[r] over the unnormalised
+// weights 2^(x c - fl(m c)), q(x) = w(x) / S.  Rows past kmax[i] give -1 and
+// 0 and launch no copy.
+template <typename T>
+__global__ void __launch_bounds__(kSampleThreads, 3) draft_sample_kernel(const FinishParams p)
+{
+    extern __shared__ __align__(128) unsigned char dsm[];
+    T *tb = reinterpret_cast<T *>(dsm);
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ float piece[kSampleThreads];
+    __shared__ ff wred[kSampleWarps];
+    __shared__ ff slice_tot[kMaxSlices];
+    __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
+    __shared__ float cl_max[kCluster];               // likewise
+    __shared__ float mred[kSampleWarps];
+    __shared__ ff s_excl[kSampleWarps];
+    __shared__ int s_hit, s_last, s_cs, s_past, s_redo, s_expired;
+    __shared__ ff s_base, s_target, s_S;
+
+    constexpr int E = Elem<T>::kPerVec;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    const int ncl = p.ncl;
+    const int64_t r = blockIdx.x / ncl;
+    const int i = (int)(r / p.Kmax), j = (int)(r - (int64_t)i * p.Kmax);
+    const int km = __ldg(p.kmax + i);
+    const bool bad_k = km < 0 || km > p.Kmax;
+    if (bad_k || j >= km) {  // the same in every CTA of the cluster: no barrier yet
+        if (rank == 0 && tid == 0) {
+            p.out_tokens[r] = -1;
+            p.out_conf[r] = bad_k ? __int_as_float(0x7fc00000) : 0.f;
+            if (bad_k)
+                set_status(p.status, ST_INVALID);
+        }
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        s_expired = 0;
+    }
+    cluster_arrive_relaxed();  // (0) this CTA has started
+    const float uf = __ldg(p.u_final + r);
+    const T *row = reinterpret_cast<const T *>(p.target) + r * p.V;
+    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
+    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+
+    // ---- this range's maximum, slices in reverse so that slice 0 stays staged
+    float mx = -INFINITY;
+    uint32_t phase = 0;
+    __syncthreads();  // the barrier's initialisation is visible
+    for (int sl = nsl - 1; sl >= 0; --sl) {
+        const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+        if (sl != nsl - 1)
+            __syncthreads();  // every thread is done with the previous slice
+        if (p.tma) {
+            if (tid == 0) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
+                mbar_arrive_expect_tx(&bar, bytes);
+                bulk_g2s(tb, row + c0, bytes, &bar);
+            }
+            if (!mbar_wait_bounded(&bar, phase)) {
+                set_status(p.status, ST_TIMEOUT);
+                s_expired = 1;
+                mbar_wait_bounded(&bar, phase);  // the copy in flight, once more
+            }
+            phase ^= 1u;
+        } else {
+            for (int k = tid; k < len; k += kSampleThreads)
+                tb[k] = row[c0 + k];
+            __syncthreads();
+        }
+        const int nv = (len + E - 1) / E;
+        const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
+        for (int v = tid; v < nv; v += kSampleThreads) {
+            float f[E];
+            Elem<T>::unpack(tv[v], f);
+#pragma unroll
+            for (int h = 0; h < E; ++h)
+                if (v * E + h < len)
+                    mx = max_nan(mx, f[h]);
+        }
+    }
+    mx = warp_max_nan(mx);
+    if (lane == 0)
+        mred[warp] = mx;
+    __syncthreads();
+    cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
+    if (warp == 0) {
+        float v = lane < kSampleWarps ? mred[lane] : -INFINITY;
+        v = warp_max_nan(v);
+        if (lane < ncl) {
+            uint32_t remote;
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
+                         : "=r"(remote)
+                         : "r"(smem_u32(&cl_max[rank])), "r"((uint32_t)lane));
+            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+        }
+    }
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (1) every CTA holds every range's maximum
+    float m = -INFINITY;
+    for (int q = 0; q < ncl; ++q)
+        m = max_nan(m, cl_max[q]);
+    if (!(m > -INFINITY && m < INFINITY)) {  // NaN, +inf or a fully masked row: the same
+        if (rank == 0 && tid == 0) {          // in every CTA, after the last exchange
+            set_status(p.status, ST_NONFINITE);
+            p.out_tokens[r] = -1;
+            p.out_conf[r] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+    DrawCtx d;
+    d.resid = false;
+    d.c = p.c;
+    d.mct = m * p.c;
+    d.sc_t = 0.f;
+    d.mcd = 0.f;
+    d.sc_d = 0.f;
+    const DrawShared<T> sh{tb,      nullptr, &bar,   piece,   wred,    slice_tot, s_excl,
+                           cl_sum,  &s_hit,  &s_last, &s_cs, &s_past, &s_redo,   &s_expired,
+                           &s_base, &s_target, &s_S};
+    const int y0 =
+        draw_token<T>(p, d, row, nullptr, uf, rank, ncl, sh, nsl > 0 ? 0 : -1, phase);
+    if (y0 == -2)
+        return;  // another CTA's range holds u*S
+    if (tid == 0) {
+        int y = y0;
+        float conf = __int_as_float(0x7fc00000);
+        if (y < 0) {
+            set_status(p.status, ST_NONFINITE);
+        } else {
+            const float w = ex2_approx(fmaf(Elem<T>::ld_global(row, y), d.c, -d.mct));
+            conf = __fdiv_rn(w, __fadd_rn(s_S.hi, s_S.lo));
+        }
+        if (s_expired || (read_status(p.status) & ST_TIMEOUT)) {  // a copy gave up
+            y = -1;
+            conf = __int_as_float(0x7fc00000);
+        }
+        p.out_tokens[r] = y;
+        p.out_conf[r] = conf;
+    }
+}
+
+// T = 0: one warp per padded draft row takes the row's lowest-index maximum.
+template <typename T>
+__global__ void __launch_bounds__(kFinishThreads) draft_greedy_kernel(const FinishParams p)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t r = (int64_t)blockIdx.x * kFinishWarps + warp;
+    const int64_t nrow = (int64_t)p.B * p.Kmax;
+    int km = 0;
+    if (r < nrow)
+        km = __ldg(p.kmax + r / p.Kmax);
+    pdl_wait();
+    if (r >= nrow)
+        return;
+    const int j = (int)(r % p.Kmax);
+    const bool bad_k = km < 0 || km > p.Kmax;
+    int y = -1;
+    float conf = 0.f;
+    uint32_t err = bad_k ? ST_INVALID : 0u;
+    if (!bad_k && j < km) {
+        const int gi = merge_argmax_row(p.part, p.g, r);
+        if (gi < 0)
+            err = ST_NONFINITE;
+        else {
+            y = gi;
+            conf = 1.f;
+        }
+    }
+    if (lane == 0) {
+        if (err) {
+            set_status(p.status, err);
+            conf = __int_as_float(0x7fc00000);
+        }
+        p.out_tokens[r] = y;
+        p.out_conf[r] = conf;
+    }
+}
+
+// Acceptance statistics of one verification call, one CTA: per position j
+// the requests that tested it (K_i > j, a_i >= j) and accepted it (a_i > j),
+// and the mean accepted length over requests with a_i >= 0.  Integer counts,
+// so the result does not depend on the order of the atomic adds.
+constexpr int kStatsThreads = 1024;
+
+struct StatsParams {
+    const int32_t *accept_len;
+    const int32_t *cu;
+    int B, Kmax;
+    int32_t *out_reached;
+    int32_t *out_accepted;
+    float *out_mean;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kStatsThreads) acceptance_stats_kernel(const StatsParams p)
+{
+    __shared__ int reached[kMaxDraft], accepted[kMaxDraft];
+    __shared__ unsigned long long total;
+    __shared__ int n, bad;
+    const int tid = threadIdx.x;
+    if (tid < kMaxDraft)
+        reached[tid] = accepted[tid] = 0;
+    if (tid == 0) {
+        total = 0ull;
+        n = 0;
+        bad = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < p.B; i += kStatsThreads) {
+        const int a = __ldg(p.accept_len + i);
+        const int k = __ldg(p.cu + i + 1) - __ldg(p.cu + i);
+        if (a < 0)
+            continue;  // a poisoned request
+        if (a > k || k > p.Kmax || k < 0) {
+            bad = 1;
+            continue;
+        }
+        atomicAdd(&total, (unsigned long long)a);
+        atomicAdd(&n, 1);
+        for (int j = 0; j < k; ++j) {
+            if (a >= j)
+                atomicAdd(&reached[j], 1);
+            if (a > j)
+                atomicAdd(&accepted[j], 1);
+        }
+    }
+    __syncthreads();
+    if (tid < p.Kmax) {
+        p.out_reached[tid] = bad ? -1 : reached[tid];
+        p.out_accepted[tid] = bad ? -1 : accepted[tid];
+    }
+    if (tid == 0) {
+        if (bad)
+            set_status(p.status, ST_INVALID);
+        *p.out_mean = bad ? __int_as_float(0x7fc00000)
+                          : (n > 0 ? (float)((double)total / (double)n) : 0.f);
     }
 }
 

@@ -85,4 +85,35 @@ struct ConfArgs {
 // confidence kernel (2 launches).
 cudaError_t launch_confidence(const ConfArgs &a, cudaStream_t stream, Tracer &tr);
 
+struct DraftArgs {
+    const void *draft;  // [B*Kmax][V]
+    int dtype;
+    const int32_t *kmax;
+    int B;
+    int Kmax;
+    int V;
+    double temperature;  // 0 = greedy
+    const float *u;      // [B*Kmax] (T > 0)
+    int32_t *out_tokens;
+    float *out_conf;
+    void *ws;
+};
+
+// Enqueue the streaming pass over the B*Kmax draft rows and the drafting
+// kernel (a cluster draw per row, or a warp argmax per row at T = 0).
+cudaError_t launch_draft(const DraftArgs &a, cudaStream_t stream, Tracer &tr);
+
+struct StatsArgs {
+    const int32_t *accept_len;
+    const int32_t *cu;
+    int B;
+    int Kmax;
+    int32_t *out_reached;
+    int32_t *out_accepted;
+    float *out_mean;
+    void *ws;
+};
+
+cudaError_t launch_acceptance_stats(const StatsArgs &a, cudaStream_t stream, Tracer &tr);
+
 }  // namespace sv

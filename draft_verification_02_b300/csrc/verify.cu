@@ -132,6 +132,40 @@ static cudaError_t prepare_finish_sample()
     return once;
 }
 
+template <typename T>
+static cudaError_t prepare_draft_sample()
+{
+    static cudaError_t once = [] {
+        cudaError_t e = cudaFuncSetAttribute(draft_sample_kernel<T>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kStageRowBytes);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(draft_sample_kernel<T>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        return e;
+    }();
+    return once;
+}
+
+// Geometry of a cluster draw over V entries, one cluster per draw: ncl
+// ranges of R entries, weighed in slices.  16 CTAs per draw while the
+// clusters fit the GPU at one CTA per SM (larger clusters are harder to
+// place), else 8.  False when the vocabulary exceeds the slice table.
+static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
+{
+    const int gran = 16 / e;
+    const int ncl = draws * kCluster <= (int64_t)sm_count() ? kCluster : kCluster / 2;
+    fp.ncl = ncl;
+    const int R = (int)((((int64_t)V + ncl - 1) / ncl + gran - 1) / gran * gran);
+    const int slice = std::min(R, kStageRowBytes / e);
+    const int nv = (slice * e + 15) / 16;
+    fp.R = R;
+    fp.slice = slice;
+    fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
+    fp.stage_smem = (int)align_up((size_t)slice * e, 128);
+    return (R + slice - 1) / slice <= kMaxSlices;
+}
+
 template <typename T, bool GREEDY>
 static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
 {
@@ -181,22 +215,8 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
     fp.draft_stride = a.draft_stride;
     fp.g = g;
-    {  // final-draw geometry: ncl ranges of R entries, weighed in slices.  16
-        // CTAs per request while the clusters fit the GPU at one CTA per SM
-        // (larger clusters are harder to place), else 8.
-        const int gran = 16 / e;
-        const int ncl = (int64_t)a.B * kCluster <= (int64_t)sm_count() ? kCluster : kCluster / 2;
-        fp.ncl = ncl;
-        const int R = (int)((((int64_t)a.V + ncl - 1) / ncl + gran - 1) / gran * gran);
-        const int slice = std::min(R, kStageRowBytes / e);
-        const int nv = (slice * e + 15) / 16;
-        fp.R = R;
-        fp.slice = slice;
-        fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
-        fp.stage_smem = (int)align_up((size_t)slice * e, 128);
-        if ((R + slice - 1) / slice > kMaxSlices)
-            return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
-    }
+    if (!GREEDY && !draw_geometry(fp, a.B, a.V, e))
+        return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
     fp.tma = tma;
     fp.c = sp.c;
     fp.status = sp.status;
@@ -246,47 +266,34 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     return cudaSuccess;
 }
 
+// The streaming pass over the B*Kmax padded drafter rows (every row is read):
+// the per-row partials the drafting kernels merge.
 template <typename T, bool GREEDY>
-static cudaError_t launch_conf_typed(const ConfArgs &a, cudaStream_t s, Tracer &tr)
+static cudaError_t launch_draft_pass(const void *draft, int B, int Kmax, int V, double temperature,
+                                     void *ws_ptr, cudaStream_t s, Tracer &tr, StreamParams &sp)
 {
     const int e = (int)sizeof(T);
-    const int64_t rows = (int64_t)a.B * a.Kmax;
-    const WsLayout L = ws_layout(a.B, (int64_t)a.B * (a.Kmax + 1), a.V);
-    unsigned char *ws = static_cast<unsigned char *>(a.ws);
+    const int64_t rows = (int64_t)B * Kmax;
+    const WsLayout L = ws_layout(B, (int64_t)B * (Kmax + 1), V);
+    unsigned char *ws = static_cast<unsigned char *>(ws_ptr);
     const int ctas_max = sm_count() * SV_STREAM_CTAS_PER_SM;
-    const Geometry g = plan(rows, rows, a.V, e, std::min(kMaxWorkers, ctas_max * kStreamWarps));
-    const bool tma = ((int64_t)a.V * e) % 16 == 0 && reinterpret_cast<uintptr_t>(a.draft) % 16 == 0;
-    const double c = GREEDY ? 0.0 : 1.4426950408889634074 / a.temperature;  // log2(e) / T
-
-    StreamParams sp{};
-    sp.target = a.draft;  // every draft row is read as a row of the pass
+    const Geometry g = plan(rows, rows, V, e, std::min(kMaxWorkers, ctas_max * kStreamWarps));
+    const double c = GREEDY ? 0.0 : 1.4426950408889634074 / temperature;  // log2(e) / T
+    sp = StreamParams{};
+    sp.target = draft;  // every draft row is read as a row of the pass
     sp.draft = nullptr;
-    sp.cu = nullptr;      // no offsets: every row is real
-    sp.B = a.B;
-    sp.V = a.V;
+    sp.cu = nullptr;    // no offsets: every row is real
+    sp.B = B;
+    sp.V = V;
     sp.draft_slots = 0;
     sp.draft_stride = 0;
     sp.g = g;
-    sp.tma = tma;
+    sp.tma = ((int64_t)V * e) % 16 == 0 && reinterpret_cast<uintptr_t>(draft) % 16 == 0;
     sp.piece_smem = (int)align_up((size_t)g.Q * e, 128);
     sp.c = (float)c;
     sp.status = reinterpret_cast<uint32_t *>(ws + L.status);
     sp.cu_flag = sp.status + 1;
     sp.part = reinterpret_cast<Partial *>(ws + L.part1);
-
-    ConfParams cp{};
-    cp.draft = a.draft;
-    cp.tokens = a.tokens;
-    cp.kmax = a.kmax;
-    cp.B = a.B;
-    cp.Kmax = a.Kmax;
-    cp.V = a.V;
-    cp.g = g;
-    cp.c = sp.c;
-    cp.out_conf = a.out_conf;
-    cp.status = sp.status;
-    cp.part = sp.part;
-
     cudaError_t err = prepare_stream<T, GREEDY>();
     if (err != cudaSuccess)
         return err;
@@ -297,15 +304,56 @@ static cudaError_t launch_conf_typed(const ConfArgs &a, cudaStream_t s, Tracer &
     if ((err = cudaGetLastError()) != cudaSuccess)
         return err;
     tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+static cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     cudaLaunchAttribute (&attr)[2], int cluster)
+{
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)((rows + kFinishWarps - 1) / kFinishWarps));
-    cfg.blockDim = dim3(kFinishThreads);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    return cfg;
+}
+
+template <typename T, bool GREEDY>
+static cudaError_t launch_conf_typed(const ConfArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const int64_t rows = (int64_t)a.B * a.Kmax;
+    StreamParams sp;
+    cudaError_t err = launch_draft_pass<T, GREEDY>(a.draft, a.B, a.Kmax, a.V, a.temperature, a.ws,
+                                                   s, tr, sp);
+    if (err != cudaSuccess)
+        return err;
+    ConfParams cp{};
+    cp.draft = a.draft;
+    cp.tokens = a.tokens;
+    cp.kmax = a.kmax;
+    cp.B = a.B;
+    cp.Kmax = a.Kmax;
+    cp.V = a.V;
+    cp.g = sp.g;
+    cp.c = sp.c;
+    cp.out_conf = a.out_conf;
+    cp.status = sp.status;
+    cp.part = sp.part;
+    cudaLaunchAttribute attr[2];
+    const cudaLaunchConfig_t cfg =
+        pdl_config(dim3((unsigned)((rows + kFinishWarps - 1) / kFinishWarps)), dim3(kFinishThreads),
+                   0, s, attr, 1);
     if ((err = cudaLaunchKernelEx(&cfg, confidence_kernel<T, GREEDY>, cp)) != cudaSuccess)
         return err;
     tr.after_kernel(s);
@@ -320,6 +368,88 @@ cudaError_t launch_confidence(const ConfArgs &a, cudaStream_t s, Tracer &tr)
                       : launch_conf_typed<float, false>(a, s, tr);
     return greedy ? launch_conf_typed<uint16_t, true>(a, s, tr)
                   : launch_conf_typed<uint16_t, false>(a, s, tr);
+}
+
+// T > 0: one kernel (draft_sample_kernel reads each row once and draws from
+// it); T = 0: the streaming pass over the rows and a warp argmax merge per row.
+template <typename T, bool GREEDY>
+static cudaError_t launch_draft_typed(const DraftArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const int e = (int)sizeof(T);
+    const int64_t rows = (int64_t)a.B * a.Kmax;
+    FinishParams fp{};
+    fp.target = a.draft;
+    fp.u_final = a.u;
+    fp.out_tokens = a.out_tokens;
+    fp.out_conf = a.out_conf;
+    fp.kmax = a.kmax;
+    fp.Kmax = a.Kmax;
+    fp.B = a.B;
+    fp.V = a.V;
+    const WsLayout L = ws_layout(a.B, (int64_t)a.B * (a.Kmax + 1), a.V);
+    fp.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
+    fp.cu_flag = fp.status + 1;
+    cudaLaunchAttribute attr[2];
+    cudaError_t err;
+    if (GREEDY) {
+        StreamParams sp;
+        if ((err = launch_draft_pass<T, true>(a.draft, a.B, a.Kmax, a.V, 0.0, a.ws, s, tr, sp)) !=
+            cudaSuccess)
+            return err;
+        fp.g = sp.g;
+        fp.part = sp.part;
+        const cudaLaunchConfig_t cfg = pdl_config(
+            dim3((unsigned)((rows + kFinishWarps - 1) / kFinishWarps)), dim3(kFinishThreads), 0, s,
+            attr, 1);
+        err = cudaLaunchKernelEx(&cfg, draft_greedy_kernel<T>, fp);
+    } else {
+        if (!draw_geometry(fp, rows, a.V, e))
+            return cudaErrorInvalidValue;
+        if ((err = prepare_draft_sample<T>()) != cudaSuccess)
+            return err;
+        fp.tma = ((int64_t)a.V * e) % 16 == 0 && reinterpret_cast<uintptr_t>(a.draft) % 16 == 0;
+        fp.c = (float)(1.4426950408889634074 / a.temperature);  // log2(e) / T
+        cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(rows * fp.ncl)), dim3(kSampleThreads),
+                                            (size_t)fp.stage_smem, s, attr, fp.ncl);
+        cfg.attrs = attr + 1;  // a cluster launch with no programmatic predecessor
+        cfg.numAttrs = 1;
+        tr.begin(s);
+        err = cudaLaunchKernelEx(&cfg, draft_sample_kernel<T>, fp);
+    }
+    if (err != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+cudaError_t launch_draft(const DraftArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const bool greedy = a.temperature == 0.0;
+    if (a.dtype == 0)
+        return greedy ? launch_draft_typed<float, true>(a, s, tr)
+                      : launch_draft_typed<float, false>(a, s, tr);
+    return greedy ? launch_draft_typed<uint16_t, true>(a, s, tr)
+                  : launch_draft_typed<uint16_t, false>(a, s, tr);
+}
+
+cudaError_t launch_acceptance_stats(const StatsArgs &a, cudaStream_t s, Tracer &tr)
+{
+    StatsParams sp{};
+    sp.accept_len = a.accept_len;
+    sp.cu = a.cu;
+    sp.B = a.B;
+    sp.Kmax = a.Kmax;
+    sp.out_reached = a.out_reached;
+    sp.out_accepted = a.out_accepted;
+    sp.out_mean = a.out_mean;
+    sp.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) +
+                                             ws_layout(0, 0, 0).status);
+    tr.begin(s);
+    acceptance_stats_kernel<<<1, kStatsThreads, 0, s>>>(sp);
+    if (cudaError_t err = cudaGetLastError(); err != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
+    return cudaSuccess;
 }
 
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t s, Tracer &tr)

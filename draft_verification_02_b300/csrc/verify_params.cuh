@@ -64,6 +64,9 @@ struct FinishParams {
     int pv;          // 16-byte vectors per thread piece of a slice (odd)
     int stage_smem;  // bytes per staged row slice (multiple of 128)
     int tma;         // rows 16-byte aligned: TMA bulk copies
+    const int32_t *kmax;  // drafting only: rows per request that hold a draft
+    int Kmax;             // drafting only: rows per request (padded)
+    float *out_conf;      // drafting only: q(x) of each drawn token
     float c;
     uint32_t *status;
     const uint32_t *cu_flag;

@@ -31,7 +31,8 @@ SPEC_DCUT_MAX_CANDIDATES = 8192
 EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
            "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
-           "spec_verify_sample_static", "dcut_allocate_cost", "spec_draft_confidence")
+           "spec_verify_sample_static", "dcut_allocate_cost", "spec_draft_confidence",
+           "spec_draft_sample", "spec_acceptance_stats")
 SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -67,6 +68,10 @@ def _load():
     lib.dcut_allocate_cost.restype = INT
     lib.spec_draft_confidence.argtypes = [P, INT, P, P, I32, I32, I32, F32, P, P, SZ, P]
     lib.spec_draft_confidence.restype = INT
+    lib.spec_draft_sample.argtypes = [P, INT, P, I32, I32, I32, F32, P, P, P, P, SZ, P]
+    lib.spec_draft_sample.restype = INT
+    lib.spec_acceptance_stats.argtypes = [P, P, I32, I32, P, P, P, P, SZ, P]
+    lib.spec_acceptance_stats.restype = INT
     lib.dcut_allocate.restype = INT
     lib.spec_get_device_status.argtypes = [P, P]
     lib.spec_get_device_status.restype = INT
@@ -249,6 +254,33 @@ def spec_draft_confidence(draft_logits, draft_tokens, kmax, B: int, Kmax: int, V
         _dev(draft_tokens, "draft_tokens", torch.int32, n),
         _dev(kmax, "kmax", torch.int32, B), B, Kmax, V, float(temperature),
         _dev(out_conf, "out_conf", torch.float32, n),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_draft_sample(draft_logits, kmax, B: int, Kmax: int, V: int, temperature: float, u_draft,
+                      out_tokens, out_conf, workspace, stream=None) -> int:
+    n = B * Kmax
+    if n == 0:
+        return SPEC_OK
+    return LIB.spec_draft_sample(
+        _dev(draft_logits, "draft_logits", min_numel=n * V), dtype_code(draft_logits),
+        _dev(kmax, "kmax", torch.int32, B), B, Kmax, V, float(temperature),
+        _dev(u_draft, "u_draft", torch.float32, n, allow_none=temperature == 0),
+        _dev(out_tokens, "out_tokens", torch.int32, n),
+        _dev(out_conf, "out_conf", torch.float32, n),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_acceptance_stats(accept_len, cu_draft, B: int, Kmax: int, out_reached, out_accepted,
+                          out_mean, workspace, stream=None) -> int:
+    return LIB.spec_acceptance_stats(
+        _dev(accept_len, "accept_len", torch.int32, B, allow_none=B == 0),
+        _dev(cu_draft, "cu_draft", torch.int32, B + 1, allow_none=B == 0), B, Kmax,
+        _dev(out_reached, "out_reached", torch.int32, Kmax, allow_none=Kmax == 0),
+        _dev(out_accepted, "out_accepted", torch.int32, Kmax, allow_none=Kmax == 0),
+        _dev(out_mean, "out_mean", torch.float32, 1),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
 

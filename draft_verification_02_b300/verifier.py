@@ -73,5 +73,38 @@ class Verifier:
         out["status"] = st
         return out
 
+    def draft(self, draft_logits: torch.Tensor, kmax: torch.Tensor, Kmax: int,
+              temperature: float, u_draft: Optional[torch.Tensor] = None, stream=None,
+              check: bool = True) -> dict:
+        """Drafted tokens and their q(x) from [B*Kmax][V] drafter logits (the
+        workspace must hold B*(Kmax+1) target rows)."""
+        B = kmax.numel()
+        n = B * Kmax
+        V = draft_logits.shape[-1]
+        dev = self.device
+        out = {"tokens": torch.full((max(n, 1),), -7, dtype=torch.int32, device=dev),
+               "conf": torch.full((max(n, 1),), float("nan"), dtype=torch.float32, device=dev)}
+        st = sv.spec_draft_sample(draft_logits, kmax, B, Kmax, V, temperature, u_draft,
+                                  out["tokens"], out["conf"], self.workspace, stream)
+        if check:
+            sv.check(st, "draft_sample")
+        out["status"] = st
+        return out
+
+    def acceptance_stats(self, accept_len: torch.Tensor, cu_draft: torch.Tensor, Kmax: int,
+                         stream=None, check: bool = True) -> dict:
+        """Per-position reached/accepted counts and the mean accepted length."""
+        B = accept_len.numel()
+        dev = self.device
+        out = {"reached": torch.full((max(Kmax, 1),), -7, dtype=torch.int32, device=dev),
+               "accepted": torch.full((max(Kmax, 1),), -7, dtype=torch.int32, device=dev),
+               "mean": torch.full((1,), float("nan"), dtype=torch.float32, device=dev)}
+        st = sv.spec_acceptance_stats(accept_len, cu_draft, B, Kmax, out["reached"],
+                                      out["accepted"], out["mean"], self.workspace, stream)
+        if check:
+            sv.check(st, "acceptance_stats")
+        out["status"] = st
+        return out
+
     def device_status(self, stream=None) -> int:
         return sv.spec_get_device_status(self.workspace, stream)

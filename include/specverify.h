@@ -226,6 +226,61 @@ int spec_draft_confidence(const void *draft_logits, int dtype, const int32_t *dr
                           spec_stream_t stream);
 
 /*
+ * The drafter's own step: draw the drafted tokens from its logits (the step
+ * before verification: a lightweight drafter proposes the candidate tokens
+ * that the target then checks, "Tencent Hunyuan Turns Speculative Decoding
+ * Into a Full Open-Source Stack", "What problem does it solve").  For row
+ * r = i*Kmax + j with j < kmax[i], q = softmax(draft row r / T) and
+ *   out_tokens[r] = the smallest v with C(v) > u_draft[r] * S   (T > 0)
+ *   out_tokens[r] = the row's lowest-index maximum                (T == 0)
+ * where C is the running sum of the unnormalised weights 2^((x - m) log2(e)/T)
+ * over the vocabulary and S its total (the same inverse-CDF reading as the
+ * final draw of spec_verify_sample); out_conf[r] = q(out_tokens[r]) (1 at
+ * T == 0), which is the input of dcut_allocate for a drafter that samples.
+ * Rows j >= kmax[i] give -1 and 0.
+ *
+ *   draft_logits  [B*Kmax][V] f32 or bf16, padded (every row is read)
+ *   kmax          int32 [B], u_draft float [B*Kmax] in [0, 1) (T > 0; may be
+ *                 NULL at T == 0), out_tokens int32 [B*Kmax], out_conf float
+ *                 [B*Kmax]; all device pointers
+ * A workspace of spec_workspace_size(B, B * (Kmax + 1), V) bytes suffices.
+ * A row with NaN / +inf / no finite logit gives -1 and NaN and sets
+ * SPEC_ERR_NONFINITE on the device; kmax outside [0, Kmax] sets
+ * SPEC_ERR_INVALID_ARG there.  A draw near a CDF boundary may differ from an
+ * exact-arithmetic draw by one token (fp32 weights; the float-float running
+ * sums keep the error near 1e-7 of S).  T > 0: one kernel launch, one
+ * cluster of 8 or 16 CTAs per row that reads the row once (each CTA keeps
+ * its share in shared memory between the maximum and the draw).  T == 0: two
+ * launches, the streaming pass over the B*Kmax rows and a per-row argmax
+ * merge, its programmatic dependent.
+ */
+int spec_draft_sample(const void *draft_logits, int dtype, const int32_t *kmax, int32_t B,
+                      int32_t Kmax, int32_t V, float temperature, const float *u_draft,
+                      int32_t *out_tokens, float *out_conf, void *workspace, size_t ws_bytes,
+                      spec_stream_t stream);
+
+/*
+ * The acceptance statistics the pages report per drafter: mean accepted
+ * length and acceptance by draft position ("Tencent Hunyuan Turns
+ * Speculative Decoding Into a Full Open-Source Stack", "Five angles worth a
+ * closer look", item 4: read from the serving engine during training; the
+ * French/Russian page's table of acceptance rates by position at T = 0).
+ * From one verification call's outputs (accept_len = out_accept_len, cu_draft
+ * its offsets), over the requests with accept_len[i] >= 0:
+ *   out_reached[j]  = #{ i : K_i > j and a_i >= j }   position j was tested
+ *   out_accepted[j] = #{ i : a_i > j }                 and accepted
+ *   *out_mean       = sum a_i / #requests (0 with no request), fp32
+ * for j < Kmax; the per-position rate is accepted[j] / reached[j].  A request
+ * with a_i > K_i or K_i > Kmax sets SPEC_ERR_INVALID_ARG on the device and
+ * every output to -1 (mean NaN).  All pointers are device pointers; only the
+ * workspace's status word is used (any workspace from spec_workspace_size
+ * will do).  One kernel launch (one CTA); B <= SPEC_MAX_BATCH.
+ */
+int spec_acceptance_stats(const int32_t *accept_len, const int32_t *cu_draft, int32_t B,
+                          int32_t Kmax, int32_t *out_reached, int32_t *out_accepted,
+                          float *out_mean, void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
  * spec_verify_sample without a workspace, for callers that cannot allocate
  * device memory: an engine whose memory pool already owns all of HBM (for
  * its KV cache), a plugin whose host runtime forbids allocations outside its
