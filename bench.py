@@ -195,6 +195,20 @@ def read_stream_reference(nbytes: int, device, reps: int = 20) -> float:
     return 2 * n / sec / 1e9
 
 
+def replay_percentiles(events, steps_per_replay):
+    """Median, p10 and p90 of the per-step time (ms) over the timed graph
+    replays (events recorded between replays, none inside a graph)."""
+    ms = sorted(events[q].elapsed_time(events[q + 1]) / steps_per_replay
+                for q in range(len(events) - 1))
+    if not ms:
+        return None
+
+    def pct(x):
+        return ms[min(len(ms) - 1, int(round(x * (len(ms) - 1))))]
+    return {"replays": len(ms), "steps_per_replay": steps_per_replay, "median": pct(0.5),
+            "p10": pct(0.1), "p90": pct(0.9)}
+
+
 def workload_desc(w, T):
     return f"{W.describe(w)}, T={T}"
 
@@ -448,15 +462,19 @@ def run_ours(args, dist):
     dist.barrier()
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
+    rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(n_rep):
+        rep_ev[0].record(stream)
+        for q in range(n_rep):
             g_main.replay()
+            rep_ev[q + 1].record(stream)
         if g_rem is not None:
             g_rem.replay()
         end.record(stream)
     torch.cuda.synchronize(device)
     t_wall1 = time.time()
+    step_dist = replay_percentiles(rep_ev, G)
     dist.barrier()
     # per-kernel durations: one traced replay of G steps right after
     t0e = torch.cuda.Event(enable_timing=True)
@@ -489,18 +507,17 @@ def run_ours(args, dist):
     step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
     achieved = alg_bytes / (rows_mean / 1e6) / 1e9
 
-    # acceptance statistics of the last outputs (the quantities the pages report)
-    acc = {}
-    if T >= 0:
-        a = first["out"]["accept_len"].cpu().numpy().astype(np.int64)
-        k_arr = batch0.k.cpu().numpy()
-        rates = []
-        for j in range(int(k_arr.max()) if k_arr.size else 0):
-            elig = k_arr > j
-            reach = (a >= j) & elig
-            if reach.sum():
-                rates.append(round(float(((a > j) & reach).sum() / reach.sum()), 4))
-        acc = {"mean_accepted_len": round(float(a.mean()), 4), "per_position_rate": rates}
+    # acceptance statistics of input set 0's last outputs (the quantities the
+    # pages report), by the library's own kernel, outside the timed region
+    kmax_stats = w.kmax or w.k or w.k_range[1]
+    cu0 = first["dcut_out"]["cu"] if is_dcut else batch0.cu_draft
+    st = v.acceptance_stats(first["out"]["accept_len"], cu0, kmax_stats)
+    reached = st["reached"][:kmax_stats].cpu().numpy()
+    accepted = st["accepted"][:kmax_stats].cpu().numpy()
+    acc = {"mean_accepted_len": round(float(st["mean"].item()), 4),
+           "per_position_rate": [round(float(a_) / float(r_), 4)
+                                 for a_, r_ in zip(accepted, reached) if r_ > 0],
+           "per_position_reached": reached.tolist()}
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -511,15 +528,20 @@ def run_ours(args, dist):
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        rate, nreq, el = oracle_sample_rate(host_arrays(batch0), args.cpu_seconds, threads)
+        h0 = host_arrays(batch0)
+        rate, nreq, el = oracle_sample_rate(h0, args.cpu_seconds, threads)
+        rate1, nreq1, el1 = oracle_sample_rate(h0, args.cpu_seconds / 3, 1)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{nreq} whole requests of input set 0 ({workload_desc(w, T)}), "
-                         f"one oracle call per request on {threads} host threads, {el:.1f} s"}
+                         f"one oracle call per request on {threads} host threads, {el:.1f} s",
+               "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                                 "sample": f"{nreq1} whole requests, {el1:.1f} s"}}
 
     traffic = recorded_traffic(args.workload, "stream_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_dist": step_dist,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": workload_desc(w, T), "B": w.B, "V": w.V, "logits_dtype": w.dtype,
@@ -753,15 +775,19 @@ def run_draft(args, dist):
     dist.barrier()
     torch.cuda.synchronize(device)
     t_wall0 = time.time()
+    rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
     with torch.cuda.stream(stream):
         start.record(stream)
-        for _ in range(n_rep):
+        rep_ev[0].record(stream)
+        for q in range(n_rep):
             g_main.replay()
+            rep_ev[q + 1].record(stream)
         if g_rem is not None:
             g_rem.replay()
         end.record(stream)
     torch.cuda.synchronize(device)
     t_wall1 = time.time()
+    step_dist = replay_percentiles(rep_ev, G)
     dist.barrier()
     with torch.cuda.stream(stream):
         g_traced.replay()
@@ -823,15 +849,19 @@ def run_draft(args, dist):
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        rate, n, el = oracle_draft_rate(host_draft(first["draft"]), host_draft(first["u"]), T,
-                                        args.cpu_seconds, threads)
+        hd, hu = host_draft(first["draft"]), host_draft(first["u"])
+        rate, n, el = oracle_draft_rate(hd, hu, T, args.cpu_seconds, threads)
+        rate1, n1, el1 = oracle_draft_rate(hd, hu, T, args.cpu_seconds / 3, 1)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n} drafter rows of input set 0 ({workload_desc(w, T)}), drawn by "
-                         f"the oracle 4 rows per call on {threads} host threads, {el:.1f} s"}
+                         f"the oracle 4 rows per call on {threads} host threads, {el:.1f} s",
+               "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
+                                 "sample": f"{n1} drafter rows, {el1:.1f} s"}}
 
     line = {
         "metric": DRAFT_METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_dist": step_dist,
+        "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
             "workload": f"drafter step of {workload_desc(w, T)}: {n_rows} rows, Kmax={Kmax}",

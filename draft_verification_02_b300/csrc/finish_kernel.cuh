@@ -227,6 +227,8 @@ __device__ __forceinline__ float draw_w(const DrawCtx &d, float t, float x)
 
 // Sum of the final-draw weights of one thread's contiguous piece (16-byte
 // vectors [v0, v1) of a staged slice of len elements), in index order, fp32.
+// Vectors wholly inside the slice take no per-element bounds test; only the
+// slice's last vector can be partial.
 template <typename T>
 __device__ __forceinline__ float piece_sum(const DrawCtx d, const T *tb, const T *db, int len,
                                            int v0, int v1)
@@ -234,9 +236,29 @@ __device__ __forceinline__ float piece_sum(const DrawCtx d, const T *tb, const T
     constexpr int E = Elem<T>::kPerVec;
     const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
     const uint4 *dv = reinterpret_cast<const uint4 *>(db);
+    const int vfull = min(v1, len / E);
     float acc = 0.f;
+    if (d.resid) {
 #pragma unroll 1
-    for (int v = v0; v < v1; ++v) {
+        for (int v = v0; v < vfull; ++v) {
+            float ft[E], fd[E];
+            Elem<T>::unpack(tv[v], ft);
+            Elem<T>::unpack(dv[v], fd);
+#pragma unroll
+            for (int h = 0; h < E; ++h)
+                acc = __fadd_rn(acc, draw_w(d, ft[h], fd[h]));
+        }
+    } else {
+#pragma unroll 1
+        for (int v = v0; v < vfull; ++v) {
+            float ft[E];
+            Elem<T>::unpack(tv[v], ft);
+#pragma unroll
+            for (int h = 0; h < E; ++h)
+                acc = __fadd_rn(acc, draw_w(d, ft[h], 0.f));
+        }
+    }
+    for (int v = max(v0, vfull); v < v1; ++v) {  // the partial last vector
         float ft[E], fd[E];
         Elem<T>::unpack(tv[v], ft);
         if (d.resid)
@@ -253,7 +275,7 @@ __device__ __forceinline__ float piece_sum(const DrawCtx d, const T *tb, const T
 // The same walk, stopping at the first element whose running sum exceeds
 // rem: its index in the slice, or (none) the last element with weight > 0
 // (-1 if there is none).  The running sums are those of piece_sum, bit for
-// bit.
+// bit (the same additions in the same order).
 template <typename T>
 __device__ __forceinline__ int piece_find(const DrawCtx d, const T *tb, const T *db, int len,
                                           int v0, int v1, float rem)
@@ -932,16 +954,26 @@ __global__ void __launch_bounds__(kSampleThreads, 3) draft_sample_kernel(const F
                 tb[k] = row[c0 + k];
             __syncthreads();
         }
-        const int nv = (len + E - 1) / E;
         const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
-        for (int v = tid; v < nv; v += kSampleThreads) {
-            float f[E];
-            Elem<T>::unpack(tv[v], f);
-#pragma unroll
-            for (int h = 0; h < E; ++h)
-                if (v * E + h < len)
-                    mx = max_nan(mx, f[h]);
+        const int nfull = len / E;  // whole vectors, then the partial tail (plain loads only)
+        if constexpr (sizeof(T) == 2) {
+            uint32_t m2 = 0xff80ff80u;  // -inf, -inf
+#pragma unroll 4
+            for (int v = tid; v < nfull; v += kSampleThreads) {
+                const uint4 x = tv[v];
+                m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(x.x, x.y),
+                                                       max_nan_bf16x2(x.z, x.w)));
+            }
+            mx = max_nan(mx, max_nan(bf16_lo(m2), bf16_hi(m2)));
+        } else {
+#pragma unroll 4
+            for (int v = tid; v < nfull; v += kSampleThreads) {
+                const float4 x = reinterpret_cast<const float4 *>(tb)[v];
+                mx = max_nan(mx, max_nan(max_nan(x.x, x.y), max_nan(x.z, x.w)));
+            }
         }
+        for (int k = nfull * E + tid; k < len; k += kSampleThreads)
+            mx = max_nan(mx, Elem<T>::at(tb, k));
     }
     mx = warp_max_nan(mx);
     if (lane == 0)

@@ -132,13 +132,23 @@ static cudaError_t prepare_finish_sample()
     return once;
 }
 
+// Drafting at T > 0: CTAs per row (0: the verification draw's rule) and the
+// staging buffer of each CTA's range.
+#ifndef SV_DRAFT_NCL
+#define SV_DRAFT_NCL 0
+#endif
+#ifndef SV_DRAFT_STAGE_KB
+#define SV_DRAFT_STAGE_KB 48
+#endif
+constexpr int kDraftStageBytes = SV_DRAFT_STAGE_KB * 1024;
+
 template <typename T>
 static cudaError_t prepare_draft_sample()
 {
     static cudaError_t once = [] {
         cudaError_t e = cudaFuncSetAttribute(draft_sample_kernel<T>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kStageRowBytes);
+                                             kDraftStageBytes);
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(draft_sample_kernel<T>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -151,13 +161,16 @@ static cudaError_t prepare_draft_sample()
 // ranges of R entries, weighed in slices.  16 CTAs per draw while the
 // clusters fit the GPU at one CTA per SM (larger clusters are harder to
 // place), else 8.  False when the vocabulary exceeds the slice table.
-static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
+static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e, int ncl_force = 0,
+                          int stage_bytes = kStageRowBytes)
 {
     const int gran = 16 / e;
-    const int ncl = draws * kCluster <= (int64_t)sm_count() ? kCluster : kCluster / 2;
+    const int ncl = ncl_force > 0 ? ncl_force
+                                  : (draws * kCluster <= (int64_t)sm_count() ? kCluster
+                                                                              : kCluster / 2);
     fp.ncl = ncl;
     const int R = (int)((((int64_t)V + ncl - 1) / ncl + gran - 1) / gran * gran);
-    const int slice = std::min(R, kStageRowBytes / e);
+    const int slice = std::min(R, stage_bytes / e);
     const int nv = (slice * e + 15) / 16;
     fp.R = R;
     fp.slice = slice;
@@ -217,6 +230,9 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.g = g;
     if (!GREEDY && !draw_geometry(fp, a.B, a.V, e))
         return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
+    // the finish kernel merges up to two rows per warp of the cluster
+    if (!GREEDY && 2 * kMaxDraft + 1 > 2 * kSampleWarps * fp.ncl)
+        return cudaErrorInvalidValue;
     fp.tma = tma;
     fp.c = sp.c;
     fp.status = sp.status;
@@ -403,7 +419,7 @@ static cudaError_t launch_draft_typed(const DraftArgs &a, cudaStream_t s, Tracer
             attr, 1);
         err = cudaLaunchKernelEx(&cfg, draft_greedy_kernel<T>, fp);
     } else {
-        if (!draw_geometry(fp, rows, a.V, e))
+        if (!draw_geometry(fp, rows, a.V, e, SV_DRAFT_NCL, kDraftStageBytes))
             return cudaErrorInvalidValue;
         if ((err = prepare_draft_sample<T>()) != cudaSuccess)
             return err;
