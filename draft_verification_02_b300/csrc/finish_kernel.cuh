@@ -305,6 +305,39 @@ __device__ __forceinline__ int piece_find(const DrawCtx d, const T *tb, const T 
     return lastp;
 }
 
+// piece_find by one warp: the lanes compute the piece's weights (its
+// exponentials) into wbuf, then lane 0 adds them in index order with the
+// additions of piece_sum, so the running sums are the same bit for bit.
+// Every lane of the warp calls it and gets the same index.
+template <typename T>
+__device__ __forceinline__ int piece_find_warp(const DrawCtx d, const T *tb, const T *db, int len,
+                                               int v0, int v1, float rem, float *wbuf)
+{
+    constexpr int E = Elem<T>::kPerVec;
+    const int lane = threadIdx.x & 31;
+    const int k0 = v0 * E, n = max(0, min(v1 * E, len) - k0);  // the piece's elements
+    for (int q = lane; q < n; q += 32) {
+        const int k = k0 + q;
+        wbuf[q] = draw_w(d, Elem<T>::at(tb, k), d.resid ? Elem<T>::at(db, k) : 0.f);
+    }
+    __syncwarp();
+    int res = -1;
+    if (lane == 0) {
+        float acc = 0.f;
+        for (int q = 0; q < n; ++q) {
+            const float w = wbuf[q];
+            acc = __fadd_rn(acc, w);
+            if (w > 0.f)
+                res = k0 + q;
+            if (acc > rem) {
+                res = k0 + q;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xffffffffu, res, 0);
+}
+
 // Stage elements [c0, c0 + len) of the draw rows into shared memory (one
 // TMA bulk copy per row, or plain loads when the rows are not 16-byte
 // aligned), then every thread sums its contiguous piece (kept in piece[]
@@ -399,13 +432,13 @@ struct DrawShared {
 // all CTAs when no range has mass.  Every CTA of the cluster must call it
 // (it contains cluster barriers); no shared memory of another CTA is touched
 // after it returns.  `staged`: the slice of this CTA's range already in the
-// target buffer (-1 none); phase0: the parity of the copy barrier's next
-// phase.
+// target buffer (-1 none); phase_io (may be null): the parity of the copy
+// barrier's next phase, updated for the copies made here.
 template <typename T>
 __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, const T *trow,
                                           const T *drow, float uf, uint32_t rank, int ncl,
                                           const DrawShared<T> &sh, int staged = -1,
-                                          uint32_t phase0 = 0)
+                                          uint32_t *phase_io = nullptr)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     T *tb = sh.tb, *db = sh.db;
@@ -419,7 +452,7 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
     const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
     int weighed = -1;  // slice staged in shared memory
-    uint32_t phase = phase0;  // parity of the copy barrier's next phase
+    uint32_t phase = phase_io ? *phase_io : 0u;  // parity of the copy barrier's next phase
 
     // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
     // second pass over p_a (the same decision in every CTA)
@@ -481,6 +514,8 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
         d.resid = false;  // all-zero residual: draw from p_a instead
     }
     // no shared memory of another CTA is touched after this point
+    if (phase_io)
+        *phase_io = phase;
     const int cs = s_cs;
     bool past = s_past != 0;
     ff base = s_base;
@@ -518,8 +553,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
         }
     }
     const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-    if (sl != weighed)
+    if (sl != weighed) {
         weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
+        if (phase_io)
+            *phase_io = phase;
+    }
     // scan of the piece sums (float-float, fixed order).  A piece's lower end
     // is the previous piece's upper end bit for bit, so the pieces tile the
     // slice with no gap and no overlap.
@@ -553,10 +591,18 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     constexpr int E = Elem<T>::kPerVec;
     const int nv = (len + E - 1) / E;
     const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
-    if (s_hit == tid) {
-        const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
-        s_last = piece_find<T>(d, tb, db, len, v0, v1, rem);
-    } else if (s_hit == INT_MAX) {  // past the end after rounding: the last element with mass
+    const int hit = s_hit;
+    if (hit != INT_MAX) {
+        if (warp == hit >> 5) {  // the hit thread's warp walks its piece
+            const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+            const int hl = hit & 31;
+            const int k = piece_find_warp<T>(d, tb, db, len, __shfl_sync(0xffffffffu, v0, hl),
+                                             __shfl_sync(0xffffffffu, v1, hl),
+                                             __shfl_sync(0xffffffffu, rem, hl), piece);
+            if (lane == 0)
+                s_last = k;
+        }
+    } else {  // past the end after rounding: the last element with mass
         const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
         if (lp >= 0)
             atomicMax(&s_last, lp);
@@ -876,40 +922,43 @@ __global__ void __launch_bounds__(kFinishThreads) confidence_kernel(const ConfPa
 // drafted tokens and acceptance statistics
 // ---------------------------------------------------------------------------
 
-// T > 0, one kernel, one read of each row: one cluster per padded draft row
-// r = i*Kmax + j.  Each CTA stages its range of the row in shared memory
-// (the same ranges and slices as the final draw of a verification) and takes
-// its maximum; the maxima are exchanged through distributed shared memory,
-// and with m known every CTA weighs its range, still in shared memory, by
-// the cluster draw: x = the inverse CDF of q at u[r] over the unnormalised
-// weights 2^(x c - fl(m c)), q(x) = w(x) / S.  Rows past kmax[i] give -1 and
-// 0 and launch no copy.
+// T > 0: one CTA per padded draft row r = i*Kmax + j, one read of the row
+// from HBM.  The row streams through a ring of two slices (TMA bulk copies).
+// Each slice's maximum fixes an integer reference M_k = ceil(max * c), and
+// the slice is weighed in it, w = 2^(x c - M_k) <= 1, by thread pieces as in
+// the verification draw, into the slice total T_k.  Totals in different
+// references meet by exact power-of-two scaling, S = sum_k T_k 2^(M_k - M)
+// with M = max_k M_k, so the slice holding u*S is found from the totals;
+// that slice is copied once more and walked in its own reference, meeting
+// the same running sums as its weighing, bit for bit.  x = the inverse CDF
+// of q = softmax(row / T) at u[r]; q(x) = w(x) 2^(M_k - M) / S.  Rows past
+// kmax[i] give -1 and 0 and are never read.
+constexpr int kMaxRowSlices = 768;  // slices of a row of kMaxVocab f32 logits
+
+// ff scaled by 2^n, exactly unless the low part leaves the normal range
+__device__ __forceinline__ ff ff_ldexp(ff v, int n) { return {ldexpf(v.hi, n), ldexpf(v.lo, n)}; }
+
 template <typename T>
-__global__ void __launch_bounds__(kSampleThreads, 3) draft_sample_kernel(const FinishParams p)
+__global__ void __launch_bounds__(kSampleThreads, 2) draft_sample_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
-    T *tb = reinterpret_cast<T *>(dsm);
-    __shared__ __align__(8) uint64_t bar;
+    __shared__ __align__(8) uint64_t bars[2];
     __shared__ float piece[kSampleThreads];
     __shared__ ff wred[kSampleWarps];
-    __shared__ ff slice_tot[kMaxSlices];
-    __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
-    __shared__ float cl_max[kCluster];               // likewise
     __shared__ float mred[kSampleWarps];
-    __shared__ ff s_excl[kSampleWarps];
-    __shared__ int s_hit, s_last, s_cs, s_past, s_redo, s_expired;
-    __shared__ ff s_base, s_target, s_S;
+    __shared__ ff sl_tot[kMaxRowSlices];
+    __shared__ float sl_ref[kMaxRowSlices];  // M_k, or -inf for a slice without mass
+    __shared__ int s_bad, s_hit, s_last, s_sl, s_past, s_expired, s_shift;
+    __shared__ ff s_rem, s_S;
 
     constexpr int E = Elem<T>::kPerVec;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t rank = cluster_ctarank();
-    const int ncl = p.ncl;
-    const int64_t r = blockIdx.x / ncl;
+    const int64_t r = blockIdx.x;
     const int i = (int)(r / p.Kmax), j = (int)(r - (int64_t)i * p.Kmax);
     const int km = __ldg(p.kmax + i);
     const bool bad_k = km < 0 || km > p.Kmax;
-    if (bad_k || j >= km) {  // the same in every CTA of the cluster: no barrier yet
-        if (rank == 0 && tid == 0) {
+    if (bad_k || j >= km) {  // the whole CTA: no barrier yet
+        if (tid == 0) {
             p.out_tokens[r] = -1;
             p.out_conf[r] = bad_k ? __int_as_float(0x7fc00000) : 0.f;
             if (bad_k)
@@ -917,45 +966,91 @@ __global__ void __launch_bounds__(kSampleThreads, 3) draft_sample_kernel(const F
         }
         return;
     }
-    if (tid == 0) {
-        mbar_init(&bar, 1);
-        fence_mbar_init();
-        s_expired = 0;
-    }
-    cluster_arrive_relaxed();  // (0) this CTA has started
     const float uf = __ldg(p.u_final + r);
     const T *row = reinterpret_cast<const T *>(p.target) + r * p.V;
-    const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
-    const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
+    T *const buf0 = reinterpret_cast<T *>(dsm);
+    T *const buf1 = reinterpret_cast<T *>(dsm + p.stage_smem);
+    const int nsl = (p.V + p.slice - 1) / p.slice;
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+        s_expired = 0;
+        s_bad = 0;
+    }
+    __syncthreads();
 
-    // ---- this range's maximum, slices in reverse so that slice 0 stays staged
-    float mx = -INFINITY;
-    uint32_t phase = 0;
-    __syncthreads();  // the barrier's initialisation is visible
-    for (int sl = nsl - 1; sl >= 0; --sl) {
-        const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-        if (sl != nsl - 1)
-            __syncthreads();  // every thread is done with the previous slice
+    auto issue = [&](int sl, T *dst, uint64_t *bar) {  // thread 0: one bulk copy of slice sl
+        const int c0 = sl * p.slice, len = min(p.slice, p.V - c0);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(dst, row + c0, bytes, bar);
+    };
+    auto land = [&](int sl, T *dst, uint64_t *bar, uint32_t &ph) {  // slice sl is in dst
         if (p.tma) {
-            if (tid == 0) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                const uint32_t bytes = (uint32_t)len * (uint32_t)sizeof(T);
-                mbar_arrive_expect_tx(&bar, bytes);
-                bulk_g2s(tb, row + c0, bytes, &bar);
-            }
-            if (!mbar_wait_bounded(&bar, phase)) {
+            if (!mbar_wait_bounded(bar, ph)) {
                 set_status(p.status, ST_TIMEOUT);
                 s_expired = 1;
-                mbar_wait_bounded(&bar, phase);  // the copy in flight, once more
+                mbar_wait_bounded(bar, ph);  // the copy in flight, once more
             }
-            phase ^= 1u;
+            ph ^= 1u;
         } else {
+            const int c0 = sl * p.slice, len = min(p.slice, p.V - c0);
             for (int k = tid; k < len; k += kSampleThreads)
-                tb[k] = row[c0 + k];
+                dst[k] = row[c0 + k];
             __syncthreads();
         }
-        const uint4 *tv = reinterpret_cast<const uint4 *>(tb);
-        const int nfull = len / E;  // whole vectors, then the partial tail (plain loads only)
+    };
+    // block sum of one float per thread as float-float, in a fixed order; the
+    // closing barrier also ends every thread's reads of the slice
+    auto block_sum = [&](float x) -> ff {
+        ff w{x, 0.f};
+#pragma unroll 1
+        for (int o = 16; o > 0; o >>= 1)
+            w = ff_add(w, ff_shfl_xor(w, o));
+        if (lane == 0)
+            wred[warp] = w;
+        __syncthreads();
+        ff t = wred[0];
+        for (int q = 1; q < kSampleWarps; ++q)
+            t = ff_add(t, wred[q]);
+        __syncthreads();  // wred may be written again
+        return t;
+    };
+    // this thread's piece of a slice of len elements: vectors [v0, v1)
+    auto piece_of = [&](int len, int &v0, int &v1) {
+        const int nv = (len + E - 1) / E;
+        v0 = min(nv, tid * p.pv);
+        v1 = min(nv, v0 + p.pv);
+    };
+    DrawCtx d;
+    d.resid = false;
+    d.c = p.c;
+    d.sc_t = 0.f;
+    d.mcd = 0.f;
+    d.sc_d = 0.f;
+
+    // ---- one pass over the row: slice maxima, references and totals
+    uint32_t ph0 = 0u, ph1 = 0u;
+    if (p.tma && tid == 0) {
+        issue(0, buf0, &bars[0]);
+        if (nsl > 1)
+            issue(1, buf1, &bars[1]);
+    }
+    for (int sl = 0; sl < nsl; ++sl) {
+        const bool odd = sl & 1;
+        T *const buf = odd ? buf1 : buf0;
+        uint64_t *const bar = odd ? &bars[1] : &bars[0];
+        if (odd)
+            land(sl, buf, bar, ph1);
+        else
+            land(sl, buf, bar, ph0);
+        const int len = min(p.slice, p.V - sl * p.slice);
+        // maximum (packed for bf16)
+        const uint4 *tv = reinterpret_cast<const uint4 *>(buf);
+        const int nfull = len / E;
+        float mx = -INFINITY;
         if constexpr (sizeof(T) == 2) {
             uint32_t m2 = 0xff80ff80u;  // -inf, -inf
 #pragma unroll 4
@@ -964,68 +1059,199 @@ __global__ void __launch_bounds__(kSampleThreads, 3) draft_sample_kernel(const F
                 m2 = max_nan_bf16x2(m2, max_nan_bf16x2(max_nan_bf16x2(x.x, x.y),
                                                        max_nan_bf16x2(x.z, x.w)));
             }
-            mx = max_nan(mx, max_nan(bf16_lo(m2), bf16_hi(m2)));
+            mx = max_nan(bf16_lo(m2), bf16_hi(m2));
         } else {
 #pragma unroll 4
             for (int v = tid; v < nfull; v += kSampleThreads) {
-                const float4 x = reinterpret_cast<const float4 *>(tb)[v];
+                const float4 x = reinterpret_cast<const float4 *>(buf)[v];
                 mx = max_nan(mx, max_nan(max_nan(x.x, x.y), max_nan(x.z, x.w)));
             }
         }
         for (int k = nfull * E + tid; k < len; k += kSampleThreads)
-            mx = max_nan(mx, Elem<T>::at(tb, k));
-    }
-    mx = warp_max_nan(mx);
-    if (lane == 0)
-        mred[warp] = mx;
-    __syncthreads();
-    cluster_wait_acquire();  // (0) complete: every CTA's shared memory is live
-    if (warp == 0) {
-        float v = lane < kSampleWarps ? mred[lane] : -INFINITY;
-        v = warp_max_nan(v);
-        if (lane < ncl) {
-            uint32_t remote;
-            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;"
-                         : "=r"(remote)
-                         : "r"(smem_u32(&cl_max[rank])), "r"((uint32_t)lane));
-            asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+            mx = max_nan(mx, Elem<T>::at(buf, k));
+        mx = warp_max_nan(mx);
+        if (lane == 0)
+            mred[warp] = mx;
+        __syncthreads();
+        float sm = mred[0];
+        for (int q = 1; q < kSampleWarps; ++q)
+            sm = max_nan(sm, mred[q]);
+        // the slice's reference: NaN / +inf (or a reference beyond the float
+        // range of the weights) make the row an error
+        const float ref = sm == -INFINITY ? -INFINITY : ceilf(sm * p.c);
+        const bool bad = !(sm == -INFINITY || (ref > -1e30f && ref < 1e30f));
+        ff tot{0.f, 0.f};
+        if (!bad && ref > -INFINITY) {
+            d.mct = ref;
+            int v0, v1;
+            piece_of(len, v0, v1);
+            tot = block_sum(piece_sum<T>(d, buf, nullptr, len, v0, v1));
+        } else {
+            __syncthreads();  // every thread is done with the slice
+        }
+        if (tid == 0) {
+            sl_tot[sl] = tot;
+            sl_ref[sl] = bad ? -INFINITY : ref;
+            if (bad)
+                s_bad = 1;
+            if (p.tma && sl + 2 < nsl)  // the buffer is free: the slice after next
+                issue(sl + 2, buf, bar);
         }
     }
-    cluster_arrive_release();
-    cluster_wait_acquire();  // (1) every CTA holds every range's maximum
-    float m = -INFINITY;
-    for (int q = 0; q < ncl; ++q)
-        m = max_nan(m, cl_max[q]);
-    if (!(m > -INFINITY && m < INFINITY)) {  // NaN, +inf or a fully masked row: the same
-        if (rank == 0 && tid == 0) {          // in every CTA, after the last exchange
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
             set_status(p.status, ST_NONFINITE);
             p.out_tokens[r] = -1;
             p.out_conf[r] = __int_as_float(0x7fc00000);
         }
         return;
     }
-    DrawCtx d;
-    d.resid = false;
-    d.c = p.c;
-    d.mct = m * p.c;
-    d.sc_t = 0.f;
-    d.mcd = 0.f;
-    d.sc_d = 0.f;
-    const DrawShared<T> sh{tb,      nullptr, &bar,   piece,   wred,    slice_tot, s_excl,
-                           cl_sum,  &s_hit,  &s_last, &s_cs, &s_past, &s_redo,   &s_expired,
-                           &s_base, &s_target, &s_S};
-    const int y0 =
-        draw_token<T>(p, d, row, nullptr, uf, rank, ncl, sh, nsl > 0 ? 0 : -1, phase);
-    if (y0 == -2)
-        return;  // another CTA's range holds u*S
+
+    // ---- S and the slice holding u*S (warp 0, slices in chunks of 32)
+    if (warp == 0) {
+        float M = -INFINITY;
+        for (int k = lane; k < nsl; k += 32)
+            M = fmaxf(M, sl_ref[k]);
+        M = warp_max_nan(M);
+        auto scaled = [&](int k) -> ff {  // T_k 2^(M_k - M), exact
+            if (k >= nsl || sl_ref[k] == -INFINITY)
+                return ff{0.f, 0.f};
+            return ff_ldexp(sl_tot[k], max(-300, (int)(sl_ref[k] - M)));
+        };
+        ff S{0.f, 0.f};
+        for (int c0 = 0; c0 < nsl; c0 += 32) {
+            ff incl = scaled(c0 + lane);
+#pragma unroll 1
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff n = ff_shfl_up(incl, o);
+                if (lane >= o)
+                    incl = ff_add(n, incl);
+            }
+            S = ff_add(S, ff{__shfl_sync(0xffffffffu, incl.hi, 31),
+                             __shfl_sync(0xffffffffu, incl.lo, 31)});
+        }
+        const ff target = ff_mul(S, uf);
+        int found = -1, lastm = -1;
+        ff run{0.f, 0.f}, base{0.f, 0.f}, lastbase{0.f, 0.f};
+        for (int c0 = 0; c0 < nsl && found < 0; c0 += 32) {
+            const ff v = scaled(c0 + lane);
+            ff incl = v;
+#pragma unroll 1
+            for (int o = 1; o < 32; o <<= 1) {
+                const ff n = ff_shfl_up(incl, o);
+                if (lane >= o)
+                    incl = ff_add(n, incl);
+            }
+            ff excl = ff_shfl_up(incl, 1);
+            if (lane == 0)
+                excl = {0.f, 0.f};
+            const ff full = ff_add(run, incl);
+            const unsigned over = __ballot_sync(0xffffffffu, c0 + lane < nsl && ff_gt(full, target));
+            const unsigned mass = __ballot_sync(0xffffffffu, c0 + lane < nsl && v.hi > 0.f);
+            if (mass) {  // the last slice with mass so far, for u*S past the end
+                const int src = 31 - __clz(mass);
+                lastm = c0 + src;
+                lastbase = ff_add(run, ff{__shfl_sync(0xffffffffu, excl.hi, src),
+                                          __shfl_sync(0xffffffffu, excl.lo, src)});
+            }
+            if (over) {
+                const int src = __ffs(over) - 1;
+                found = c0 + src;
+                base = ff_add(run, ff{__shfl_sync(0xffffffffu, excl.hi, src),
+                                      __shfl_sync(0xffffffffu, excl.lo, src)});
+            }
+            run = ff_add(run, ff{__shfl_sync(0xffffffffu, incl.hi, 31),
+                                 __shfl_sync(0xffffffffu, incl.lo, 31)});
+        }
+        if (lane == 0) {
+            const bool past = found < 0;
+            const int k = past ? lastm : found;
+            s_sl = k;
+            s_past = past;
+            s_S = S;
+            if (k >= 0) {
+                const int sh = (int)(M - sl_ref[k]);  // >= 0
+                s_shift = sh;
+                s_rem = ff_ldexp(ff_add(target, ff{-(past ? lastbase : base).hi,
+                                                   -(past ? lastbase : base).lo}),
+                                 min(sh, 300));
+            }
+        }
+    }
+    __syncthreads();
+    const int ks = s_sl;
+    if (ks < 0) {  // no mass at all (an all-masked row was caught above)
+        if (tid == 0) {
+            set_status(p.status, ST_NONFINITE);
+            p.out_tokens[r] = -1;
+            p.out_conf[r] = __int_as_float(0x7fc00000);
+        }
+        return;
+    }
+
+    // ---- the chosen slice once more, its pieces, then one thread's walk
+    const int c0 = ks * p.slice, len = min(p.slice, p.V - c0);
+    if (p.tma && tid == 0)
+        issue(ks, buf0, &bars[0]);
+    land(ks, buf0, &bars[0], ph0);
+    d.mct = sl_ref[ks];
+    int v0, v1;
+    piece_of(len, v0, v1);
+    const float ps = piece_sum<T>(d, buf0, nullptr, len, v0, v1);
+    piece[tid] = ps;
+    ff incl{ps, 0.f};
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(incl, o);
+        if (lane >= o)
+            incl = ff_add(n, incl);
+    }
+    ff excl = ff_shfl_up(incl, 1);
+    if (lane == 0)
+        excl = {0.f, 0.f};
     if (tid == 0) {
-        int y = y0;
+        s_hit = INT_MAX;
+        s_last = -1;
+    }
+    if (lane == 31)
+        wred[warp] = incl;
+    __syncthreads();
+    ff wbase{0.f, 0.f};
+    for (int q = 0; q < warp; ++q)
+        wbase = ff_add(wbase, wred[q]);
+    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
+    const ff rem = s_rem;
+    const bool past = s_past != 0;
+    if (!past && ff_le(lo, rem) && ff_gt(hi, rem))
+        atomicMin(&s_hit, tid);
+    __syncthreads();
+    const int hit = s_hit;
+    if (hit != INT_MAX) {
+        if (warp == hit >> 5) {  // the hit thread's warp walks its piece
+            const float rr = __fadd_rn(__fsub_rn(rem.hi, lo.hi), __fsub_rn(rem.lo, lo.lo));
+            const int hl = hit & 31;
+            const int k = piece_find_warp<T>(d, buf0, nullptr, len,
+                                             __shfl_sync(0xffffffffu, v0, hl),
+                                             __shfl_sync(0xffffffffu, v1, hl),
+                                             __shfl_sync(0xffffffffu, rr, hl), piece);
+            if (lane == 0)
+                s_last = k;
+        }
+    } else {  // past the end after rounding: the last element with mass
+        const int lp = piece_find<T>(d, buf0, nullptr, len, v0, v1, INFINITY);
+        if (lp >= 0)
+            atomicMax(&s_last, lp);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int y = s_last >= 0 ? c0 + s_last : -1;
         float conf = __int_as_float(0x7fc00000);
         if (y < 0) {
             set_status(p.status, ST_NONFINITE);
         } else {
             const float w = ex2_approx(fmaf(Elem<T>::ld_global(row, y), d.c, -d.mct));
-            conf = __fdiv_rn(w, __fadd_rn(s_S.hi, s_S.lo));
+            conf = __fdiv_rn(ldexpf(w, -min(s_shift, 300)), __fadd_rn(s_S.hi, s_S.lo));
         }
         if (s_expired || (read_status(p.status) & ST_TIMEOUT)) {  // a copy gave up
             y = -1;

@@ -132,11 +132,8 @@ static cudaError_t prepare_finish_sample()
     return once;
 }
 
-// Drafting at T > 0: CTAs per row (0: the verification draw's rule) and the
-// staging buffer of each CTA's range.
-#ifndef SV_DRAFT_NCL
-#define SV_DRAFT_NCL 0
-#endif
+// Drafting at T > 0: each CTA streams its row through two slices of at most
+// this size, which leaves room for two CTAs per SM.
 #ifndef SV_DRAFT_STAGE_KB
 #define SV_DRAFT_STAGE_KB 48
 #endif
@@ -148,10 +145,7 @@ static cudaError_t prepare_draft_sample()
     static cudaError_t once = [] {
         cudaError_t e = cudaFuncSetAttribute(draft_sample_kernel<T>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kDraftStageBytes);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(draft_sample_kernel<T>,
-                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+                                             2 * kDraftStageBytes);
         return e;
     }();
     return once;
@@ -419,16 +413,23 @@ static cudaError_t launch_draft_typed(const DraftArgs &a, cudaStream_t s, Tracer
             attr, 1);
         err = cudaLaunchKernelEx(&cfg, draft_greedy_kernel<T>, fp);
     } else {
-        if (!draw_geometry(fp, rows, a.V, e, SV_DRAFT_NCL, kDraftStageBytes))
+        // one CTA per row; the row streams through two slices of shared memory
+        const int gran = 16 / e;
+        const int slice = std::min((a.V + gran - 1) / gran * gran, kDraftStageBytes / e);
+        if (((int64_t)a.V + slice - 1) / slice > kMaxRowSlices)
             return cudaErrorInvalidValue;
+        fp.slice = slice;
+        fp.pv = (((slice * e + 15) / 16 + kSampleThreads - 1) / kSampleThreads) | 1;
+        fp.stage_smem = (int)align_up((size_t)slice * e, 128);
         if ((err = prepare_draft_sample<T>()) != cudaSuccess)
             return err;
         fp.tma = ((int64_t)a.V * e) % 16 == 0 && reinterpret_cast<uintptr_t>(a.draft) % 16 == 0;
         fp.c = (float)(1.4426950408889634074 / a.temperature);  // log2(e) / T
-        cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)(rows * fp.ncl)), dim3(kSampleThreads),
-                                            (size_t)fp.stage_smem, s, attr, fp.ncl);
-        cfg.attrs = attr + 1;  // a cluster launch with no programmatic predecessor
-        cfg.numAttrs = 1;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)rows);
+        cfg.blockDim = dim3(kSampleThreads);
+        cfg.dynamicSmemBytes = 2 * (size_t)fp.stage_smem;
+        cfg.stream = s;
         tr.begin(s);
         err = cudaLaunchKernelEx(&cfg, draft_sample_kernel<T>, fp);
     }
