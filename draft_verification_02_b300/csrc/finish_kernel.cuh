@@ -933,7 +933,7 @@ __global__ void __launch_bounds__(kFinishThreads) confidence_kernel(const ConfPa
 // the same running sums as its weighing, bit for bit.  x = the inverse CDF
 // of q = softmax(row / T) at u[r]; q(x) = w(x) 2^(M_k - M) / S.  Rows past
 // kmax[i] give -1 and 0 and are never read.
-constexpr int kMaxRowSlices = 768;  // slices of a row of kMaxVocab f32 logits
+constexpr int kMaxRowSlices = 1408;  // 24 KB slices of a row of kMaxVocab f32 logits
 
 // ff scaled by 2^n, exactly unless the low part leaves the normal range
 __device__ __forceinline__ ff ff_ldexp(ff v, int n) { return {ldexpf(v.hi, n), ldexpf(v.lo, n)}; }
@@ -946,8 +946,6 @@ __global__ void __launch_bounds__(kSampleThreads, 2) draft_sample_kernel(const F
     __shared__ float piece[kSampleThreads];
     __shared__ ff wred[kSampleWarps];
     __shared__ float mred[kSampleWarps];
-    __shared__ ff sl_tot[kMaxRowSlices];
-    __shared__ float sl_ref[kMaxRowSlices];  // M_k, or -inf for a slice without mass
     __shared__ int s_bad, s_hit, s_last, s_sl, s_past, s_expired, s_shift;
     __shared__ ff s_rem, s_S;
 
@@ -971,6 +969,9 @@ __global__ void __launch_bounds__(kSampleThreads, 2) draft_sample_kernel(const F
     T *const buf0 = reinterpret_cast<T *>(dsm);
     T *const buf1 = reinterpret_cast<T *>(dsm + p.stage_smem);
     const int nsl = (p.V + p.slice - 1) / p.slice;
+    // per slice: its total (float-float) and reference M_k (-inf: no mass)
+    ff *const sl_tot = reinterpret_cast<ff *>(dsm + 2 * (size_t)p.stage_smem);
+    float *const sl_ref = reinterpret_cast<float *>(sl_tot + nsl);
     if (tid == 0) {
         mbar_init(&bars[0], 1);
         mbar_init(&bars[1], 1);
@@ -1002,21 +1003,18 @@ __global__ void __launch_bounds__(kSampleThreads, 2) draft_sample_kernel(const F
             __syncthreads();
         }
     };
-    // block sum of one float per thread as float-float, in a fixed order; the
-    // closing barrier also ends every thread's reads of the slice
-    auto block_sum = [&](float x) -> ff {
-        ff w{x, 0.f};
+    // float-float sum of piece[0 .. kSampleThreads) in a fixed order, by warp 0
+    // (every lane gets it)
+    auto warp0_sum = [&]() -> ff {
+        constexpr int per = kSampleThreads / 32;
+        ff w{0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < per; ++q)
+            w = ff_add(w, ff{piece[lane * per + q], 0.f});
 #pragma unroll 1
         for (int o = 16; o > 0; o >>= 1)
             w = ff_add(w, ff_shfl_xor(w, o));
-        if (lane == 0)
-            wred[warp] = w;
-        __syncthreads();
-        ff t = wred[0];
-        for (int q = 1; q < kSampleWarps; ++q)
-            t = ff_add(t, wred[q]);
-        __syncthreads();  // wred may be written again
-        return t;
+        return w;
     };
     // this thread's piece of a slice of len elements: vectors [v0, v1)
     auto piece_of = [&](int len, int &v0, int &v1) {
@@ -1080,22 +1078,26 @@ __global__ void __launch_bounds__(kSampleThreads, 2) draft_sample_kernel(const F
         // range of the weights) make the row an error
         const float ref = sm == -INFINITY ? -INFINITY : ceilf(sm * p.c);
         const bool bad = !(sm == -INFINITY || (ref > -1e30f && ref < 1e30f));
-        ff tot{0.f, 0.f};
-        if (!bad && ref > -INFINITY) {
+        const bool weigh = !bad && ref > -INFINITY;
+        float ps = 0.f;
+        if (weigh) {
             d.mct = ref;
             int v0, v1;
             piece_of(len, v0, v1);
-            tot = block_sum(piece_sum<T>(d, buf, nullptr, len, v0, v1));
-        } else {
-            __syncthreads();  // every thread is done with the slice
+            ps = piece_sum<T>(d, buf, nullptr, len, v0, v1);
         }
-        if (tid == 0) {
-            sl_tot[sl] = tot;
-            sl_ref[sl] = bad ? -INFINITY : ref;
-            if (bad)
-                s_bad = 1;
-            if (p.tma && sl + 2 < nsl)  // the buffer is free: the slice after next
-                issue(sl + 2, buf, bar);
+        piece[tid] = ps;
+        __syncthreads();  // every thread is done with the slice and piece[] is complete
+        if (warp == 0) {  // the slice total; the other warps go on to the next slice
+            const ff tot = weigh ? warp0_sum() : ff{0.f, 0.f};
+            if (lane == 0) {
+                sl_tot[sl] = tot;
+                sl_ref[sl] = bad ? -INFINITY : ref;
+                if (bad)
+                    s_bad = 1;
+                if (p.tma && sl + 2 < nsl)  // the buffer is free: the slice after next
+                    issue(sl + 2, buf, bar);
+            }
         }
     }
     __syncthreads();
