@@ -419,8 +419,7 @@ struct DrawShared {
     float *piece;
     ff *wred, *slice_tot, *s_excl;
     ff (*cl_sum)[kCluster];  // written by every CTA of the cluster
-    int *s_hit, *s_last, *s_cs, *s_past, *s_redo, *s_expired;
-    ff *s_base, *s_target;
+    int *s_hit, *s_last, *s_expired;
     ff *s_total;  // S, the sum of every weight (may be null)
 };
 
@@ -445,9 +444,7 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     float *piece = sh.piece;
     ff *wred = sh.wred, *slice_tot = sh.slice_tot, *s_excl = sh.s_excl;
     ff(*cl_sum)[kCluster] = sh.cl_sum;
-    int &s_hit = *sh.s_hit, &s_last = *sh.s_last, &s_cs = *sh.s_cs, &s_past = *sh.s_past,
-        &s_redo = *sh.s_redo, &s_expired = *sh.s_expired;
-    ff &s_base = *sh.s_base, &s_target = *sh.s_target;
+    int &s_hit = *sh.s_hit, &s_last = *sh.s_last, &s_expired = *sh.s_expired;
     uint64_t &bar = *sh.bar;
     const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
     const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
@@ -456,7 +453,9 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
 
     // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
     // second pass over p_a (the same decision in every CTA)
-    int slot = 0;
+    int cs = -1;
+    bool past = true, redo = false;
+    ff base{0.f, 0.f}, target{0.f, 0.f};
     for (int pass = 0; pass < 2; ++pass) {
         ff mine{0.f, 0.f};
         for (int sl = 0; sl < nsl; ++sl) {
@@ -472,12 +471,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
             st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
         cluster_arrive_release();
         cluster_wait_acquire();  // (2 + pass) every CTA holds every range sum
-        slot = pass;
-        // S and the range holding u*S, by warp 0 (lane r holds range r): an
-        // inclusive float-float scan in range order, the same in every CTA.
-        // `past` marks u*S at or beyond the end after rounding: then the
-        // last weight > 0 wins.
-        if (warp == 0) {
+        // S and the range holding u*S, in every warp (lane r holds range r):
+        // an inclusive float-float scan in range order, the same bits in every
+        // warp of every CTA.  `past` marks u*S at or beyond the end after
+        // rounding: then the last weight > 0 wins.
+        {
             const ff v = lane < ncl ? cl_sum[pass][lane] : ff{0.f, 0.f};
             ff incl = v;
 #pragma unroll 1
@@ -488,38 +486,27 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
             }
             const ff S = {__shfl_sync(0xffffffffu, incl.hi, 31),
                           __shfl_sync(0xffffffffu, incl.lo, 31)};
-            const ff target = ff_mul(S, uf);
+            target = ff_mul(S, uf);
             const unsigned over = __ballot_sync(0xffffffffu, lane < ncl && ff_gt(incl, target));
             const unsigned mass = __ballot_sync(0xffffffffu, lane < ncl && v.hi > 0.f);
-            const int cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
+            cs = over ? __ffs(over) - 1 : (mass ? 31 - __clz(mass) : -1);
             ff excl = ff_shfl_up(incl, 1);
             if (lane == 0)
                 excl = {0.f, 0.f};
             const int src = cs < 0 ? 0 : cs;
-            const ff base = {__shfl_sync(0xffffffffu, excl.hi, src),
-                             __shfl_sync(0xffffffffu, excl.lo, src)};
-            if (lane == 0) {
-                if (sh.s_total)
-                    *sh.s_total = S;
-                s_cs = cs;
-                s_past = over == 0u;
-                s_base = base;
-                s_target = target;
-                s_redo = !(S.hi > 0.f);
-            }
+            base = {__shfl_sync(0xffffffffu, excl.hi, src), __shfl_sync(0xffffffffu, excl.lo, src)};
+            past = over == 0u;
+            if (sh.s_total && tid == 0)
+                *sh.s_total = S;
+            redo = !(S.hi > 0.f);
         }
-        __syncthreads();
-        if (!(d.resid && s_redo))
+        if (!(d.resid && redo))
             break;
         d.resid = false;  // all-zero residual: draw from p_a instead
     }
     // no shared memory of another CTA is touched after this point
     if (phase_io)
         *phase_io = phase;
-    const int cs = s_cs;
-    bool past = s_past != 0;
-    ff base = s_base;
-    const ff target = s_target;
     if ((int)rank != cs)
         return cs < 0 ? -1 : -2;  // -1: no mass at all (never with finite rows)
 
@@ -626,9 +613,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     __shared__ ff slice_tot[kMaxSlices];
     __shared__ __align__(8) ff cl_sum[2][kCluster];  // written by every CTA of the cluster
     __shared__ ff s_excl[kSampleWarps];
-    __shared__ int s_a, s_bad, s_hit, s_last, s_cs, s_past, s_redo, s_expired;
-    __shared__ ff s_base, s_target;
-    __shared__ DrawCtx s_d;
+    __shared__ int s_hit, s_last, s_expired;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t rank = cluster_ctarank();
@@ -648,8 +633,8 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     const bool shape = request_shape_ok(p, i, cu_i, K);
     const int64_t t0 = (int64_t)cu_i + i;
     const int nrows = 2 * K + 1;
-    // warp 0, lane j < K: the drafted token and its uniform (accept test)
-    const bool act = shape && warp == 0 && lane < K;
+    // lane j < K of every warp: the drafted token and its uniform (accept test)
+    const bool act = shape && lane < K;
     int x = -1;
     float u = 0.f;
     int64_t di = 0;
@@ -735,8 +720,12 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
     }
 
-    // ---- accept test and first rejection (warp 0; identical in every CTA)
-    if (warp == 0) {
+    // ---- accept test and first rejection: every warp takes the same decision
+    // from the same shared rows (no broadcast, no barrier); warp 0 writes
+    int a;
+    bool bad;
+    DrawCtx d;
+    {
         bool bad_tok = act && (x < 0 || x >= p.V), bad_nf = false, acc = true;
         float pp = 0.f, qq = 0.f;
         if (act && !bad_tok) {
@@ -757,9 +746,9 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         const unsigned rej = __ballot_sync(0xffffffffu, act && !acc);
         // bad depends only on the request's data, so every CTA of the cluster
         // takes the same branch; an expired wait only poisons (best effort)
-        const bool bad = nf || bt;
-        const int a = rej ? __ffs(rej) - 1 : K;
-        if (rank == 0) {  // the request's outputs, written once
+        bad = nf || bt;
+        a = rej ? __ffs(rej) - 1 : K;
+        if (rank == 0 && warp == 0) {  // the request's outputs, written once
             if (bad || timeout) {
                 if (lane == 0)
                     set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
@@ -782,40 +771,30 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
                     p.out_len[i] = a;
             }
         }
-        if (lane == 0) {
-            s_a = a;
-            s_bad = bad;
-            // the final draw's constants, once for the CTA
-            DrawCtx d0;
-            d0.resid = a < K;
-            d0.c = p.c;
-            const float mt = row_m[a];
-            d0.mct = mt * p.c;
-            d0.sc_t = ff_recip_scaled(mc_correction(mt, d0.mct, p.c), row_s[a]);
-            d0.mcd = 0.f;
-            d0.sc_d = 0.f;
-            if (d0.resid) {
-                const float md = row_m[K + 1 + a];
-                d0.mcd = md * p.c;
-                d0.sc_d = ff_recip_scaled(mc_correction(md, d0.mcd, p.c), row_s[K + 1 + a]);
-            }
-            s_d = d0;
+        // the final draw's constants
+        d.resid = a < K;
+        d.c = p.c;
+        const float mt = row_m[a];
+        d.mct = mt * p.c;
+        d.sc_t = ff_recip_scaled(mc_correction(mt, d.mct, p.c), row_s[a]);
+        d.mcd = 0.f;
+        d.sc_d = 0.f;
+        if (d.resid) {
+            const float md = row_m[K + 1 + a];
+            d.mcd = md * p.c;
+            d.sc_d = ff_recip_scaled(mc_correction(md, d.mcd, p.c), row_s[K + 1 + a]);
         }
     }
-    __syncthreads();
-    if (s_bad)
-        return;  // same decision in every CTA of the cluster; no more cluster traffic
+    if (bad)
+        return;  // same decision in every warp and CTA of the cluster; no more cluster traffic
 
     // ---- final draw: this CTA weighs its range of the vocabulary
-    const int a = s_a;
     const int64_t trow_i = t0 + a;
     const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
-    DrawCtx d = s_d;
     const T *trow = tbase + trow_i * p.V;
     const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
-    const DrawShared<T> sh{tb,     db,     &bar,   piece,   wred,    slice_tot, s_excl,
-                           cl_sum, &s_hit, &s_last, &s_cs, &s_past, &s_redo, &s_expired,
-                           &s_base, &s_target, nullptr};
+    const DrawShared<T> sh{tb,     db,      &bar,    piece,      wred,   slice_tot,
+                           s_excl, cl_sum,  &s_hit,  &s_last,    &s_expired, nullptr};
     const int y0 = draw_token<T>(p, d, trow, drow, uf, rank, ncl, sh);
     if (y0 == -2)
         return;  // another CTA's range holds u*S
