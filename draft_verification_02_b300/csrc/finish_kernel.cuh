@@ -345,7 +345,7 @@ __device__ __forceinline__ int piece_find_warp(const DrawCtx d, const T *tb, con
 // order.  Once any copy of this call has timed out nothing more is copied.
 // With copy == false the slice is already staged.
 template <typename T>
-__device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, const T *trow,
+__device__ __forceinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, const T *trow,
                                        const T *drow, int c0, int len, T *tb, T *db,
                                        uint64_t *bar, uint32_t *phase, float *piece, ff *wred,
                                        int *expired, bool copy = true)
@@ -397,6 +397,19 @@ __device__ __noinline__ ff weigh_slice(const FinishParams &p, const DrawCtx d, c
     return tot;
 }
 
+// The same, compiled once out of line.  A kernel that calls it keeps more
+// registers per thread (the call's convention), so fewer of its CTAs share
+// an SM with the streaming kernel's; measured, that suits small grids.
+template <typename T>
+__device__ __noinline__ ff weigh_slice_outlined(const FinishParams &p, const DrawCtx d,
+                                                const T *trow, const T *drow, int c0, int len,
+                                                T *tb, T *db, uint64_t *bar, uint32_t *phase,
+                                                float *piece, ff *wred, int *expired, bool copy)
+{
+    return weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, bar, phase, piece, wred, expired,
+                          copy);
+}
+
 // Store (m, s, p(x)) of row k into the shared memory of cluster CTA `rank`.
 __device__ __forceinline__ void st_cluster_row(float *row_m, ff *row_s, float *row_p, int k,
                                                uint32_t rank, float m, ff s, float px)
@@ -433,7 +446,7 @@ struct DrawShared {
 // after it returns.  `staged`: the slice of this CTA's range already in the
 // target buffer (-1 none); phase_io (may be null): the parity of the copy
 // barrier's next phase, updated for the copies made here.
-template <typename T>
+template <typename T, bool OUTLINE>
 __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, const T *trow,
                                           const T *drow, float uf, uint32_t rank, int ncl,
                                           const DrawShared<T> &sh, int staged = -1,
@@ -460,8 +473,12 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
         ff mine{0.f, 0.f};
         for (int sl = 0; sl < nsl; ++sl) {
             const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-            const ff ss = weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
-                                         wred, &s_expired, !(pass == 0 && sl == 0 && staged == 0));
+            const bool cp = !(pass == 0 && sl == 0 && staged == 0);
+            const ff ss =
+                OUTLINE ? weigh_slice_outlined<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase,
+                                                  piece, wred, &s_expired, cp)
+                        : weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
+                                         wred, &s_expired, cp);
             weighed = sl;
             if (tid == 0)
                 slice_tot[sl] = ss;
@@ -541,7 +558,12 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     }
     const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
     if (sl != weighed) {
-        weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred, &s_expired);
+        if (OUTLINE)
+            weigh_slice_outlined<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
+                                    &s_expired, true);
+        else
+            weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
+                           &s_expired);
         if (phase_io)
             *phase_io = phase;
     }
@@ -598,7 +620,7 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     return s_last >= 0 ? c0 + s_last : -1;
 }
 
-template <typename T>
+template <typename T, bool OUTLINE>
 __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
@@ -795,7 +817,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
     const DrawShared<T> sh{tb,     db,      &bar,    piece,      wred,   slice_tot,
                            s_excl, cl_sum,  &s_hit,  &s_last,    &s_expired, nullptr};
-    const int y0 = draw_token<T>(p, d, trow, drow, uf, rank, ncl, sh);
+    const int y0 = draw_token<T, OUTLINE>(p, d, trow, drow, uf, rank, ncl, sh);
     if (y0 == -2)
         return;  // another CTA's range holds u*S
     if (tid == 0) {

@@ -117,15 +117,15 @@ static cudaError_t prepare_stream()
     return once;
 }
 
-template <typename T>
+template <typename T, bool OUTLINE>
 static cudaError_t prepare_finish_sample()
 {
     static cudaError_t once = [] {
-        cudaError_t e = cudaFuncSetAttribute(finish_sample_kernel<T>,
+        cudaError_t e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              2 * kStageRowBytes);
         if (e == cudaSuccess)  // clusters of 16 CTAs
-            e = cudaFuncSetAttribute(finish_sample_kernel<T>,
+            e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         return e;
     }();
@@ -235,8 +235,15 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.part = sp.part;
 
     cudaError_t err = prepare_stream<T, GREEDY>();
+    // The finish kernel with its weighing out of line (more registers, at
+    // most two CTAs per SM) when its CTAs can each have an SM and the rows
+    // are long, inline otherwise (72 registers, three CTAs per SM).  Measured
+    // on B300: B=16, V=128000 (128 CTAs) 22.0 us out of line vs 22.4 inline;
+    // B=4, V=1024 10.4 inline vs 10.9; B=32 and B=64 at V >= 128000 0.7-3.3 us
+    // faster inline.
+    const bool outline = (int64_t)a.B * fp.ncl <= (int64_t)sm_count() && a.V >= 32768;
     if (err == cudaSuccess && !GREEDY)
-        err = prepare_finish_sample<T>();
+        err = outline ? prepare_finish_sample<T, true>() : prepare_finish_sample<T, false>();
     if (err != cudaSuccess)
         return err;
     const int grid1 = (g.P + kStreamWarps - 1) / kStreamWarps;
@@ -269,7 +276,8 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        err = cudaLaunchKernelEx(&cfg, finish_sample_kernel<T>, fp);
+        err = outline ? cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, true>, fp)
+                      : cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, false>, fp);
     }
     if (err != cudaSuccess)
         return err;
