@@ -14,12 +14,13 @@
 //
 // Kernel: every candidate (i, d) becomes one 64-bit key
 //   hi 32 bits: 0x3F800000 - bits(P)   (P in [0,1]: larger P -> smaller key)
-//   lo 32 bits: i * Kp + (d - 1)       (ties: lower request, then lower depth)
-// Each request's keys are already ascending (P never grows with d), so the
-// batch is sorted by log2(#requests) rounds of pairwise merges of sorted runs
-// in shared memory: an element's place in the merged run is its index in its
-// own run plus the number of smaller keys in the partner run (binary search;
-// keys are unique).  The first min(budget, #{P >= min_gain}) keys are kept.
+//   lo 32 bits: i * Kmax + (d - 1)     (ties: lower request, then lower depth)
+// The first keep = min(budget, #{P >= min_gain}) keys in key order are kept.
+// No sort is needed: a most-significant-digit radix select (8 bits a pass,
+// shared-memory histograms) finds the keep-th smallest key tau, and a request's
+// depth is the number of its keys <= tau.  Keys are unique and ascend with d
+// in every request (P never grows with d), so the kept keys are a prefix of
+// every request and exactly keep in all.
 #include <climits>
 #include <cstdint>
 
@@ -76,42 +77,46 @@ __device__ __forceinline__ int block_excl_scan_int(int v, int *warp_tot /* [32] 
 __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    const int Np = p.Bp * p.Kp;
-    uint64_t *ka = reinterpret_cast<uint64_t *>(dsm);
-    uint64_t *kb = ka + Np;
-    int *depth_s = reinterpret_cast<int *>(kb + Np);
-    int *kmax_s = depth_s + p.Bp;
-    float *conf_s = reinterpret_cast<float *>(kmax_s + p.Bp);
+    const int n = p.B * p.Kmax;         // candidate keys, stored position-major: [d][request]
+    const int cs = p.Kmax | 1;          // odd row stride of the staged confidences: no bank conflicts
+    uint64_t *keys = reinterpret_cast<uint64_t *>(dsm);
+    int *depth_s = reinterpret_cast<int *>(keys + n);
+    int *kmax_s = depth_s + p.B;
+    float *conf_s = reinterpret_cast<float *>(kmax_s + p.B);  // [B][cs]
+    __shared__ int hist[256];
     __shared__ int warp_tot[33];
-    __shared__ int s_elig;
+    __shared__ int s_elig, s_bucket, s_below, s_count;
 
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0)
         s_elig = 0;
     // stage the inputs with coalesced loads (one round trip), then work from
     // shared memory
-    for (int r = tid; r < p.Bp; r += kDcutThreads) {
+    for (int r = tid; r < p.B; r += kDcutThreads) {
         depth_s[r] = 0;
-        kmax_s[r] = r < p.B ? __ldg(p.kmax + r) : 0;
+        kmax_s[r] = __ldg(p.kmax + r);
     }
-    for (int k = tid; k < p.B * p.Kmax; k += kDcutThreads)
-        conf_s[k] = __ldg(p.conf + k);
+    for (int k = tid; k < n; k += kDcutThreads)
+        conf_s[(k / p.Kmax) * cs + k % p.Kmax] = __ldg(p.conf + k);
     __syncthreads();
 
-    // 1. prefix products (fp32, left to right) -> keys; validate inputs
+    // 1. prefix products (fp32, left to right) -> keys; validate inputs.  A
+    // key orders candidates by (P desc, request asc, depth asc): high word
+    // 0x3F800000 - bits(P) (P in [0, 1]), low word request * Kmax + depth - 1;
+    // a position past kmax gets a key above every real one.
     int bad = 0, elig = 0;
-    for (int r = tid; r < p.Bp; r += kDcutThreads) {
+    for (int r = tid; r < p.B; r += kDcutThreads) {
         int km = kmax_s[r];
         if (km < 0 || km > p.Kmax) {
             bad = 1;
             km = 0;
         }
         float P = 1.f;
-        for (int d = 1; d <= p.Kp; ++d) {
-            const uint64_t lo = (uint32_t)(r * p.Kp + (d - 1));
+        for (int d = 1; d <= p.Kmax; ++d) {
+            const uint64_t lo = (uint32_t)(r * p.Kmax + (d - 1));
             uint64_t key;
             if (d <= km) {
-                float c = conf_s[r * p.Kmax + (d - 1)];
+                float c = conf_s[r * cs + (d - 1)];
                 if (!(c >= 0.f && c <= 1.f)) {
                     bad = 1;
                     c = 0.f;
@@ -120,9 +125,9 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
                 key = ((uint64_t)(0x3F800000u - __float_as_uint(P)) << 32) | lo;
                 elig += P >= p.min_gain;
             } else {
-                key = (0xFFFFFFFFull << 32) | lo;  // not a candidate: sorts last
+                key = (0xFFFFFFFFull << 32) | lo;  // not a candidate
             }
-            ka[r * p.Kp + (d - 1)] = key;
+            keys[(d - 1) * p.B + r] = key;
         }
     }
     bad = __syncthreads_or(bad);
@@ -140,36 +145,76 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
     }
     if (elig)
         atomicAdd(&s_elig, elig);
+    __syncthreads();
 
-    // 2. merge sorted runs of length L pairwise until one run remains
-    uint64_t *src = ka, *dst = kb;
-    for (int L = p.Kp; L < Np; L <<= 1) {
-        for (int e = tid; e < Np; e += kDcutThreads) {
-            const int run = e / L;
-            const int pos = e - run * L;
-            const uint64_t key = src[e];
-            const uint64_t *other = src + (size_t)((run ^ 1) * L);
-            int lo = 0, hi = L;
-            while (lo < hi) {
-                const int mid = (lo + hi) >> 1;
-                if (other[mid] < key)
-                    lo = mid + 1;
-                else
-                    hi = mid;
-            }
-            dst[(run & ~1) * L + pos + lo] = key;
-        }
-        __syncthreads();
-        uint64_t *t = src;
-        src = dst;
-        dst = t;
-    }
-
-    // 3. keep the first min(budget, eligible) keys; count them per request
+    // 2. the keep-th smallest key tau (keep = min(budget, eligible)) by a
+    // most-significant-digit radix select, 8 bits a pass; it stops once the
+    // keys sharing the digits found so far are exactly the ones still needed.
+    // Keys are distinct, so exactly `keep` keys are <= tau, and since P never
+    // grows with depth they are a prefix of every request.
     const int keep = min(p.budget, s_elig);
-    for (int t = tid; t < keep; t += kDcutThreads) {
-        const uint32_t lo = (uint32_t)src[t];
-        atomicAdd(&depth_s[lo / (uint32_t)p.Kp], 1);
+    uint64_t tau = 0;
+    if (keep > 0) {
+        uint64_t prefix = 0, mask = 0;
+        int remaining = keep;  // rank of tau among the keys matching prefix
+        tau = ~0ull;
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            for (int q = tid; q < 256; q += kDcutThreads)
+                hist[q] = 0;
+            __syncthreads();
+            for (int e = tid; e < n; e += kDcutThreads) {
+                const uint64_t k = keys[e];
+                if ((k & mask) == prefix)
+                    atomicAdd(&hist[(k >> shift) & 255], 1);
+            }
+            __syncthreads();
+            if (warp == 0) {  // the digit holding the remaining-th key: lane l holds digits 8l..8l+7
+                int c[8], sum = 0;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    c[q] = hist[lane * 8 + q];
+                    sum += c[q];
+                }
+                int incl = sum;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o)
+                        incl += v;
+                }
+                const int excl = incl - sum;
+                if (excl < remaining && remaining <= incl) {
+                    int run = excl;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (run + c[q] >= remaining) {
+                            s_bucket = lane * 8 + q;
+                            s_below = run;
+                            s_count = c[q];
+                            break;
+                        }
+                        run += c[q];
+                    }
+                }
+            }
+            __syncthreads();
+            remaining -= s_below;
+            prefix |= (uint64_t)s_bucket << shift;
+            mask |= 0xFFull << shift;
+            const bool done = s_count == remaining;  // every key matching prefix is taken
+            __syncthreads();  // s_* are read before the next pass writes them
+            if (done) {
+                tau = prefix | ~mask;
+                break;
+            }
+            tau = prefix;
+        }
+        // 3. depth of each request: its keys <= tau
+        for (int e = tid; e < n; e += kDcutThreads) {
+            const uint64_t k = keys[e];
+            if (k <= tau)
+                atomicAdd(&depth_s[(int)((uint32_t)k / (uint32_t)p.Kmax)], 1);
+        }
     }
     __syncthreads();
 
@@ -189,7 +234,7 @@ __global__ void __launch_bounds__(kDcutThreads) dcut_kernel(const DcutParams p)
             float P = 1.f;
             double e = 0.0;
             for (int d = 1; d <= depth_s[r]; ++d) {
-                P = __fadd_rn(__fmul_rn(P, conf_s[r * p.Kmax + (d - 1)]), 0.f);
+                P = __fadd_rn(__fmul_rn(P, conf_s[r * cs + (d - 1)]), 0.f);
                 e += (double)P;
             }
             p.out_expected[r] = (float)e;
@@ -211,7 +256,7 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 {
     static cudaError_t once = cudaFuncSetAttribute(
         dcut_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        2 * 8 * kDcutMaxCand + 8 * kMaxBatch + 4 * kDcutMaxCand);
+        8 * kDcutMaxCand + 8 * kMaxBatch + 4 * (kDcutMaxCand + kMaxBatch));
     if (once != cudaSuccess)
         return once;
     DcutParams p{};
@@ -228,8 +273,8 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
     p.out_expected = a.out_expected;
     const WsLayout L = ws_layout(0, 0, 0);
     p.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
-    const size_t smem = 2 * sizeof(uint64_t) * (size_t)p.Bp * p.Kp + 8 * (size_t)p.Bp +
-                        4 * (size_t)p.B * p.Kmax;
+    const size_t smem = sizeof(uint64_t) * (size_t)a.B * a.Kmax + 8 * (size_t)a.B +
+                        4 * (size_t)a.B * (a.Kmax | 1);
     tr.begin(s);
     dcut_kernel<<<1, kDcutThreads, smem, s>>>(p);
     cudaError_t e = cudaGetLastError();

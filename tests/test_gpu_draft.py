@@ -129,6 +129,27 @@ def test_draft_sample_errors():
     assert np.all(got_t[:6] >= 0) and np.all(got_t[9:] >= 0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_draft_sample_degenerate_rows(dtype):
+    """V = 1 (the only token, q = 1); rows with most entries masked; an
+    all-masked row is an error for that row only."""
+    d, kmax, u = _inputs(3, 2, 1, dtype, seed=41, full=True)
+    got_t, got_c, st = _run(d, kmax, u, 3, 2, 1, 1.0)
+    assert st == sv.SPEC_OK
+    assert np.all(got_t == 0) and np.allclose(got_c, 1.0, rtol=1e-6)
+    B, Kmax, V = 2, 2, 5000
+    d, kmax, u = _inputs(B, Kmax, V, dtype, seed=42, full=True)
+    g = torch.Generator().manual_seed(43)
+    d[torch.rand(d.shape, generator=g) < 0.999] = float("-inf")  # about 5 live entries per row
+    d[1, :] = float("-inf")                                     # request 0, position 1: nothing live
+    got_t, got_c, st = _run(d, kmax, u, B, Kmax, V, 0.8)
+    assert st == sv.SPEC_ERR_NONFINITE
+    assert got_t[1] == -1 and np.isnan(got_c[1])
+    ost, want_t, want_c = O.draft_sample(d, kmax, Kmax, 0.8, u)
+    assert ost == O.ERR_NONFINITE
+    _compare(d, u, 0.8, got_t, got_c, want_t, want_c, rows=[0, 2, 3])
+
+
 def test_draft_sample_empty_and_host_checks():
     v = Verifier(1, 2, 100)
     t = torch.zeros(1, dtype=torch.int32, device="cuda")

@@ -397,6 +397,29 @@ def test_dcut_random_against_oracle():
     assert v.device_status() == sv.SPEC_OK
 
 
+@pytest.mark.parametrize("B,Kmax", [(256, 32), (4096, 2), (1000, 8), (37, 5)])
+def test_dcut_large_against_oracle(B, Kmax):
+    """Many candidates per thread (up to SPEC_DCUT_MAX_CANDIDATES), exact ties
+    across requests, budgets below, at and above the eligible count."""
+    rng = np.random.default_rng(B * 100 + Kmax)
+    v = Verifier(B, B, 1)
+    kmax = rng.integers(0, Kmax + 1, size=B).astype(np.int32)
+    for ties in (False, True):
+        conf = (rng.beta(8, 2, size=(B, Kmax)) * 0.95 ** np.arange(Kmax)).astype(np.float32)
+        if ties:
+            conf = (0.5 ** rng.integers(0, 3, size=(B, Kmax))).astype(np.float32)
+        total = int(kmax.sum())
+        for budget in (0, 1, total // 3, total, total + 7):
+            for min_gain in (0.0, 0.3):
+                d = v.dcut(torch.from_numpy(conf).cuda(), torch.from_numpy(kmax).cuda(), budget,
+                           min_gain)
+                o = O.dcut_allocate(conf, kmax, budget, min_gain)
+                assert o.status == O.OK
+                assert d["depth"].cpu().numpy()[:B].tolist() == o.depth.tolist(), (budget, ties)
+                assert d["cu"].cpu().numpy().tolist() == o.cu.tolist(), (budget, ties)
+    assert v.device_status() == sv.SPEC_OK
+
+
 def test_dcut_golden_on_gpu():
     v = Verifier(4, 4, 1)
     for case in json.load(open(os.path.join(GOLDEN, "dcut_ties.json")))["cases"]:
