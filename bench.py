@@ -3,6 +3,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mtp|block|block_greedy|dcut|tiny]
     python bench.py --workload draft|draft_greedy   (the drafter's step: spec_draft_sample)
+    python bench.py --workload confidence           (spec_draft_confidence on the drafter rows)
+    python bench.py --workload dcut_cost            (dcut_allocate_cost + verification)
     python bench.py --impl reference ...     (the CPU oracle, timed on the host cores)
 
 One step = one pass of the whole verification path over one batch whose
@@ -51,8 +53,16 @@ WORKLOADS = {  # name -> (workload, temperature)
     # the padded drafter rows (spec_draft_sample); its own metric
     "draft": (W.BLOCK, 0.7),
     "draft_greedy": (W.BLOCK, 0.0),
+    # prefix confidence q(x) of the drafted tokens from the same drafter rows
+    "confidence": (W.BLOCK, 0.7),
+    "dcut_cost": (W.DCUT, 1.0),
 }
-DRAFT_WORKLOADS = ("draft", "draft_greedy")
+DRAFT_WORKLOADS = ("draft", "draft_greedy", "confidence")
+# the D-cut workload with the cost-unit scheduler (dcut_allocate_cost) in place
+# of the token-budget one: requests are admitted while their summed latency
+# cost stays within DCUT_MAX_COST units
+COST_WORKLOADS = ("dcut_cost",)
+DCUT_MAX_COST = 96.0
 DRAFT_METRIC = "drafted positions/sec and achieved HBM GB/s (fraction of peak) at 1 B300"
 # the sources of each roofline kernel: a recorded ncu traffic figure holds
 # only while these hash the same
@@ -195,6 +205,32 @@ def read_stream_reference(nbytes: int, device, reps: int = 20) -> float:
     return 2 * n / sec / 1e9
 
 
+def max_depth_per_cost(kmax: int) -> float:
+    """max over d = 1..kmax of d / cost(d), cost the cost-unit scheduler's
+    latency table {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0} interpolated
+    linearly and clamped at its ends."""
+    dep, lat = (1, 2, 4, 8, 16), (1.0, 1.2, 1.5, 2.0, 3.0)
+
+    def cost(d):
+        if d <= dep[0]:
+            return lat[0]
+        if d >= dep[-1]:
+            return lat[-1]
+        for k in range(4):
+            if dep[k] <= d <= dep[k + 1]:
+                return lat[k] + (d - dep[k]) / (dep[k + 1] - dep[k]) * (lat[k + 1] - lat[k])
+    return max(d / cost(d) for d in range(1, max(1, kmax) + 1))
+
+
+def inputs_sha256(tensors) -> str:
+    """SHA-256 over the bytes of the given tensors (host copies), in order:
+    a fingerprint of the synthetic inputs a run measured."""
+    h = hashlib.sha256()
+    for t in tensors:
+        h.update(t.detach().contiguous().view(torch.uint8).cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
 def replay_percentiles(events, steps_per_replay):
     """Median, p10 and p90 of the per-step time (ms) over the timed graph
     replays (events recorded between replays, none inside a graph)."""
@@ -209,8 +245,10 @@ def replay_percentiles(events, steps_per_replay):
             "p10": pct(0.1), "p90": pct(0.9)}
 
 
-def workload_desc(w, T):
-    return f"{W.describe(w)}, T={T}"
+def workload_desc(w, T, name=None):
+    extra = (f", cost-unit D-cut (dcut_allocate_cost, max_cost {DCUT_MAX_COST})"
+             if name in COST_WORKLOADS else "")
+    return f"{W.describe(w)}, T={T}{extra}"
 
 
 def l2_bytes(device) -> int:
@@ -354,7 +392,12 @@ def run_ours(args, dist):
     sampler = ClockSampler(device, enabled=not args.no_clocks)
     dist.init("nccl")
     w, T = WORKLOADS[args.workload]
-    rows = W.max_target_rows(w)
+    is_cost = args.workload in COST_WORKLOADS
+    # host bound on target rows for the cost scheduler: an admitted depth d
+    # costs cost(d) units, so the admitted depths sum to at most
+    # max_cost * max_d d / cost(d)
+    rows = (min(w.B * (w.kmax + 1), int(DCUT_MAX_COST * max_depth_per_cost(w.kmax)) + w.B)
+            if is_cost else W.max_target_rows(w))
     is_dcut = bool(w.kmax)
     v = Verifier(w.B, rows, w.V, device=device)
 
@@ -363,8 +406,15 @@ def run_ours(args, dist):
         s = {}
         if is_dcut:
             prob = W.make_dcut_problem(w, device, rep=rep)
-            d = v.dcut(prob.conf, prob.kmax, prob.budget)
-            depth = d["depth"].cpu()
+            if is_cost:
+                depth_d = torch.empty(w.B, dtype=torch.int32, device=device)
+                cu_d = torch.empty(w.B + 1, dtype=torch.int32, device=device)
+                sv.check(sv.dcut_allocate_cost(prob.conf, prob.kmax, w.B, w.kmax, DCUT_MAX_COST,
+                                               depth_d, cu_d, None, v.workspace), "dcut_cost")
+                depth = depth_d.cpu()
+            else:
+                d = v.dcut(prob.conf, prob.kmax, prob.budget)
+                depth = d["depth"].cpu()
             b = W.make_verify_batch(w, T, device, rep=rep, depths=depth, draft_stride=w.kmax)
             if b.target_logits.shape[0] < rows:  # pad to the host bound
                 t = torch.zeros((rows, w.V), dtype=b.target_logits.dtype, device=device)
@@ -396,8 +446,12 @@ def run_ours(args, dist):
             if trace_dcut is not None:
                 sv.spec_set_trace(trace_dcut)
             d = s["dcut_out"]
-            sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax, s["prob"].budget, 0.0,
-                             d["depth"], d["cu"], d["expected"], v.workspace)
+            if is_cost:
+                sv.dcut_allocate_cost(s["prob"].conf, s["prob"].kmax, w.B, w.kmax, DCUT_MAX_COST,
+                                      d["depth"], d["cu"], None, v.workspace)
+            else:
+                sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax, s["prob"].budget,
+                                 0.0, d["depth"], d["cu"], d["expected"], v.workspace)
             cu = d["cu"]
         if trace_verify is not None:
             sv.spec_set_trace(trace_verify)
@@ -544,7 +598,8 @@ def run_ours(args, dist):
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": workload_desc(w, T), "B": w.B, "V": w.V, "logits_dtype": w.dtype,
+            "workload": workload_desc(w, T, args.workload), "B": w.B, "V": w.V,
+            "logits_dtype": w.dtype,
             "temperature": T, "verified_positions_per_step": positions,
             "target_rows_per_step": batch0.n_target_rows,
             "l2": f"inputs rotate through {n_sets} independent sets "
@@ -552,6 +607,11 @@ def run_ours(args, dist):
             "timing": f"CUDA graphs of {G} steps replayed, CUDA events on the launching stream;"
                       " per-kernel times from a traced replay",
             "parallelism": f"{dist.world} GPU(s), independent batches per GPU",
+            "inputs_sha256": inputs_sha256(
+                [batch0.target_logits, batch0.draft_logits, batch0.draft_tokens, batch0.cu_draft,
+                 batch0.u_accept, batch0.u_final]
+                + ([first["prob"].conf, first["prob"].kmax] if is_dcut else [])),
+            "torch": torch.__version__,
         },
         "requests_per_s": dist.sum(w.B * K, device) / (elapsed_ms_max / 1e3),
         "hbm_gbs_step": step_gbs,
@@ -567,7 +627,8 @@ def run_ours(args, dist):
         "kernels_us": {"stream_kernel": rows_mean,
                        ("finish_greedy_kernel" if T == 0 else "finish_sample_kernel"):
                            statistics.mean(finish_us),
-                       "dcut_kernel": statistics.mean(dcut_us) if dcut_us else None,
+                       ("dcut_cost_kernel" if is_cost else "dcut_kernel"):
+                           statistics.mean(dcut_us) if dcut_us else None,
                        "note": "from one traced replay of the step graph after the timed "
                                "region (events between kernels)",
                        "traced_ms_per_step": traced_ms_per_step},
@@ -612,9 +673,14 @@ def run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist)
             s["prob"].conf.copy_(hs["conf"], non_blocking=True)
             s["prob"].kmax.copy_(hs["kmax"], non_blocking=True)
             d = s["dcut_out"]
-            sv.check(sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax,
-                                      s["prob"].budget, 0.0, d["depth"], d["cu"],
-                                      d["expected"], v.workspace), "dcut")
+            if args.workload in COST_WORKLOADS:
+                sv.check(sv.dcut_allocate_cost(s["prob"].conf, s["prob"].kmax, w.B, w.kmax,
+                                               DCUT_MAX_COST, d["depth"], d["cu"], None,
+                                               v.workspace), "dcut_cost")
+            else:
+                sv.check(sv.dcut_allocate(s["prob"].conf, s["prob"].kmax, w.B, w.kmax,
+                                          s["prob"].budget, 0.0, d["depth"], d["cu"],
+                                          d["expected"], v.workspace), "dcut")
             cu = d["cu"]
         o = s["out"]
         if T == 0:
@@ -662,16 +728,20 @@ def draft_inputs(w, T, device, rep):
     return {"draft": b.draft_logits, "kmax": kmax, "u": u}
 
 
-def oracle_draft_rows(orc, d, u, T, rows):
-    """The oracle's draws for the given rows (each row drawn on its own)."""
+def oracle_draft_rows(orc, d, u, T, rows, tokens=None):
+    """The oracle on the given rows (each row on its own): drawn tokens, or
+    with `tokens` the confidence q(x) of those drafted tokens."""
     n = len(rows)
-    st, tok, conf = orc.draft_sample(d[rows], np.ones(n, np.int32), 1, T, u[rows])
+    if tokens is None:
+        st, tok, conf = orc.draft_sample(d[rows], np.ones(n, np.int32), 1, T, u[rows])
+    else:
+        st, conf = orc.draft_confidence(d[rows], tokens[rows], np.ones(n, np.int32), T)
     if st != orc.OK:
         raise RuntimeError(f"oracle status {st}")
     return n
 
 
-def oracle_draft_rate(d, u, T, seconds, threads, rows_per_call=4):
+def oracle_draft_rate(d, u, T, seconds, threads, rows_per_call=4, tokens=None):
     import oracle as orc
     orc.load()
     n_rows = d.shape[0]
@@ -683,7 +753,7 @@ def oracle_draft_rate(d, u, T, seconds, threads, rows_per_call=4):
             chunks = [[(i + k * rows_per_call + j) % n_rows for j in range(rows_per_call)]
                       for k in range(threads)]
             i += threads * rows_per_call
-            done += sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r), chunks))
+            done += sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r, tokens), chunks))
             if time.perf_counter() - t0 >= seconds:
                 break
     el = time.perf_counter() - t0
@@ -715,18 +785,26 @@ def run_draft(args, dist):
         s = draft_inputs(w, T, device, rep)
         s["tokens"] = torch.empty(n_rows, dtype=torch.int32, device=device)
         s["conf"] = torch.empty(n_rows, dtype=torch.float32, device=device)
+        if args.workload == "confidence":  # the drafted tokens whose q(x) is asked
+            s["drafted"] = W.make_verify_batch(w, T, device, rep=rep).draft_tokens
         return s
 
     first = make_set(rank_seed_offset(dist.rank))
     n_sets = max(2, min(64, math.ceil(2.2 * l2_bytes(device) / alg_bytes)))
     sets = [first] + [make_set(rank_seed_offset(dist.rank) + r) for r in range(1, n_sets)]
 
+    is_conf = args.workload == "confidence"
+
     def step(s, trace=None):
         if trace is not None:
             sv.spec_set_trace(trace)
-        st = sv.spec_draft_sample(s["draft"], s["kmax"], w.B, Kmax, w.V, T,
-                                  None if T == 0 else s["u"], s["tokens"], s["conf"],
-                                  v.workspace)
+        if is_conf:  # q(x) of drafted tokens (the drawn ones of set s, fixed inputs here)
+            st = sv.spec_draft_confidence(s["draft"], s["drafted"], s["kmax"], w.B, Kmax, w.V, T,
+                                          s["conf"], v.workspace)
+        else:
+            st = sv.spec_draft_sample(s["draft"], s["kmax"], w.B, Kmax, w.V, T,
+                                      None if T == 0 else s["u"], s["tokens"], s["conf"],
+                                      v.workspace)
         if trace is not None:
             sv.spec_set_trace(None)
         return st
@@ -743,8 +821,14 @@ def run_draft(args, dist):
     stream = torch.cuda.Stream(device)
 
     # T > 0: one kernel reads and draws (draft_sample_kernel); T = 0: the
-    # streaming pass, then the per-row argmax merge
-    kernels = ["draft_sample_kernel"] if T > 0 else ["stream_kernel", "draft_greedy_kernel"]
+    # streaming pass, then the per-row argmax merge; confidence: the streaming
+    # pass, then the per-row q(x)
+    if args.workload == "confidence":
+        kernels = ["stream_kernel", "confidence_kernel"]
+    elif T > 0:
+        kernels = ["draft_sample_kernel"]
+    else:
+        kernels = ["stream_kernel", "draft_greedy_kernel"]
 
     def capture(n_steps, offset, traced):
         evs = []
@@ -813,7 +897,8 @@ def run_draft(args, dist):
     e2e = None
     if not args.no_e2e:
         steps = max(1, min(args.e2e_steps, K))
-        host = [{n: sets[k][n].cpu().pin_memory() for n in ("draft", "kmax", "u")}
+        in_names = ("draft", "kmax", "drafted") if is_conf else ("draft", "kmax", "u")
+        host = [{n: sets[k][n].cpu().pin_memory() for n in in_names}
                 for k in range(min(n_sets, 3))]
         out_t = torch.empty(n_rows, dtype=torch.int32).pin_memory()
         out_c = torch.empty(n_rows, dtype=torch.float32).pin_memory()
@@ -823,7 +908,7 @@ def run_draft(args, dist):
 
         def one(k):
             s, hs = sets[k % len(host)], host[k % len(host)]
-            for n in ("draft", "kmax", "u"):
+            for n in in_names:
                 s[n].copy_(hs[n], non_blocking=True)
             sv.check(step(s), "draft step")
             out_t.copy_(s["tokens"], non_blocking=True)
@@ -850,8 +935,9 @@ def run_draft(args, dist):
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
         hd, hu = host_draft(first["draft"]), host_draft(first["u"])
-        rate, n, el = oracle_draft_rate(hd, hu, T, args.cpu_seconds, threads)
-        rate1, n1, el1 = oracle_draft_rate(hd, hu, T, args.cpu_seconds / 3, 1)
+        ht = host_draft(first["drafted"]) if is_conf else None
+        rate, n, el = oracle_draft_rate(hd, hu, T, args.cpu_seconds, threads, tokens=ht)
+        rate1, n1, el1 = oracle_draft_rate(hd, hu, T, args.cpu_seconds / 3, 1, tokens=ht)
         cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n} drafter rows of input set 0 ({workload_desc(w, T)}), drawn by "
                          f"the oracle 4 rows per call on {threads} host threads, {el:.1f} s",
@@ -864,7 +950,8 @@ def run_draft(args, dist):
         "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {
-            "workload": f"drafter step of {workload_desc(w, T)}: {n_rows} rows, Kmax={Kmax}",
+            "workload": (f"{'prefix confidence q(x) of the drafted tokens' if is_conf else 'drafter step'}"
+                         f" of {workload_desc(w, T)}: {n_rows} rows, Kmax={Kmax}"),
             "B": w.B, "Kmax": Kmax, "V": w.V, "logits_dtype": w.dtype, "temperature": T,
             "drafted_positions_per_step": n_rows,
             "l2": f"inputs rotate through {n_sets} independent sets "
@@ -872,6 +959,10 @@ def run_draft(args, dist):
             "timing": f"CUDA graphs of {G} steps replayed, CUDA events on the launching stream;"
                       " per-kernel times from a traced replay",
             "parallelism": f"{dist.world} GPU(s), independent batches per GPU",
+            "inputs_sha256": inputs_sha256(
+                [first["draft"], first["kmax"]]
+                + ([first["drafted"]] if is_conf else ([first["u"]] if T > 0 else []))),
+            "torch": torch.__version__,
         },
         "hbm_gbs_step": step_gbs,
         "hbm_frac_step": step_gbs / peak,
@@ -898,10 +989,12 @@ def run_reference_draft(args, dist):
     w, T = WORKLOADS[args.workload]
     s = draft_inputs(w, T, "cpu", 0)
     d, u = host_draft(s["draft"]), host_draft(s["u"])
+    tok = (host_draft(W.make_verify_batch(w, T, "cpu", rep=0).draft_tokens)
+           if args.workload == "confidence" else None)
     n_rows = d.shape[0]
     threads = os.cpu_count() or 1
     t0 = time.perf_counter()
-    oracle_draft_rows(orc, d, u, T, [0])
+    oracle_draft_rows(orc, d, u, T, [0], tok)
     t_row = max(time.perf_counter() - t0, 1e-5)
     per_step = args.reference_seconds / max(1, args.steps + args.warmup)
     n = int(max(threads, min(n_rows, per_step * threads / t_row)))
@@ -910,7 +1003,7 @@ def run_reference_draft(args, dist):
     def one(k):
         rows = [(k * n + j) % n_rows for j in range(n)]
         chunks = [rows[c::threads] for c in range(threads) if rows[c::threads]]
-        return sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r), chunks))
+        return sum(ex.map(lambda r: oracle_draft_rows(orc, d, u, T, r, tok), chunks))
 
     for k in range(args.warmup):
         one(k)
@@ -921,7 +1014,9 @@ def run_reference_draft(args, dist):
     el = time.perf_counter() - t0
     ex.shutdown()
     value = done / el
-    desc = f"drafter step of {workload_desc(w, T)}: {n_rows} rows"
+    what = ("prefix confidence q(x) of the drafted tokens" if args.workload == "confidence"
+            else "drafter step")
+    desc = f"{what} of {workload_desc(w, T)}: {n_rows} rows"
     print(json.dumps({
         "impl": "reference", "metric": DRAFT_METRIC, "value": value, "unit": UNIT,
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
@@ -951,7 +1046,10 @@ def run_reference(args, dist):
     w, T = WORKLOADS[args.workload]
     if w.kmax:
         prob = W.make_dcut_problem(w, "cpu")
-        o = orc.dcut_allocate(prob.conf.numpy(), prob.kmax.numpy(), prob.budget)
+        if args.workload in COST_WORKLOADS:
+            o = orc.dcut_schedule_cost(prob.conf.numpy(), prob.kmax.numpy(), DCUT_MAX_COST)
+        else:
+            o = orc.dcut_allocate(prob.conf.numpy(), prob.kmax.numpy(), prob.budget)
         batch = W.make_verify_batch(w, T, "cpu", depths=torch.from_numpy(o.depth),
                                     draft_stride=w.kmax)
     else:
@@ -984,7 +1082,7 @@ def run_reference(args, dist):
         "n_gpus": dist.world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": el * 1e3 / max(1, args.steps), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(w, T), "B": w.B, "V": w.V,
+        "config": {"workload": workload_desc(w, T, args.workload), "B": w.B, "V": w.V,
                    "logits_dtype": w.dtype, "temperature": T,
                    "sample_per_step": f"{n_req} of {w.B} requests"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
