@@ -342,37 +342,87 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     int *best_d = reinterpret_cast<int *>(benefit + p.B);
     int *order = best_d + p.B;  // request at each rank
     int *depth = order + p.B;
+    __shared__ double cost_tab[kMaxDraft + 1];  // cost(d), d = 1..Kmax
     __shared__ int s_ncand;
-    const int tid = threadIdx.x;
+    __shared__ int warp_tot[33];
+    const int tid = threadIdx.x, lane = tid & 31;
     if (tid == 0)
         s_ncand = 0;
+    if (tid >= 1 && tid <= kMaxDraft)
+        cost_tab[tid] = latency_cost(tid);
+    for (int r = tid; r < p.B; r += kCostThreads)
+        depth[r] = 0;
     __syncthreads();
 
-    // 1. best depth per request; inputs validated on the way
+    // 1. best depth per request; inputs validated on the way.  With at most
+    // one (request, depth) pair per thread, each pair is its own thread (the
+    // prefix product recomputed left to right, one division), and a group of
+    // Kp lanes keeps the first maximum; otherwise a thread walks a request.
+    int Kp = 1;
+    while (Kp < p.Kmax)
+        Kp <<= 1;
     int bad = 0, ncand = 0;
-    for (int r = tid; r < p.B; r += kCostThreads) {
-        int km = __ldg(p.kmax + r);
-        if (km < 0 || km > p.Kmax) {
-            bad = 1;
-            km = 0;
-        }
-        double P = 1.0, best = -1.0;
-        int bd = 0;
-        for (int d = 1; d <= km; ++d) {
-            const float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
-            if (!(c >= 0.f && c <= 1.f))
+    if ((int64_t)p.B * Kp <= kCostThreads) {
+        const int r = tid / Kp, d = tid % Kp + 1;
+        int km = 0;
+        double b = -1.0;
+        if (r < p.B) {
+            km = __ldg(p.kmax + r);
+            if (km < 0 || km > p.Kmax) {
                 bad = 1;
-            P = __dmul_rn(P, (double)c);
-            const double b = __ddiv_rn(__dmul_rn(P, (double)d), latency_cost(d));
-            if (b > best) {
-                best = b;
-                bd = d;
+                km = 0;
+            }
+            if (d <= km) {
+                double P = 1.0;
+                for (int j = 0; j < d; ++j) {
+                    const float c = __ldg(p.conf + (int64_t)r * p.Kmax + j);
+                    if (!(c >= 0.f && c <= 1.f))
+                        bad = 1;
+                    P = __dmul_rn(P, (double)c);
+                }
+                b = __ddiv_rn(__dmul_rn(P, (double)d), cost_tab[d]);
             }
         }
-        benefit[r] = km > 0 ? best : -1.0;
-        best_d[r] = bd;
-        depth[r] = 0;
-        ncand += km > 0;
+        // the group's first maximum: larger benefit, then smaller depth
+        double bb = b;
+        int bd = b >= 0.0 ? d : 0;
+        for (int o = Kp >> 1; o > 0; o >>= 1) {
+            const double ob = __shfl_xor_sync(0xffffffffu, bb, o);
+            const int od = __shfl_xor_sync(0xffffffffu, bd, o);
+            if (ob > bb || (ob == bb && od != 0 && (bd == 0 || od < bd))) {
+                bb = ob;
+                bd = od;
+            }
+        }
+        if (r < p.B && d == 1) {
+            benefit[r] = km > 0 ? bb : -1.0;
+            best_d[r] = bd;
+            ncand += km > 0;
+        }
+    } else {
+        for (int r = tid; r < p.B; r += kCostThreads) {
+            int km = __ldg(p.kmax + r);
+            if (km < 0 || km > p.Kmax) {
+                bad = 1;
+                km = 0;
+            }
+            double P = 1.0, best = -1.0;
+            int bd = 0;
+            for (int d = 1; d <= km; ++d) {
+                const float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
+                if (!(c >= 0.f && c <= 1.f))
+                    bad = 1;
+                P = __dmul_rn(P, (double)c);
+                const double b = __ddiv_rn(__dmul_rn(P, (double)d), cost_tab[d]);
+                if (b > best) {
+                    best = b;
+                    bd = d;
+                }
+            }
+            benefit[r] = km > 0 ? best : -1.0;
+            best_d[r] = bd;
+            ncand += km > 0;
+        }
     }
     bad = __syncthreads_or(bad);
     if (bad) {
@@ -404,13 +454,12 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     }
     __syncthreads();
 
-    // 3. admission in rank order (sequential by definition)
+    // 3. admission in rank order (sequential by definition; costs from the table)
     if (tid == 0) {
         double total = 0.0;
         for (int t = 0; t < s_ncand; ++t) {
             const int r = order[t];
-            const double c = latency_cost(best_d[r]);
-            const double nt = __dadd_rn(total, c);
+            const double nt = __dadd_rn(total, cost_tab[best_d[r]]);
             if (nt <= p.max_cost) {
                 total = nt;
                 depth[r] = best_d[r];
@@ -419,20 +468,24 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     }
     __syncthreads();
 
-    // 4. depths, offsets, benefits of the admitted requests
-    if (tid == 0) {
-        int off = 0;
-        for (int r = 0; r < p.B; ++r) {
-            p.out_cu[r] = off;
-            off += depth[r];
-        }
-        p.out_cu[p.B] = off;
-    }
-    for (int r = tid; r < p.B; r += kCostThreads) {
+    // 4. depths, offsets (exclusive scan), benefits of the admitted requests
+    const int per = (p.B + kCostThreads - 1) / kCostThreads;
+    const int r0 = min(p.B, tid * per), r1 = min(p.B, r0 + per);
+    int seg = 0;
+    for (int r = r0; r < r1; ++r)
+        seg += depth[r];
+    int total = 0;
+    int off = block_excl_scan_int(seg, warp_tot, total);
+    for (int r = r0; r < r1; ++r) {
+        p.out_cu[r] = off;
+        off += depth[r];
         p.out_depth[r] = depth[r];
         if (p.out_benefit)
             p.out_benefit[r] = depth[r] > 0 ? benefit[r] : 0.0;
     }
+    if (tid == 0)
+        p.out_cu[p.B] = total;
+    (void)lane;
 }
 
 cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t s, Tracer &tr)
