@@ -339,6 +339,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
 
     // Where the unit at (row rg, column chunk q) comes from; false when the
     // row lies past the real rows (nt target, nd draft) and `check` is set.
+    int req_hint = 0;  // request of the last slot found (consecutive units share rows)
     auto locate = [&](int64_t rg, int q, const T *&src, int &len, int &col0, int64_t nt,
                       int64_t nd, bool check) -> bool {
         col0 = q * g.Q;
@@ -354,13 +355,18 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
             return false;
         int64_t row = slot;
         if (padded) {  // packed slot -> (request, position) -> padded row
-            int lo = 0, hi = B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (cu_s[mid] <= slot)
-                    lo = mid;
-                else
-                    hi = mid - 1;
+            int lo = req_hint;
+            if (!(cu_s[lo] <= slot && slot < cu_s[lo + 1])) {  // the request holding slot
+                lo = 0;
+                int hi = B - 1;
+                while (lo < hi) {
+                    const int mid = (lo + hi + 1) >> 1;
+                    if (cu_s[mid] <= slot)
+                        lo = mid;
+                    else
+                        hi = mid - 1;
+                }
+                req_hint = lo;
             }
             row = (int64_t)lo * p.draft_stride + (slot - cu_s[lo]);
         }
