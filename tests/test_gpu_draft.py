@@ -77,10 +77,10 @@ def _compare(d, u, T, got_t, got_c, want_t, want_c, rows=None):
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
 @pytest.mark.parametrize("B,Kmax,V", [
-    (2, 4, 50000),    # 8 rows: clusters of 16 CTAs
-    (5, 3, 1001),     # rows not 16-byte multiples (f32: plain loads), ragged ranges
+    (2, 4, 50000),    # 8 rows of several slices each, a short last slice
+    (5, 3, 1001),     # rows not 16-byte multiples (plain loads), one partial slice
     (16, 16, 32000),
-    (64, 8, 128000),  # 512 rows, clusters of 8
+    (64, 8, 128000),  # 512 rows, more rows than resident CTAs
 ])
 def test_draft_sample_against_oracle(B, Kmax, V, T, dtype):
     d, kmax, u = _inputs(B, Kmax, V, dtype, seed=B * 131 + Kmax * 7 + V)
