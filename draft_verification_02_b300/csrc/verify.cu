@@ -36,11 +36,15 @@
 //  - T > 0, finish_sample_kernel: one cluster of 8 or 16 CTAs per request.
 //    The request's rows are merged one or two per warp of the cluster (their
 //    (m, s) and p(x) sent to every CTA through distributed shared memory);
-//    every CTA runs the accept test and first-rejection ballot (identical
-//    bits everywhere), then stages its share of the final-draw rows with TMA
-//    and sums the weights.  The range sums are exchanged the same way; the
-//    CTA whose range holds u*S finds the token with a block scan of
-//    per-thread piece sums and one thread's walk through its piece.
+//    every warp of every CTA runs the accept test and first-rejection ballot
+//    (identical bits everywhere), then each CTA stages its share of the
+//    final-draw rows with TMA and sums the weights.  The range sums are
+//    exchanged the same way; the CTA whose range holds u*S finds the token
+//    with a block scan of per-thread piece sums, then a warp computes the
+//    chosen piece's weights and one lane walks them in order.
+// The drafter's kernels (confidence_kernel, draft_sample_kernel,
+// draft_greedy_kernel) and the acceptance statistics are launched from here
+// too; D-cut from dcut.cu.
 // Every merge runs in a fixed order, so repeated calls give identical bits.
 #include <algorithm>
 #include <cstdint>

@@ -248,11 +248,11 @@ int spec_draft_confidence(const void *draft_logits, int dtype, const int32_t *dr
  * SPEC_ERR_NONFINITE on the device; kmax outside [0, Kmax] sets
  * SPEC_ERR_INVALID_ARG there.  A draw near a CDF boundary may differ from an
  * exact-arithmetic draw by one token (fp32 weights; the float-float running
- * sums keep the error near 1e-7 of S).  T > 0: one kernel launch, one
- * cluster of 8 or 16 CTAs per row that reads the row once (each CTA keeps
- * its share in shared memory between the maximum and the draw).  T == 0: two
- * launches, the streaming pass over the B*Kmax rows and a per-row argmax
- * merge, its programmatic dependent.
+ * sums keep the error near 1e-7 of S).  T > 0: one kernel launch, one CTA
+ * per row that reads the row once, slice by slice (each slice weighed
+ * against its own power-of-two reference; the slice holding u*S is weighed
+ * again from L2 and walked).  T == 0: two launches, the streaming pass over
+ * the B*Kmax rows and a per-row argmax merge, its programmatic dependent.
  */
 int spec_draft_sample(const void *draft_logits, int dtype, const int32_t *kmax, int32_t B,
                       int32_t Kmax, int32_t V, float temperature, const float *u_draft,
