@@ -103,3 +103,31 @@ def test_reference_arm_prints_one_line(workload):
         assert k in d, k
     assert d["impl"] == "reference" and d["value"] > 0 and d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_bench_host_helpers():
+    """The bench's host-side helpers: the cost table's depth bound, replay
+    percentiles and input fingerprints."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    # d / cost(d) peaks at the largest depth: 16 / 3.0 up to Kmax = 16, then d / 3
+    assert bench.max_depth_per_cost(1) == 1.0
+    assert bench.max_depth_per_cost(16) == 16 / 3.0
+    assert bench.max_depth_per_cost(32) == 32 / 3.0
+    # d = 4 costs 1.5 (a table point), d = 3 interpolates 1.2 + 0.5 * 0.3 = 1.35
+    assert abs(bench.max_depth_per_cost(4) - 4 / 1.5) < 1e-12
+
+    class Ev:
+        def __init__(self, t):
+            self.t = t
+
+        def elapsed_time(self, other):
+            return other.t - self.t
+    ev = [Ev(t) for t in (0.0, 10.0, 30.0, 60.0, 100.0)]  # replays of 10, 20, 30, 40 ms
+    d = bench.replay_percentiles(ev, 10)
+    assert d["replays"] == 4 and d["p10"] == 1.0 and d["p90"] == 4.0 and d["median"] in (2.0, 3.0)
+    a = torch.arange(6, dtype=torch.float32)
+    b = torch.tensor([1, 2], dtype=torch.int32)
+    assert bench.inputs_sha256([a, b]) == bench.inputs_sha256([a.clone(), b.clone()])
+    assert bench.inputs_sha256([a, b]) != bench.inputs_sha256([b, a])
