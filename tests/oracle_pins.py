@@ -795,3 +795,23 @@ def pin_acceptance_stats(lib):
 
 
 ALL_PINS += [pin_draft_sample, pin_draft_sample_chi_square, pin_acceptance_stats]
+
+
+def pin_masked_in_both_rows_rejects(lib):
+    """The drafted token masked in both the target and the draft row: p = q = 0,
+    so no u in [0, 1) accepts it (the limit of min(1, p/q) with p = 0 is 0;
+    an underflowed q only accepts when p > 0).  The residual max(0, p - q) is
+    then identically zero on the uniform rows below, so the token is drawn
+    from p itself: u_final = 0.6 over p = (1/2, 1/2, 0) picks token 1."""
+    ninf = float("-inf")
+    target = np.array([[0.0, 0.0, ninf], [0.0, 0.0, ninf]], np.float32)  # rows 0 and bonus
+    draft = np.array([[0.0, 0.0, ninf]], np.float32)
+    for u in (0.0, 0.5, 0.999):
+        r = O.verify_sample(target, draft, np.array([2], np.int32), np.array([0, 1], np.int32),
+                            1.0, np.array([u], np.float32), np.array([0.6], np.float32), lib=lib)
+        assert r.status == O.OK
+        assert r.accept_len.tolist() == [0], (u, r.accept_len)
+        assert r.tokens.tolist() == [1, -1], (u, r.tokens)
+
+
+ALL_PINS += [pin_masked_in_both_rows_rejects]

@@ -67,6 +67,15 @@ MUTANTS = [
      "    *out_mean = B > 0 ? (double)total / (double)B : 0.0;"),
     ("cost variant keeps the last maximising depth", "if (b > best) { /* strict",
      "if (b >= best) { /* strict"),
+    ("an underflowed q accepts even when p is 0", "ratio = p > 0 ? INFINITY : 0.0;",
+     "ratio = INFINITY;"),
+    ("expected length counts one depth too many",
+     "            for (int32_t d = 1; d <= out_depth[i]; ++d) {\n                P = P * conf",
+     "            for (int32_t d = 1; d <= out_depth[i] + (out_depth[i] < Kmax); ++d) {\n                P = P * conf"),
+    ("cost table clamps long depths to the shortest cost", "    if (d >= dep[4])\n        return lat[4];",
+     "    if (d >= dep[4])\n        return lat[0];"),
+    ("acceptance counts the first rejection as accepted", "            if (a > j)\n                out_accepted[j] += 1;",
+     "            if (a >= j)\n                out_accepted[j] += 1;"),
     ("cost variant sorts ascending",
      "if (a->benefit > b->benefit)\n        return -1;\n    if (a->benefit < b->benefit)\n        return 1;",
      "if (a->benefit < b->benefit)\n        return -1;\n    if (a->benefit > b->benefit)\n        return 1;"),
