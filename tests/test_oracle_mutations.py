@@ -76,6 +76,8 @@ MUTANTS = [
      "    if (d >= dep[4])\n        return lat[0];"),
     ("acceptance counts the first rejection as accepted", "            if (a > j)\n                out_accepted[j] += 1;",
      "            if (a >= j)\n                out_accepted[j] += 1;"),
+    ("D-cut keeps only products strictly above min_gain", "            if (P >= min_gain)",
+     "            if (P > min_gain)"),
     ("cost variant sorts ascending",
      "if (a->benefit > b->benefit)\n        return -1;\n    if (a->benefit < b->benefit)\n        return 1;",
      "if (a->benefit < b->benefit)\n        return -1;\n    if (a->benefit > b->benefit)\n        return 1;"),
