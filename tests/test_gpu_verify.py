@@ -99,6 +99,23 @@ def test_drafted_token_masked_in_target_rejects():
     parity.compare_batch(batch, out)
 
 
+def test_drafted_token_masked_in_both_rows_rejects():
+    """p = q = 0 for the drafted token: rejected for every u (an underflowed q
+    accepts only when p > 0), then the residual is drawn as usual."""
+    b = ragged_batch(4, 2048, 1.0, "f32", seed=7, kmin=2, kmax=4)
+    b.u_accept[:] = 0.0  # the most permissive uniform still rejects
+    for i in range(4):
+        t0, d0 = int(b.cu_draft[i]) + i, int(b.cu_draft[i])
+        x = b.draft_tokens[d0].long()
+        b.target_logits[t0, x] = float("-inf")
+        b.draft_logits[d0, x] = float("-inf")
+    batch, out, v = run_gpu(b)
+    assert torch.all(out["accept_len"].cpu() == 0)
+    assert v.device_status() == sv.SPEC_OK
+    rep = parity.compare_batch(batch, out)
+    assert rep["exempt_final"] <= MAX_EXEMPT, rep
+
+
 def test_identical_rows_accept_everything():
     """q = p makes p/q = 1, so every u < 1 accepts.  The kernels sum the
     target and draft rows in different orders, so their p/q is 1 only to
