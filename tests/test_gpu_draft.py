@@ -93,6 +93,24 @@ def test_draft_sample_against_oracle(B, Kmax, V, T, dtype):
     _compare(d, u, T, got_t, got_c, want_t, want_c)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_draft_greedy_ties_take_the_lowest_index(dtype):
+    """T = 0: rows with their maximum repeated take its lowest index, as the
+    oracle (and numpy's argmax) do; rows with a NaN are errors."""
+    B, Kmax, V = 6, 4, 40000
+    g = torch.Generator().manual_seed(51)
+    d = torch.randint(-3, 3, (B * Kmax, V), generator=g).float()  # many ties everywhere
+    d[5, 31000] = 7.0
+    d[5, 12] = 7.0  # lowest of two maxima far apart
+    d = d.to(torch.bfloat16 if dtype == "bf16" else torch.float32)
+    kmax = torch.full((B,), Kmax, dtype=torch.int32)
+    got_t, got_c, st = _run(d, kmax, torch.zeros(B * Kmax), B, Kmax, V, 0.0)
+    assert st == sv.SPEC_OK
+    want = np.argmax(d.float().numpy(), axis=1)
+    assert got_t.tolist() == want.tolist() and got_t[5] == 12
+    assert np.all(got_c == 1.0)
+
+
 def test_draft_sample_follows_u():
     """Over one row drawn at many u, the tokens are non-decreasing in u and
     each token's share of a fine u grid matches q within the grid step."""
