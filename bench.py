@@ -1,7 +1,10 @@
 #!/usr/bin/env python3
 """Benchmark of batched draft verification (+ D-cut) on B300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload mtp|block|block_greedy|dcut|tiny]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload ragged17|mtp|block|...]
+                    [--temperature T]
+    python bench.py --workload ragged<k>   (the ragged sweep's pair k = 0..17, B-major;
+                                            the default is ragged17: B=128, V=151936, T=0.7)
     python bench.py --workload draft|draft_greedy   (the drafter's step: spec_draft_sample)
     python bench.py --workload confidence           (spec_draft_confidence on the drafter rows)
     python bench.py --workload dcut_cost            (dcut_allocate_cost + verification)
@@ -57,6 +60,12 @@ WORKLOADS = {  # name -> (workload, temperature)
     "confidence": (W.BLOCK, 0.7),
     "dcut_cost": (W.DCUT, 1.0),
 }
+# the ragged sweep: B in {4..128} x V in {32000, 128000, 151936}, K_i ~ U{1..16},
+# bf16; pair 17 (B=128, V=151936) is the largest single-GPU configuration and
+# the default line
+for _k in range(len(W.RAGGED_B) * len(W.RAGGED_V)):
+    WORKLOADS[f"ragged{_k}"] = (W.ragged(_k), 0.7)
+DEFAULT_WORKLOAD = "ragged17"
 DRAFT_WORKLOADS = ("draft", "draft_greedy", "confidence")
 # the D-cut workload with the cost-unit scheduler (dcut_allocate_cost) in place
 # of the token-budget one: requests are admitted while their summed latency
@@ -82,7 +91,9 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="mtp")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--temperature", type=float, default=None,
+                    help="override the workload's temperature (0 = greedy)")
     ap.add_argument("--graph-steps", type=int, default=500,
                     help="verify steps captured per CUDA graph")
     ap.add_argument("--e2e-steps", type=int, default=30)
@@ -245,6 +256,16 @@ def replay_percentiles(events, steps_per_replay):
             "p10": pct(0.1), "p90": pct(0.9)}
 
 
+def workload_of(args):
+    """(workload, temperature) of the command line."""
+    w, T = WORKLOADS[args.workload]
+    if args.temperature is not None:
+        if args.temperature < 0:
+            raise SystemExit("--temperature must be >= 0")
+        T = float(args.temperature)
+    return w, T
+
+
 def workload_desc(w, T, name=None):
     extra = (f", cost-unit D-cut (dcut_allocate_cost, max_cost {DCUT_MAX_COST})"
              if name in COST_WORKLOADS else "")
@@ -391,7 +412,7 @@ def run_ours(args, dist):
     # the sampler process starts now so that it samples well before the timed region
     sampler = ClockSampler(device, enabled=not args.no_clocks)
     dist.init("nccl")
-    w, T = WORKLOADS[args.workload]
+    w, T = workload_of(args)
     is_cost = args.workload in COST_WORKLOADS
     # host bound on target rows for the cost scheduler: an admitted depth d
     # costs cost(d) units, so the admitted depths sum to at most
@@ -399,6 +420,13 @@ def run_ours(args, dist):
     rows = (min(w.B * (w.kmax + 1), int(DCUT_MAX_COST * max_depth_per_cost(w.kmax)) + w.B)
             if is_cost else W.max_target_rows(w))
     is_dcut = bool(w.kmax)
+    # ragged depths are drawn once: every rotated set verifies the same depth
+    # vector (fresh logits and uniforms), so a step's positions and bytes are
+    # fixed and the host passes the exact row count as max_target_rows
+    depths0 = None
+    if not is_dcut and w.k is None:
+        depths0 = W.make_depths(w, "cpu", rank_seed_offset(dist.rank))
+        rows = int(depths0.sum().item()) + w.B
     v = Verifier(w.B, rows, w.V, device=device)
 
     # ---- input sets, resident in HBM
@@ -425,7 +453,7 @@ def run_ours(args, dist):
                              "cu": torch.empty(w.B + 1, dtype=torch.int32, device=device),
                              "expected": torch.empty(w.B, dtype=torch.float32, device=device)}
         else:
-            b = W.make_verify_batch(w, T, device, rep=rep)
+            b = W.make_verify_batch(w, T, device, rep=rep, depths=depths0)
         s["batch"] = b
         s["out"] = v.outputs(b, rows)
         return s
@@ -775,7 +803,7 @@ def run_draft(args, dist):
     torch.cuda.set_device(device)
     sampler = ClockSampler(device, enabled=not args.no_clocks)
     dist.init("nccl")
-    w, T = WORKLOADS[args.workload]
+    w, T = workload_of(args)
     Kmax, n_rows = w.k, w.B * w.k
     v = Verifier(w.B, w.B * (Kmax + 1), w.V, device=device)
     e = 4 if w.dtype == "f32" else 2
@@ -986,7 +1014,7 @@ def run_draft(args, dist):
 def run_reference_draft(args, dist):
     import oracle as orc
     orc.load()
-    w, T = WORKLOADS[args.workload]
+    w, T = workload_of(args)
     s = draft_inputs(w, T, "cpu", 0)
     d, u = host_draft(s["draft"]), host_draft(s["u"])
     tok = (host_draft(W.make_verify_batch(w, T, "cpu", rep=0).draft_tokens)
@@ -1043,7 +1071,7 @@ def run_reference(args, dist):
         return run_reference_draft(args, dist)
     import oracle as orc
     orc.load()
-    w, T = WORKLOADS[args.workload]
+    w, T = workload_of(args)
     if w.kmax:
         prob = W.make_dcut_problem(w, "cpu")
         if args.workload in COST_WORKLOADS:
@@ -1052,8 +1080,9 @@ def run_reference(args, dist):
             o = orc.dcut_allocate(prob.conf.numpy(), prob.kmax.numpy(), prob.budget)
         batch = W.make_verify_batch(w, T, "cpu", depths=torch.from_numpy(o.depth),
                                     draft_stride=w.kmax)
-    else:
-        batch = W.make_verify_batch(w, T, "cpu")
+    else:  # the depth vector our arm verifies on rank 0
+        batch = W.make_verify_batch(w, T, "cpu", depths=W.make_depths(w, "cpu", 0)
+                                    if w.k is None else None)
     h = host_arrays(batch)
     threads = os.cpu_count() or 1
     # size each step's sample of whole requests to the time budget

@@ -66,7 +66,7 @@ def test_reference_arm_other_ranks_exit_without_work(capsys):
     assert capsys.readouterr().out == ""
 
 
-def test_reference_arm_prints_one_line(capsys):
+def test_reference_arm_prints_one_line_in_process(capsys):
     import json
     import sys
     sys.path.insert(0, ROOT)
@@ -131,3 +131,17 @@ def test_bench_host_helpers():
     b = torch.tensor([1, 2], dtype=torch.int32)
     assert bench.inputs_sha256([a, b]) == bench.inputs_sha256([a.clone(), b.clone()])
     assert bench.inputs_sha256([a, b]) != bench.inputs_sha256([b, a])
+
+
+def test_default_workload_is_the_largest_ragged_pair():
+    """The default line is the ragged sweep's largest single-GPU pair (B=128,
+    V=151936, K_i ~ U{1..16}, T=0.7); --temperature overrides T."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args([])
+    w, T = bench.workload_of(args)
+    assert (w.B, w.V, w.k_range, w.seed, T) == (128, 151936, (1, 16), 27, 0.7)
+    w0, T0 = bench.workload_of(bench.parse_args(["--workload", "ragged0", "--temperature", "0"]))
+    assert (w0.B, w0.V, T0) == (4, 32000, 0.0)
+    assert "ragged_B128_V151936" in bench.workload_desc(w, T)
