@@ -477,6 +477,82 @@ def pin_sample_outputs_layout(lib):
                                                                      res.accept_len)
 
 
+def _ref_final_weights(t_row, d_row, T):
+    """Final-draw weights from library softmaxes: max(0, p - q) after a
+    rejection (p when that is all zero), p alone for the bonus row."""
+    p = _ref_softmax(t_row, T)
+    if d_row is None:
+        return p
+    w = np.maximum(0.0, p - _ref_softmax(d_row, T))
+    return w if w.sum() > 0 else p
+
+
+def pin_final_cdf_and_diagnostics(lib):
+    """The final draw's running sum C and the per-request diagnostic
+    {u*S, S, C(y-1), C(y)} (which decide the GPU parity exemption) against a
+    numpy cumsum of weights built from scipy softmaxes: every accepted length
+    a = 0..K of every request (a < K residual rows, a = K the bonus row, no
+    draft row), identical rows (all-zero residual, p fallback), packed and
+    padded draft sides."""
+    rng = np.random.default_rng(21)
+    B, V, T, stride = 5, 37, 0.9, 4
+    k = np.array([3, 0, 4, 1, 2], np.int32)
+    cu = np.concatenate([[0], np.cumsum(k)]).astype(np.int32)
+    nd = int(k.sum())
+    t = (rng.standard_normal((nd + B, V)) * 1.7).astype(np.float32)
+    d = (t[np.concatenate([np.arange(cu[i] + i, cu[i] + i + k[i]) for i in range(B)])]
+         + rng.standard_normal((nd, V)).astype(np.float32) * 0.8).astype(np.float32)
+    d[cu[4] + 1] = t[cu[4] + 4 + 1]  # request 4, position 1: q = p (all-zero residual)
+    tok = rng.integers(0, V, size=nd).astype(np.int32)
+    dpad = np.zeros((B * stride, V), np.float32)
+    for i in range(B):
+        dpad[i * stride: i * stride + k[i]] = d[cu[i]: cu[i + 1]]
+    for draft, dstride in ((d, 0), (dpad, stride)):
+        for i in range(B):
+            for a in range(k[i] + 1):
+                drow = None
+                if a < k[i]:
+                    drow = draft[i * dstride + a] if dstride else draft[cu[i] + a]
+                st, C = O.final_cdf(t, draft, cu, i, a, T, draft_stride=dstride, lib=lib)
+                assert st == O.OK, (i, a, st)
+                e = np.cumsum(_ref_final_weights(t[cu[i] + i + a], drow, T))
+                np.testing.assert_allclose(C, e, rtol=1e-11, atol=1e-15,
+                                           err_msg=f"request {i}, a={a}, stride {dstride}")
+            st, _ = O.final_cdf(t, draft, cu, i, k[i] + 1, T, draft_stride=dstride, lib=lib)
+            assert st == O.ERR_INVALID_ARG
+    # the diagnostic of a verification call: u*S, S, C(y-1), C(y) around the
+    # drawn y, with C(y-1) <= u*S < C(y); request 2 accepts every draft (u = 0
+    # with identical rows), so its draw is from the bonus row
+    # requests 0, 3 and 4 reject at a chosen position: the drafter puts +6 on
+    # its drafted token there, so q(x) >> p(x), and u = 0.5 rejects
+    d2 = d.copy()
+    d2[cu[2]: cu[3]] = t[cu[2] + 2: cu[2] + 2 + k[2]]
+    ua = rng.random(nd).astype(np.float32)
+    ua[cu[2]: cu[3]] = 0.0
+    want = {0: 1, 3: 0, 4: 0}
+    for i, j in want.items():
+        ua[cu[i]: cu[i] + j] = 0.0
+        d2[cu[i]: cu[i] + j] = t[cu[i] + i: cu[i] + i + j]  # q = p before j: accepted
+        d2[cu[i] + j, tok[cu[i] + j]] += 6.0
+        ua[cu[i] + j] = 0.5
+    uf = rng.random(B).astype(np.float32)
+    res = O.verify_sample(t, d2, tok, cu, T, ua, uf, lib=lib)
+    assert res.status == O.OK and res.accept_len.tolist() == [1, 0, 4, 0, 0]
+    for i in range(B):
+        a = int(res.accept_len[i])
+        drow = d2[cu[i] + a] if a < k[i] else None
+        w = _ref_final_weights(t[cu[i] + i + a], drow, T)
+        C = np.cumsum(w)
+        y = int(res.tokens[cu[i] + i + a])
+        assert y == int(np.searchsorted(C, float(uf[i]) * C[-1], side="right")), (i, y)
+        uS, S, lo, hi = res.final[i]
+        assert abs(S - C[-1]) <= 1e-12 * C[-1], (i, S, C[-1])
+        assert abs(uS - float(uf[i]) * C[-1]) <= 1e-12 * C[-1], (i, uS)
+        assert abs(lo - (C[y - 1] if y > 0 else 0.0)) <= 1e-12 * C[-1], (i, lo)
+        assert abs(hi - C[y]) <= 1e-12 * C[-1], (i, hi)
+        assert lo <= uS < hi, (i, lo, uS, hi)
+
+
 def pin_sample_errors(lib):
     t = np.zeros((3, 4), np.float32)
     d = np.zeros((1, 4), np.float32)
@@ -595,7 +671,8 @@ ALL_PINS = [
     pin_softmax_errors, pin_argmax, pin_inverse_cdf, pin_greedy_golden,
     pin_greedy_brute_force, pin_greedy_padded_layout, pin_greedy_errors, pin_sample_golden,
     pin_lossless_chi_square, pin_q_equals_p_accepts_all, pin_residual_closed_forms,
-    pin_sample_outputs_layout, pin_sample_errors, pin_dcut_golden, pin_dcut_brute_force,
+    pin_sample_outputs_layout, pin_final_cdf_and_diagnostics, pin_sample_errors,
+    pin_dcut_golden, pin_dcut_brute_force,
     pin_dcut_expected_len, pin_dcut_errors,
 ]
 

@@ -81,6 +81,20 @@ MUTANTS = [
     ("cost variant sorts ascending",
      "if (a->benefit > b->benefit)\n        return -1;\n    if (a->benefit < b->benefit)\n        return 1;",
      "if (a->benefit < b->benefit)\n        return -1;\n    if (a->benefit > b->benefit)\n        return 1;"),
+    ("final CDF exclusive instead of inclusive",
+     "        C += cdf_out[v];\n        cdf_out[v] = C;",
+     "        const double w_v = cdf_out[v];\n        cdf_out[v] = C;\n        C += w_v;"),
+    ("final CDF at a = K reads the next draft row",
+     "    int64_t drow = a < k ? draft_index(cu, i, a, draft_stride) : -1;\n    int st = oracle_final_weights",
+     "    int64_t drow = a <= k ? draft_index(cu, i, a, draft_stride) : -1;\n    int st = oracle_final_weights"),
+    ("final CDF from the previous target row",
+     "    int st = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a), drow,\n                                  cdf_out, NULL);",
+     "    int st = oracle_final_weights(target, draft, dtype, V, T, target_row(cu, i, a > 0 ? a - 1 : a), drow,\n                                  cdf_out, NULL);"),
+    ("diagnostic S of p instead of the weights", "out_final[4 * (int64_t)i + 1] = S;",
+     "out_final[4 * (int64_t)i + 1] = 1.0;"),
+    ("diagnostic C(y-1) stops one weight short", "for (int64_t t = 0; t < v; ++t)",
+     "for (int64_t t = 0; t + 1 < v; ++t)"),
+    ("diagnostic u*S without S", "*uS_out = u * S;", "*uS_out = u;"),
 ]
 
 
