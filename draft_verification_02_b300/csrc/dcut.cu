@@ -297,15 +297,15 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 // ---------------------------------------------------------------------------
 //
 // The deep-dive page ("Tencent AngelSpec Speculative Decoding Framework Deep
-// Dive ...", its DCutScheduler listing) budgets verification in profiled
-// latency-cost units: cost(d) interpolates the table {1: 1.0, 2: 1.2,
-// 4: 1.5, 8: 2.0, 16: 3.0} linearly (clamped to its ends); each request takes
-// the depth maximising benefit(d) = P_d * d / cost(d) (the first such d);
-// requests are admitted in decreasing benefit (ties by request) while the
-// running cost stays within max_cost, skipping those that do not fit.  The
-// listing's arithmetic is fp64 and every decision here is taken in fp64
-// with each operation explicitly rounded, so depths match a sequential fp64
-// evaluation bit for bit.  One CTA: per-request best depths in parallel,
+// Dive ...", its D-cut scheduler) budgets verification in profiled
+// latency-cost units: cost(d) is the piecewise-linear function through the
+// table {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0} (constant beyond its
+// ends); each request takes the depth maximising benefit(d) = P_d * d /
+// cost(d) (the first such d); requests are admitted in decreasing benefit
+// (ties by request) while the running cost stays within max_cost, skipping
+// those that do not fit.  The page computes in Python floats (fp64); every
+// decision here is taken in fp64 with each operation explicitly rounded, so
+// depths match a sequential fp64 evaluation bit for bit.  One CTA: per-request best depths in parallel,
 // ranks by counting, then one thread walks the ranked requests (the
 // admission is sequential by definition).
 
@@ -324,21 +324,22 @@ struct DcutCostParams {
     uint32_t *status;
 };
 
+// cost(d) of the profiled latency table {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0,
+// 16: 3.0}: piecewise linear through those points, constant outside
+// [1, 16].  The table's depths are the powers 2^0 .. 2^4, so depth d in
+// (2^k, 2^(k+1)] lies on segment k, whose span is 2^k: the fraction
+// (d - 2^k) / 2^k is exact and the cost is one rounded multiply and one
+// rounded add in fp64.
 __device__ __forceinline__ double latency_cost(int d)
 {
-    const int dep[5] = {1, 2, 4, 8, 16};
-    const double lat[5] = {1.0, 1.2, 1.5, 2.0, 3.0};
-    if (d <= dep[0])
-        return lat[0];
-    if (d >= dep[4])
-        return lat[4];
-    for (int k = 0; k < 4; ++k) {
-        if (dep[k] <= d && d <= dep[k + 1]) {
-            const double r = __ddiv_rn((double)(d - dep[k]), (double)(dep[k + 1] - dep[k]));
-            return __dadd_rn(lat[k], __dmul_rn(r, __dsub_rn(lat[k + 1], lat[k])));
-        }
-    }
-    return lat[4];
+    const double at_pow2[5] = {1.0, 1.2, 1.5, 2.0, 3.0};  // cost(2^k), k = 0..4
+    if (d <= 1)
+        return at_pow2[0];
+    if (d >= 16)
+        return at_pow2[4];
+    const int k = 31 - __clz(d - 1);  // floor(log2(d - 1)): 2^k < d <= 2^(k+1)
+    const double frac = (double)(d - (1 << k)) / (double)(1 << k);  // exact
+    return __dadd_rn(at_pow2[k], __dmul_rn(__dsub_rn(at_pow2[k + 1], at_pow2[k]), frac));
 }
 
 __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostParams p)

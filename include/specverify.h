@@ -176,20 +176,21 @@ int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kma
                   spec_stream_t stream);
 
 /*
- * D-cut in latency-cost units: the policy of the DCutScheduler listing on
- * "Tencent AngelSpec Speculative Decoding Framework Deep Dive: MTP + Block
- * Diffusion Dual-Draft Strategy and D-cut High-Concurrency Throughput
- * Optimization".  cost(d) interpolates the profiled latency table
- * {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0} linearly and clamps outside
- * [1, 16].  Request i (kmax[i] >= 1) takes the depth d in 1..kmax[i]
+ * D-cut in latency-cost units: the scheduling policy that "Tencent AngelSpec
+ * Speculative Decoding Framework Deep Dive: MTP + Block Diffusion Dual-Draft
+ * Strategy and D-cut High-Concurrency Throughput Optimization" gives in its
+ * D-cut section.  cost(d) is the piecewise-linear function through the
+ * profiled latency table {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0},
+ * constant outside [1, 16].  Request i (kmax[i] >= 1) takes the depth d in 1..kmax[i]
  * maximising benefit(d) = (conf[i][0] * ... * conf[i][d-1]) * d / cost(d)
  * (the first such d); requests are then taken in decreasing benefit (ties by
  * request) and admitted while the running total of their costs stays within
  * max_cost, skipping any that would exceed it.  out_depth[i] = the chosen
  * depth if admitted, else 0 (only its bonus row is verified); out_cu as in
  * dcut_allocate; out_benefit[i] (fp64, may be NULL) = the admitted
- * request's benefit, else 0.  All arithmetic is fp64, operation by
- * operation, as in the listing.  Invalid confidences or kmax set
+ * request's benefit, else 0.  All arithmetic is fp64 (the page computes in
+ * Python floats), each operation rounded once, so the depths are those of a
+ * plain sequential fp64 evaluation.  Invalid confidences or kmax set
  * SPEC_ERR_INVALID_ARG on the device and write -1 depths and offsets.  One
  * kernel launch (one CTA); B <= SPEC_MAX_BATCH.
  */

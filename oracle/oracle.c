@@ -590,12 +590,11 @@ int oracle_dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int3
 
 /*
  * The deep-dive page ("Tencent AngelSpec Speculative Decoding Framework Deep
- * Dive ...", its DCutScheduler listing) budgets verification in profiled
+ * Dive ...", its D-cut scheduler) budgets verification in profiled
  * latency-cost units instead of tokens.  What it computes:
- *  - cost(d): the latency of verifying depth d, read from the table
- *    {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0} by linear interpolation
- *    between neighbouring entries, clamped to the first / last entry
- *    outside [1, 16];
+ *  - cost(d): the latency of verifying depth d, given by the profiled table
+ *    {1: 1.0, 2: 1.2, 4: 1.5, 8: 2.0, 16: 3.0}: the piecewise-linear
+ *    function through those points, constant beyond both ends;
  *  - per request: the depth d in 1..kmax maximising
  *    benefit(d) = (conf_0 * ... * conf_{d-1}) * d / cost(d)
  *    (the first such d when several tie);
@@ -603,25 +602,45 @@ int oracle_dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int3
  *    request order), each admitted when the running cost total plus its own
  *    cost stays within max_cost; a request that does not fit is skipped and
  *    later ones are still tried.
- * Readings: all of it in fp64 (the page's arithmetic), products left to
- * right; a request with kmax = 0 is no candidate; a request not admitted
+ * Readings: all of it in fp64 (the page computes in Python floats), products
+ * left to right; a request with kmax = 0 is no candidate; a request not admitted
  * verifies depth 0 (its bonus row only).
  */
-double oracle_dcut_cost(int32_t d)
+/* The profiled latency table: cost at depths 1, 2, 4, 8 and 16. */
+static const int32_t cost_at_depth[5] = {1, 2, 4, 8, 16};
+static const double cost_value[5] = {1.0, 1.2, 1.5, 2.0, 3.0};
+
+/*
+ * cost(d) for d = 0..ORC_MAX_DRAFT, by definition: the piecewise-linear
+ * function through the five (depth, cost) points, constant beyond the first
+ * and the last point.  Filled segment by segment: between points a < b the
+ * cost rises from cost(a) to cost(b) in proportion to (d - a) / (b - a).
+ */
+static void fill_cost_table(double table[ORC_MAX_DRAFT + 1])
 {
-    static const int32_t dep[5] = {1, 2, 4, 8, 16};
-    static const double lat[5] = {1.0, 1.2, 1.5, 2.0, 3.0};
-    if (d <= dep[0])
-        return lat[0];
-    if (d >= dep[4])
-        return lat[4];
-    for (int k = 0; k < 4; ++k) {
-        if (dep[k] <= d && d <= dep[k + 1]) {
-            double r = (double)(d - dep[k]) / (double)(dep[k + 1] - dep[k]);
-            return lat[k] + r * (lat[k + 1] - lat[k]);
+    for (int32_t d = 0; d <= cost_at_depth[0]; ++d)
+        table[d] = cost_value[0];
+    for (int seg = 0; seg + 1 < 5; ++seg) {
+        const int32_t a = cost_at_depth[seg], b = cost_at_depth[seg + 1];
+        const double rise = cost_value[seg + 1] - cost_value[seg];
+        for (int32_t d = a + 1; d <= b; ++d) {
+            const double frac = (double)(d - a) / (double)(b - a);
+            table[d] = cost_value[seg] + rise * frac;
         }
     }
-    return lat[4];
+    for (int32_t d = cost_at_depth[4] + 1; d <= ORC_MAX_DRAFT; ++d)
+        table[d] = cost_value[4];
+}
+
+double oracle_dcut_cost(int32_t d)
+{
+    double table[ORC_MAX_DRAFT + 1];
+    fill_cost_table(table);
+    if (d < 0)
+        d = 0;
+    if (d > ORC_MAX_DRAFT)
+        d = ORC_MAX_DRAFT;
+    return table[d];
 }
 
 typedef struct {

@@ -48,7 +48,7 @@ MUTANTS = [
      "p_out[v] = exp(logit_at(logits, dtype, row, V, v) / T) / s;"),
     ("inverse CDF forgets to scale u by S", "double target = u * S;", "double target = u;"),
     ("cost table interpolates from the wrong end",
-     "return lat[k] + r * (lat[k + 1] - lat[k]);", "return lat[k + 1] - r * (lat[k + 1] - lat[k]) + 0.1;"),
+     "table[d] = cost_value[seg] + rise * frac;", "table[d] = cost_value[seg + 1] - rise * frac;"),
     ("cost variant stops at the first request that does not fit",
      "if (total + c <= max_cost) {", "if (total + c > max_cost) break; {"),
     ("cost variant benefit forgets the depth factor",
@@ -72,8 +72,8 @@ MUTANTS = [
     ("expected length counts one depth too many",
      "            for (int32_t d = 1; d <= out_depth[i]; ++d) {\n                P = P * conf",
      "            for (int32_t d = 1; d <= out_depth[i] + (out_depth[i] < Kmax); ++d) {\n                P = P * conf"),
-    ("cost table clamps long depths to the shortest cost", "    if (d >= dep[4])\n        return lat[4];",
-     "    if (d >= dep[4])\n        return lat[0];"),
+    ("cost table clamps long depths to the shortest cost", "        table[d] = cost_value[4];",
+     "        table[d] = cost_value[0];"),
     ("acceptance counts the first rejection as accepted", "            if (a > j)\n                out_accepted[j] += 1;",
      "            if (a >= j)\n                out_accepted[j] += 1;"),
     ("D-cut keeps only products strictly above min_gain", "            if (P >= min_gain)",
