@@ -16,6 +16,7 @@ constexpr int kMaxTraceEvents = 16;
 thread_local cudaEvent_t g_trace[kMaxTraceEvents];
 thread_local int g_trace_n = 0;
 thread_local int64_t g_launches = 0;
+thread_local uint64_t g_expire_unit = 0;  // test hook: 1 + the unit, 0 = off
 
 sv::Tracer make_tracer()
 {
@@ -124,6 +125,7 @@ int spec_verify_greedy(const void *target_logits, int dtype, const int32_t *draf
     a.out_tokens = out_tokens;
     a.out_len = out_accept_len;
     a.ws = workspace;
+    a.debug_item = g_expire_unit;
     sv::Tracer tr = make_tracer();
     return cuda_status(sv::launch_verify(a, (cudaStream_t)stream, tr));
 }
@@ -172,6 +174,7 @@ int spec_verify_sample(const void *target_logits, const void *draft_logits, int 
     a.out_p = out_p;
     a.out_q = out_q;
     a.ws = workspace;
+    a.debug_item = g_expire_unit;
     sv::Tracer tr = make_tracer();
     return cuda_status(sv::launch_verify(a, (cudaStream_t)stream, tr));
 }
@@ -375,5 +378,13 @@ int spec_set_trace(void *const *events, int n_events)
 }
 
 int64_t spec_kernel_launch_count(void) { return g_launches; }
+
+int spec_test_expire_wait(int64_t unit)
+{
+    if (unit < -1)
+        return SPEC_ERR_INVALID_ARG;
+    g_expire_unit = (uint64_t)(unit + 1);
+    return SPEC_OK;
+}
 
 }  // extern "C"

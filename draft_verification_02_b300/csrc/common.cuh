@@ -299,4 +299,20 @@ __device__ __forceinline__ uint32_t read_status(const uint32_t *status)
     return *(volatile const uint32_t *)status;
 }
 
+// Bounds checks of the debug build (compiled with -DSV_DEBUG): an index
+// outside [0, n) of its buffer sets ST_INVALID and the access it guards is
+// skipped.  In the normal build every check is the constant true.
+#ifdef SV_DEBUG
+__device__ __forceinline__ bool in_bounds(int64_t idx, int64_t n, uint32_t *status)
+{
+    if (idx >= 0 && idx < n)
+        return true;
+    atomicOr(status, ST_INVALID);
+    return false;
+}
+#define SV_IN_BOUNDS(idx, n, status) ::sv::in_bounds((int64_t)(idx), (int64_t)(n), (status))
+#else
+#define SV_IN_BOUNDS(idx, n, status) true
+#endif
+
 }  // namespace sv

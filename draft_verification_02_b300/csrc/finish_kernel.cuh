@@ -163,14 +163,19 @@ __global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const Fin
     const int K = __ldg(p.cu + i + 1) - cu_i;
     const bool shape = request_shape_ok(p, i, cu_i, K);
     const bool act = shape && warp == 0 && lane < K;
-    const int x = act ? __ldg(p.tokens + draft_index(p.draft_stride, p.cu, i, lane)) : -1;
+    const int64_t dx = act ? draft_index(p.draft_stride, p.cu, i, lane) : 0;
+    const int x = act && SV_IN_BOUNDS(dx, p.draft_rows, p.status) ? __ldg(p.tokens + dx) : -1;
 
     pdl_wait();  // kernel 1 has completed and its writes are visible
     if (__ldcg(p.cu_flag) == 0u || !shape)
         return;  // malformed offsets: kernel 1 poisoned every output
     const int64_t t0 = (int64_t)cu_i + i;
     for (int rho = warp; rho <= K; rho += kFinishWarps) {
-        const int gj = merge_argmax_row(p.part, p.g, t0 + rho);
+        int wf, wl;
+        row_span(p.g, t0 + rho, wf, wl);
+        const int gj = SV_IN_BOUNDS(t0 + rho + wl, p.part_cap, p.status)
+                           ? merge_argmax_row(p.part, p.g, t0 + rho)
+                           : -2;
         if (lane == 0)
             row_g[rho] = gj;
     }
@@ -189,15 +194,17 @@ __global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const Fin
         if (lane == 0)
             set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
         for (int jj = lane; jj <= K; jj += 32)
-            p.out_tokens[t0 + jj] = -1;
-        if (lane == 0)
+            if (SV_IN_BOUNDS(t0 + jj, p.g.max_rows, p.status))
+                p.out_tokens[t0 + jj] = -1;
+        if (lane == 0 && SV_IN_BOUNDS(i, p.B, p.status))
             p.out_len[i] = -1;
         return;
     }
     const int a = rej ? __ffs(rej) - 1 : K;
     for (int jj = lane; jj <= K; jj += 32)
-        p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
-    if (lane == 0)
+        if (SV_IN_BOUNDS(t0 + jj, p.g.max_rows, p.status))
+            p.out_tokens[t0 + jj] = jj < a ? x : (jj == a ? row_g[a] : -1);
+    if (lane == 0 && SV_IN_BOUNDS(i, p.B, p.status))
         p.out_len[i] = a;
 }
 
@@ -662,8 +669,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     int64_t di = 0;
     if (act) {
         di = draft_index(p.draft_stride, p.cu, i, lane);
-        x = __ldg(p.tokens + di);
-        u = __ldg(p.u_accept + di);
+        if (SV_IN_BOUNDS(di, p.draft_rows, p.status)) {
+            x = __ldg(p.tokens + di);
+            u = __ldg(p.u_accept + di);
+        }
     }
     // the rows this warp merges: with at most one row per warp of a CTA,
     // every CTA merges all of them (row k = warp), else the rows are spread
@@ -682,8 +691,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         else if (my_k[t] != K) {
             const int j = my_k[t] < K ? my_k[t] : my_k[t] - K - 1;
             const int64_t dj = draft_index(p.draft_stride, p.cu, i, j);
-            const int xj = __ldg(p.tokens + dj);
-            if (xj >= 0 && xj < p.V) {
+            const int xj = SV_IN_BOUNDS(dj, p.draft_rows, p.status) ? __ldg(p.tokens + dj) : -1;
+            if (xj >= 0 && xj < p.V &&
+                (my_k[t] < K ? SV_IN_BOUNDS(t0 + j, p.g.max_rows, p.status)
+                             : SV_IN_BOUNDS(dj, p.draft_rows, p.status))) {
                 g_ok[t] = true;
                 g[t] = my_k[t] < K ? Elem<T>::ld_global(tbase + (t0 + j) * p.V, xj)
                                    : Elem<T>::ld_global(dbase + dj * p.V, xj);
@@ -713,6 +724,8 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         int wf, wl;
         row_span(p.g, rg, wf, wl);
         for (int w = wf + lane; w <= wl; w += 32) {
+            if (!SV_IN_BOUNDS(rg + w, p.part_cap, p.status))
+                continue;
             const Partial pt = load_partial(p.part + rg + w);
             lse_combine(mm[t], sm[t], pt.m, {pt.s_hi, pt.s_lo}, p.c);
         }
@@ -771,25 +784,30 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         bad = nf || bt;
         a = rej ? __ffs(rej) - 1 : K;
         if (rank == 0 && warp == 0) {  // the request's outputs, written once
+            const bool len_ok = SV_IN_BOUNDS(i, p.B, p.status);
             if (bad || timeout) {
                 if (lane == 0)
                     set_status(p.status, (nf ? ST_NONFINITE : 0u) | (bt ? ST_INVALID : 0u));
                 for (int jj = lane; jj <= K; jj += 32)
-                    p.out_tokens[t0 + jj] = -1;
-                if (lane == 0)
+                    if (SV_IN_BOUNDS(t0 + jj, p.g.max_rows, p.status))
+                        p.out_tokens[t0 + jj] = -1;
+                if (lane == 0 && len_ok)
                     p.out_len[i] = -1;
             } else {
-                if (act && p.out_p)
+                const bool di_ok = act && SV_IN_BOUNDS(di, p.draft_rows, p.status);
+                if (di_ok && p.out_p)
                     p.out_p[di] = pp;
-                if (act && p.out_q)
+                if (di_ok && p.out_q)
                     p.out_q[di] = qq;
                 for (int jj = lane; jj <= K; jj += 32) {
+                    if (!SV_IN_BOUNDS(t0 + jj, p.g.max_rows, p.status))
+                        continue;
                     if (jj < a)
                         p.out_tokens[t0 + jj] = x;  // jj == lane since a <= 32
                     else if (jj > a)
                         p.out_tokens[t0 + jj] = -1;
                 }
-                if (lane == 0)
+                if (lane == 0 && len_ok)
                     p.out_len[i] = a;
             }
         }
@@ -813,6 +831,10 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     // ---- final draw: this CTA weighs its range of the vocabulary
     const int64_t trow_i = t0 + a;
     const int64_t drow_i = a < K ? draft_index(p.draft_stride, p.cu, i, a) : -1;
+    // (the same verdict in every CTA of the cluster: no cluster barrier is split)
+    if (!(SV_IN_BOUNDS(trow_i, p.g.max_rows, p.status) &&
+          (drow_i < 0 || SV_IN_BOUNDS(drow_i, p.draft_rows, p.status))))
+        return;
     const T *trow = tbase + trow_i * p.V;
     const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
     const DrawShared<T> sh{tb,     db,      &bar,    piece,      wred,   slice_tot,
@@ -826,9 +848,11 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
             set_status(p.status, ST_NONFINITE);
         if (timeout || s_expired) {  // a copy gave up: the data may be stale
             y = -1;
-            p.out_len[i] = -1;
+            if (SV_IN_BOUNDS(i, p.B, p.status))
+                p.out_len[i] = -1;
             for (int jj = 0; jj <= K; ++jj)
-                p.out_tokens[t0 + jj] = -1;
+                if (SV_IN_BOUNDS(t0 + jj, p.g.max_rows, p.status))
+                    p.out_tokens[t0 + jj] = -1;
         }
         p.out_tokens[trow_i] = y;
     }

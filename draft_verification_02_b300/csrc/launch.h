@@ -34,9 +34,10 @@ struct VerifyArgs {
     float *out_p;
     float *out_q;
     void *ws;
+    uint64_t debug_item;  // test hook: 1 + the streaming unit whose wait reports expiry (0: off)
 };
 
-// Enqueue the verification kernels (1 launch greedy, 2 launches sampling).
+// Enqueue the verification kernels (two launches: the streaming pass and a finish kernel).
 cudaError_t launch_verify(const VerifyArgs &a, cudaStream_t stream, Tracer &tr);
 
 struct DcutArgs {

@@ -300,7 +300,7 @@ __device__ __forceinline__ void store_partial(LaneAcc &a, float c, Partial *slot
         out.s_hi = s.hi;
         out.s_lo = s.lo;
     }
-    if (lane == 0)
+    if (lane == 0 && slot)
         *slot = out;
     a.m = -INFINITY;
     a.s = 0.f;
@@ -347,6 +347,8 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
         if (rg < g.max_rows) {
             if (check && rg >= nt)
                 return false;
+            if (!SV_IN_BOUNDS(rg, g.max_rows, p.status))
+                return false;
             src = tbase + rg * (int64_t)V + col0;
             return true;
         }
@@ -370,6 +372,8 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
             }
             row = (int64_t)lo * p.draft_stride + (slot - cu_s[lo]);
         }
+        if (!SV_IN_BOUNDS(row, p.draft_rows, p.status))
+            return false;
         src = dbase + row * (int64_t)V + col0;
         return true;
     };
@@ -482,7 +486,9 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
         const bool live = locate(c_rg, c_q, src, len, col0, nt, nd, true);
         if (issued >> k & 1) {
             if (p.tma) {
-                const bool ok = mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                bool ok = mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                if ((uint64_t)(u0 + n) + 1 == p.debug_unit)
+                    ok = false;  // test hook: this wait reports expiry (its copy has landed)
                 if (__any_sync(0xffffffffu, !ok)) {
                     // a copy never completed: flag it, give every copy still in
                     // flight one more bounded wait, and stop (the finish kernel
@@ -526,7 +532,9 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
         advance(c_rg, c_q);
         const bool row_ends = (n + 1 == n_units) || (c_rg != rg);
         if (row_ends && seg_active) {
-            store_partial<GREEDY>(acc, p.c, p.part + rg + w);
+            store_partial<GREEDY>(acc, p.c,
+                                  SV_IN_BOUNDS(rg + w, p.part_cap, p.status) ? p.part + rg + w
+                                                                             : nullptr);
             seg_active = false;
         }
         if (++k == kRing)

@@ -210,6 +210,9 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     sp.status = reinterpret_cast<uint32_t *>(ws + L.status);
     sp.cu_flag = sp.status + 1;
     sp.part = reinterpret_cast<Partial *>(ws + L.part1);
+    sp.part_cap = (int64_t)((L.total - L.part1) / sizeof(Partial));
+    sp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
+    sp.debug_unit = a.debug_item;
 
     FinishParams fp{};
     fp.target = a.target;
@@ -237,6 +240,7 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.status = sp.status;
     fp.cu_flag = sp.cu_flag;
     fp.part = sp.part;
+    fp.part_cap = sp.part_cap;
 
     cudaError_t err = prepare_stream<T, GREEDY>();
     // The finish kernel with its weighing out of line (more registers, at
@@ -317,6 +321,8 @@ static cudaError_t launch_draft_pass(const void *draft, int B, int Kmax, int V, 
     sp.status = reinterpret_cast<uint32_t *>(ws + L.status);
     sp.cu_flag = sp.status + 1;
     sp.part = reinterpret_cast<Partial *>(ws + L.part1);
+    sp.part_cap = (int64_t)((L.total - L.part1) / sizeof(Partial));
+    sp.draft_rows = 0;
     cudaError_t err = prepare_stream<T, GREEDY>();
     if (err != cudaSuccess)
         return err;
@@ -421,6 +427,7 @@ static cudaError_t launch_draft_typed(const DraftArgs &a, cudaStream_t s, Tracer
             return err;
         fp.g = sp.g;
         fp.part = sp.part;
+        fp.part_cap = sp.part_cap;
         const cudaLaunchConfig_t cfg = pdl_config(
             dim3((unsigned)((rows + kFinishWarps - 1) / kFinishWarps)), dim3(kFinishThreads), 0, s,
             attr, 1);

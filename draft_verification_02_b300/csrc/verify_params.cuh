@@ -41,6 +41,9 @@ struct StreamParams {
     uint32_t *status;
     uint32_t *cu_flag;
     Partial *part;
+    int64_t part_cap;     // partials the workspace holds
+    int64_t draft_rows;   // draft rows the draft side may index
+    uint64_t debug_unit;  // test hook: the wait for unit debug_unit - 1 reports expiry (0: off)
 };
 
 struct FinishParams {
@@ -71,6 +74,7 @@ struct FinishParams {
     uint32_t *status;
     const uint32_t *cu_flag;
     const Partial *part;
+    int64_t part_cap;  // partials the workspace holds
 };
 
 // ---------------------------------------------------------------------------

@@ -15,7 +15,9 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libspecverify.so")
+# SPECVERIFY_LIB selects another in-tree build of the same library (the
+# tests use it for the bounds-checked build, libspecverify_debug.so)
+LIB_PATH = os.path.join(_HERE, os.environ.get("SPECVERIFY_LIB", "libspecverify.so"))
 
 SPEC_OK = 0
 SPEC_ERR_INVALID_ARG = -1
@@ -32,7 +34,7 @@ EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
            "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
            "spec_verify_sample_static", "dcut_allocate_cost", "spec_draft_confidence",
-           "spec_draft_sample", "spec_acceptance_stats")
+           "spec_draft_sample", "spec_acceptance_stats", "spec_test_expire_wait")
 SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -81,6 +83,8 @@ def _load():
     lib.spec_set_trace.restype = INT
     lib.spec_kernel_launch_count.argtypes = []
     lib.spec_kernel_launch_count.restype = I64
+    lib.spec_test_expire_wait.argtypes = [I64]
+    lib.spec_test_expire_wait.restype = INT
     return lib
 
 
@@ -308,6 +312,11 @@ def spec_set_trace(events) -> int:
 
 def spec_kernel_launch_count() -> int:
     return int(LIB.spec_kernel_launch_count())
+
+
+def spec_test_expire_wait(item: int) -> int:
+    """Test hook (see the header): -1 turns it off."""
+    return int(LIB.spec_test_expire_wait(int(item)))
 
 
 def check(status: int, where: str = "") -> None:

@@ -298,8 +298,10 @@ int spec_acceptance_stats(const int32_t *accept_len, const int32_t *cu_draft, in
  *  - Returns SPEC_ERR_WORKSPACE, with nothing enqueued, when
  *    spec_workspace_size(B, max_target_rows, V) > SPEC_STATIC_SCRATCH_BYTES.
  *  - The first call on each device looks up the array's device address
- *    (with that device current); make that first call before any stream
- *    capture.
+ *    (with that device current) and keeps it for the life of the process;
+ *    make that first call before any stream capture.  A device reset
+ *    (cudaDeviceReset) discards the context that address belongs to: after
+ *    one, this entry point must not be called again in the same process.
  *  - Every call on a device shares the one array, and it keeps the previous
  *    call's contents: calls that may overlap on the GPU (different streams,
  *    or concurrent host threads) race and must be serialised by the caller.
@@ -334,6 +336,19 @@ int spec_set_trace(void *const *events, int n_events);
 
 /* Number of kernels the calling thread has launched through this library. */
 int64_t spec_kernel_launch_count(void);
+
+/*
+ * Test hook for the timeout path; never needed in production (unit = -1,
+ * the default, turns it off).  The streaming pass of spec_verify_sample /
+ * spec_verify_greedy reads the rows in units (pieces of at most 4 KB, each
+ * one 1-D bulk copy), numbered from 0 in row order.  After
+ * spec_test_expire_wait(unit), the calling thread's later verification calls
+ * treat the bounded wait for that unit's copy as expired once the copy has
+ * landed: the warp holding it flags SPEC_ERR_TIMEOUT, waits for its other
+ * copies in flight and stops, and every output of the call is unspecified
+ * (the ones the kernels reach are poisoned).  Thread-local.
+ */
+int spec_test_expire_wait(int64_t unit);
 
 #ifdef __cplusplus
 }

@@ -20,6 +20,7 @@ def pytest_configure(config):
     from draft_verification_02_b300 import build as cuda_build
     oracle.build()
     cuda_build.build()
+    cuda_build.build(debug=True)
 
 
 @pytest.fixture(scope="session")

@@ -126,3 +126,10 @@ def test_binding_refuses_host_tensors():
     with pytest.raises(ValueError):
         sv.dcut_allocate(torch.zeros((2, 2)), torch.zeros(2, dtype=torch.int32), 2, 2, 2, 0.0,
                          i32[:2], i32[:3], None, ws)
+
+
+def test_expiry_hook_arguments():
+    """The test-only expiry hook takes a unit index or -1 (off)."""
+    assert sv.spec_test_expire_wait(-2) == sv.SPEC_ERR_INVALID_ARG
+    assert sv.spec_test_expire_wait(5) == sv.SPEC_OK
+    assert sv.spec_test_expire_wait(-1) == sv.SPEC_OK
