@@ -74,3 +74,30 @@ def test_static_scratch_rejects_sizes_beyond_its_array():
         1.0, f32.data_ptr(), f32.data_ptr(), i32.data_ptr(), i32.data_ptr(), None, None, None)
     assert st == sv.SPEC_ERR_WORKSPACE
     torch.cuda.synchronize()
+
+
+def test_static_scratch_data_error_then_clean_call_against_the_oracle():
+    """A request with a NaN logit is poisoned (accepted length -1, tokens -1)
+    and the others match the oracle; the next call on clean inputs starts
+    from the scratch the failed call left and matches the oracle everywhere."""
+    import parity
+    b = _batch(41, 1.0, 12, 32000)
+    bad = 5
+    row = int(b.cu_draft[bad]) + bad  # request 5's first target row
+    b.target_logits[row, 123] = float("nan")
+    o = _outputs(b)
+    assert _static_call(b, o) == sv.SPEC_OK
+    torch.cuda.synchronize()
+    assert int(o["accept_len"][bad]) == -1
+    K = int(b.k[bad])
+    assert bool((o["tokens"][row:row + K + 1] == -1).all())
+    good = [i for i in range(b.B) if i != bad]
+    rep = parity.compare_batch(b, o, good)
+    assert rep["exempt_accept"] + rep["exempt_final"] <= 2, rep
+    clean = _batch(42, 1.0, 12, 32000)
+    o2 = _outputs(clean)
+    assert _static_call(clean, o2) == sv.SPEC_OK
+    torch.cuda.synchronize()
+    assert bool((o2["accept_len"] >= 0).all())
+    rep = parity.compare_batch(clean, o2)
+    assert rep["exempt_accept"] + rep["exempt_final"] <= 2, rep
