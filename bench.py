@@ -8,6 +8,8 @@
     python bench.py --workload draft|draft_greedy   (the drafter's step: spec_draft_sample)
     python bench.py --workload confidence           (spec_draft_confidence on the drafter rows)
     python bench.py --workload dcut_cost            (dcut_allocate_cost + verification)
+    python bench.py --shards N ...           (vocabulary-sharded verification: the N shards
+                                              of a tensor-parallel target, all on this GPU)
     python bench.py --impl reference ...     (the CPU oracle, timed on the host cores)
 
 One step = one pass of the whole verification path over one batch whose
@@ -104,6 +106,9 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--shards", type=int, default=0,
+                    help="vocabulary-sharded verification: the N shards of a tensor-parallel "
+                         "target, all on this GPU (0 = unsharded)")
     return ap.parse_args(argv)
 
 
@@ -671,6 +676,208 @@ def run_ours(args, dist):
     dist.close()
 
 
+def run_sharded(args, dist):
+    """A verification workload through the vocabulary-sharded calls: the N
+    shards of a tensor-parallel target (contiguous column ranges, each shard's
+    logits contiguous as on its own rank), run one after the other on this
+    GPU.  The exchanges are stood in for by stacking and an element-wise max
+    on the same GPU, so no interconnect is measured.  value = verified
+    positions/s of the whole N-shard step on one GPU."""
+    from draft_verification_02_b300 import specverify as sv
+    from draft_verification_02_b300.sharded import Shard, shard_bounds, shard_columns
+
+    device = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(device)
+    sampler = ClockSampler(device, enabled=not args.no_clocks)
+    dist.init("nccl")
+    w, T = workload_of(args)
+    if w.kmax or args.workload in DRAFT_WORKLOADS:
+        raise SystemExit("--shards applies to the verification workloads (ragged<k>, mtp, block)")
+    N = args.shards
+    bounds = shard_bounds(w.V, N)
+    depths0 = None
+    rows = W.max_target_rows(w)
+    if w.k is None:
+        depths0 = W.make_depths(w, "cpu", rank_seed_offset(dist.rank))
+        rows = int(depths0.sum().item()) + w.B
+    shards = [Shard(w.B, rows, bounds, r, device=device) for r in range(N)]
+
+    def make_set(rep, keep_full):
+        b = W.make_verify_batch(w, T, device, rep=rep, depths=depths0)
+        s = {"batch": b, "targets": shard_columns(b.target_logits, bounds),
+             "drafts": shard_columns(b.draft_logits if T > 0 else None, bounds),
+             "outs": [sh.outputs() for sh in shards]}
+        if not keep_full:  # each shard holds only its own columns
+            b.target_logits = b.draft_logits = None
+        return s
+
+    first = make_set(rank_seed_offset(dist.rank), True)
+    batch0 = first["batch"]
+    set_bytes = sum(t.numel() * t.element_size() for t in first["targets"] + first["drafts"]
+                    if t is not None)
+    n_sets = max(2, min(64, math.ceil(2.2 * l2_bytes(device) / max(set_bytes, 1))))
+    sets = [first] + [make_set(rank_seed_offset(dist.rank) + r, False) for r in range(1, n_sets)]
+    positions = batch0.n_draft
+    alg_bytes = batch0.algorithmic_bytes()
+
+    def step(s, ev=None):
+        """ev: per shard, events [before the streaming pass, after it, after
+        the row merge, after accept, after mass, after draw]."""
+        b = s["batch"]
+        recs = []
+        for r, sh in enumerate(shards):
+            if ev is not None:
+                sv.spec_set_trace(ev[r][0:3])
+            recs.append(sh.row_stats(s["targets"][r], s["drafts"][r], b.draft_tokens, b.cu_draft,
+                                     T))
+        rows_all = torch.stack(recs)
+        for r, sh in enumerate(shards):
+            if ev is not None:
+                sv.spec_set_trace(ev[r][3:5])
+            sh.accept(rows_all, b.draft_tokens, b.cu_draft, T, b.u_accept, s["outs"][r])
+        if T > 0:
+            masses = []
+            for r, sh in enumerate(shards):
+                if ev is not None:
+                    sv.spec_set_trace(ev[r][5:7])
+                masses.append(sh.final_mass(s["targets"][r], s["drafts"][r]))
+            mass_all = torch.stack(masses)
+            for r, sh in enumerate(shards):
+                if ev is not None:
+                    sv.spec_set_trace(ev[r][7:9])
+                sh.final_draw(s["targets"][r], s["drafts"][r], mass_all, b.u_final,
+                              s["outs"][r]["tokens"])
+            top = torch.stack([o["tokens"] for o in s["outs"]]).amax(0)
+            for o in s["outs"]:
+                o["tokens"].copy_(top)
+        if ev is not None:
+            sv.spec_set_trace(None)
+
+    n0 = sv.spec_kernel_launch_count()
+    for k in range(max(1, args.warmup)):
+        step(sets[k % n_sets])
+    torch.cuda.synchronize(device)
+    launches_per_step = (sv.spec_kernel_launch_count() - n0) // max(1, args.warmup)
+    for sh in shards:
+        sv.check(sv.spec_get_device_status(sh.workspace), "device status after warm-up")
+
+    K = args.steps
+    G = max(1, min(K, args.graph_steps))
+    stream = torch.cuda.Stream(device)
+
+    def events(n):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        for e in evs:
+            e.record()
+        return evs
+
+    def capture(n_steps, offset, traced):
+        evs = [[events(9) for _ in range(N)] if traced else None for _ in range(n_steps)]
+        torch.cuda.synchronize(device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for k in range(n_steps):
+                step(sets[(offset + k) % n_sets], evs[k])
+        return g, evs
+
+    g_main = capture(G, 0, False)[0]
+    n_rep, rem = divmod(K, G)
+    g_rem = capture(rem, n_rep * G, False)[0] if rem else None
+    g_traced, ev_main = capture(G, 0, True)
+    g_main.replay()
+    g_traced.replay()
+    torch.cuda.synchronize(device)
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler.wait_first_sample(timeout=60.0)
+    dist.barrier()
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    rep_ev = [torch.cuda.Event(enable_timing=True) for _ in range(n_rep + 1)]
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        rep_ev[0].record(stream)
+        for q in range(n_rep):
+            g_main.replay()
+            rep_ev[q + 1].record(stream)
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+    torch.cuda.synchronize(device)
+    t_wall1 = time.time()
+    step_dist = replay_percentiles(rep_ev, G)
+    dist.barrier()
+    with torch.cuda.stream(stream):
+        g_traced.replay()
+    torch.cuda.synchronize(device)
+    sampler.stop()
+    for sh in shards:
+        sv.check(sv.spec_get_device_status(sh.workspace), "device status after the timed region")
+    elapsed_ms_max = dist.max(start.elapsed_time(end), device)
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    def span(a, b_):  # mean over the traced steps of the summed per-shard spans, us
+        return statistics.mean(sum(ev_main[k][r][a].elapsed_time(ev_main[k][r][b_])
+                                   for r in range(N)) * 1e3 for k in range(G))
+    kern = {"stream_kernel": span(0, 1), "shard_rows_kernel": span(1, 2),
+            "shard_accept_kernel": span(3, 4)}
+    if T > 0:
+        kern["shard_mass_kernel"] = span(5, 6)
+        kern["shard_draw_kernel"] = span(7, 8)
+    stream_sum = kern["stream_kernel"]
+    total_positions = dist.sum(positions * K, device)
+    value = total_positions / (elapsed_ms_max / 1e3)
+    ms_per_step = elapsed_ms_max / K
+    peak, peak_kind = measured_hbm_peak()
+    step_gbs = alg_bytes / (ms_per_step / 1e3) / 1e9
+    achieved = alg_bytes / (stream_sum / 1e6) / 1e9
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        rate, nreq, el = oracle_sample_rate(host_arrays(batch0), args.cpu_seconds, threads)
+        cpu = {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{nreq} whole requests of input set 0 ({workload_desc(w, T)}) on the "
+                         f"whole vocabulary, one oracle call per request on {threads} host "
+                         f"threads, {el:.1f} s"}
+    name = f"{args.workload}_tp{N}"
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_dist": step_dist,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{workload_desc(w, T, args.workload)}; vocabulary split into {N} "
+                        f"contiguous shards (a TP={N} target's layout), all {N} on this GPU, "
+                        f"the exchanges stood in for on the same GPU",
+            "B": w.B, "V": w.V, "shards": N, "shard_bounds": bounds, "logits_dtype": w.dtype,
+            "temperature": T, "verified_positions_per_step": positions,
+            "target_rows_per_step": batch0.n_target_rows,
+            "l2": f"inputs rotate through {n_sets} independent sets "
+                  f"({n_sets * set_bytes / 1e6:.0f} MB > 2x L2 of {l2_bytes(device) / 1e6:.0f} MB)",
+            "timing": f"CUDA graphs of {G} steps replayed, CUDA events on the launching stream;"
+                      " per-kernel times from a traced replay",
+            "parallelism": f"{dist.world} GPU(s), independent batches per GPU",
+        },
+        "hbm_gbs_step": step_gbs, "hbm_frac_step": step_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": "stream_kernel", "achieved": achieved,
+                     "peak": peak, "peak_kind": f"of {peak_kind}", "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": recorded_traffic(name, "stream_kernel"),
+                     "algorithmic_bytes_per_launch": alg_bytes / N,
+                     "launches": N, "launch_us_mean": stream_sum / N},
+        "kernels_us": dict(kern, note=f"summed over the {N} shards, one traced replay; the rest "
+                                      "of the step is the stand-in exchanges (torch copies)"),
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "e2e": None,
+        "cpu_baseline": cpu,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
 def run_e2e(args, v, sets, n_sets, is_dcut, T, rows, w, device, positions, dist):
     """Same metric through the public C-ABI calls, with every step's inputs
     copied from pinned host memory and its results read back."""
@@ -1129,6 +1336,8 @@ def main(argv=None):
         run_reference(args, dist)
     elif args.workload in DRAFT_WORKLOADS:
         run_draft(args, dist)
+    elif args.shards:
+        run_sharded(args, dist)
     else:
         run_ours(args, dist)
 

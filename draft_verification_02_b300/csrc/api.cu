@@ -323,6 +323,182 @@ int spec_acceptance_stats(const int32_t *accept_len, const int32_t *cu_draft, in
     return cuda_status(sv::launch_acceptance_stats(a, (cudaStream_t)stream, tr));
 }
 
+// ---- vocabulary-sharded verification ----
+
+size_t spec_shard_workspace_size(int32_t B, int64_t max_target_rows, int32_t V_shard)
+{
+    if (check_verify_sizes(B, V_shard, max_target_rows, 0) != SPEC_OK)
+        return 0;
+    return sv::shard_ws_bytes(B, max_target_rows);
+}
+
+int64_t spec_shard_row_count(int32_t B, int64_t max_target_rows, int32_t draft_stride)
+{
+    if (check_verify_sizes(B, 1, max_target_rows, draft_stride) != SPEC_OK)
+        return -1;
+    return max_target_rows + (draft_stride > 0 ? (int64_t)B * draft_stride : max_target_rows - B);
+}
+
+int spec_shard_row_stats(const void *target_shard, const void *draft_shard, int dtype,
+                         const int32_t *draft_tokens, const int32_t *cu_draft, int32_t B,
+                         int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                         int32_t draft_stride, float temperature, spec_shard_row *out_rows,
+                         void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (!valid_dtype(dtype) || !(temperature >= 0.f) || std::isinf(temperature) ||
+        v_begin < 0 || v_end <= v_begin)
+        return SPEC_ERR_INVALID_ARG;
+    const int32_t Vs = v_end - v_begin;
+    int st = check_verify_sizes(B, Vs, max_target_rows, draft_stride);
+    if (st != SPEC_OK)
+        return st;
+    if (B == 0)
+        return SPEC_OK;
+    const bool drafts = max_target_rows > B, greedy = temperature == 0.f;
+    if (!target_shard || !cu_draft || !out_rows || (drafts && !draft_tokens) ||
+        (drafts && !greedy && !draft_shard))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < sv::shard_ws_bytes(B, max_target_rows))
+        return SPEC_ERR_WORKSPACE;
+    sv::ShardStatsArgs a{};
+    a.v.target = target_shard;
+    a.v.draft = greedy ? nullptr : draft_shard;
+    a.v.dtype = dtype;
+    a.v.tokens = draft_tokens;
+    a.v.cu = cu_draft;
+    a.v.B = B;
+    a.v.V = Vs;
+    a.v.max_rows = max_target_rows;
+    a.v.draft_stride = draft_stride;
+    a.v.temperature = (double)temperature;
+    a.v.ws = workspace;
+    a.v.debug_item = g_expire_unit;
+    a.v_begin = v_begin;
+    a.out_rows = out_rows;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_shard_stats(a, (cudaStream_t)stream, tr));
+}
+
+int spec_shard_accept(const spec_shard_row *rows_all, int32_t n_shards,
+                      const int32_t *shard_begin, const int32_t *draft_tokens,
+                      const int32_t *cu_draft, int32_t B, int64_t max_target_rows,
+                      int32_t draft_stride, float temperature, const float *u_accept,
+                      int32_t *out_tokens, int32_t *out_accept_len, float *out_p, float *out_q,
+                      void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (n_shards < 1 || n_shards > sv::kMaxShards || !shard_begin || !(temperature >= 0.f) ||
+        std::isinf(temperature))
+        return SPEC_ERR_INVALID_ARG;
+    if (shard_begin[0] != 0)
+        return SPEC_ERR_INVALID_ARG;
+    for (int r = 0; r < n_shards; ++r)
+        if (shard_begin[r + 1] <= shard_begin[r])
+            return SPEC_ERR_INVALID_ARG;
+    int st = check_verify_sizes(B, shard_begin[n_shards], max_target_rows, draft_stride);
+    if (st != SPEC_OK)
+        return st;
+    if (B == 0)
+        return SPEC_OK;
+    const bool drafts = max_target_rows > B, greedy = temperature == 0.f;
+    if (!rows_all || !cu_draft || !out_tokens || !out_accept_len || (drafts && !draft_tokens) ||
+        (drafts && !greedy && !u_accept))
+        return SPEC_ERR_INVALID_ARG;
+    if (!workspace || ws_bytes < sv::shard_ws_bytes(B, max_target_rows))
+        return SPEC_ERR_WORKSPACE;
+    sv::ShardAcceptArgs a{};
+    a.rows_all = rows_all;
+    a.n_shards = n_shards;
+    a.begin = shard_begin;
+    a.tokens = draft_tokens;
+    a.cu = cu_draft;
+    a.B = B;
+    a.max_rows = max_target_rows;
+    a.draft_stride = draft_stride;
+    a.temperature = (double)temperature;
+    a.u_accept = u_accept;
+    a.out_tokens = out_tokens;
+    a.out_len = out_accept_len;
+    a.out_p = greedy ? nullptr : out_p;
+    a.out_q = greedy ? nullptr : out_q;
+    a.ws = workspace;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_shard_accept(a, (cudaStream_t)stream, tr));
+}
+
+namespace {
+
+// Checks shared by the two draw steps; fills the common arguments.
+int shard_draw_args(const void *target_shard, const void *draft_shard, int dtype, int32_t B,
+                    int32_t v_begin, int32_t v_end, int64_t max_target_rows, int32_t draft_stride,
+                    void *workspace, size_t ws_bytes, sv::ShardDrawArgs &a)
+{
+    if (!valid_dtype(dtype) || v_begin < 0 || v_end <= v_begin)
+        return SPEC_ERR_INVALID_ARG;
+    const int32_t Vs = v_end - v_begin;
+    int st = check_verify_sizes(B, Vs, max_target_rows, draft_stride);
+    if (st != SPEC_OK)
+        return st;
+    if (!sv::shard_columns_ok(Vs, dtype))
+        return SPEC_ERR_INVALID_ARG;
+    if (B > 0 && (!target_shard || (max_target_rows > B && !draft_shard)))
+        return SPEC_ERR_INVALID_ARG;
+    if (B > 0 && (!workspace || ws_bytes < sv::shard_ws_bytes(B, max_target_rows)))
+        return SPEC_ERR_WORKSPACE;
+    a.target = target_shard;
+    a.draft = draft_shard;
+    a.dtype = dtype;
+    a.B = B;
+    a.v_begin = v_begin;
+    a.V_shard = Vs;
+    a.max_rows = max_target_rows;
+    a.draft_stride = draft_stride;
+    a.ws = workspace;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+int spec_shard_final_mass(const void *target_shard, const void *draft_shard, int dtype,
+                          int32_t B, int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                          int32_t draft_stride, spec_shard_mass *out_mass, void *workspace,
+                          size_t ws_bytes, spec_stream_t stream)
+{
+    sv::ShardDrawArgs a{};
+    int st = shard_draw_args(target_shard, draft_shard, dtype, B, v_begin, v_end, max_target_rows,
+                             draft_stride, workspace, ws_bytes, a);
+    if (st != SPEC_OK || B == 0)
+        return st;
+    if (!out_mass)
+        return SPEC_ERR_INVALID_ARG;
+    a.out_mass = out_mass;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_shard_mass(a, (cudaStream_t)stream, tr));
+}
+
+int spec_shard_final_draw(const void *target_shard, const void *draft_shard, int dtype,
+                          const spec_shard_mass *mass_all, int32_t n_shards, int32_t shard,
+                          int32_t B, int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                          int32_t draft_stride, const float *u_final, int32_t *out_tokens,
+                          void *workspace, size_t ws_bytes, spec_stream_t stream)
+{
+    if (n_shards < 1 || n_shards > sv::kMaxShards || shard < 0 || shard >= n_shards)
+        return SPEC_ERR_INVALID_ARG;
+    sv::ShardDrawArgs a{};
+    int st = shard_draw_args(target_shard, draft_shard, dtype, B, v_begin, v_end, max_target_rows,
+                             draft_stride, workspace, ws_bytes, a);
+    if (st != SPEC_OK || B == 0)
+        return st;
+    if (!mass_all || !u_final || !out_tokens)
+        return SPEC_ERR_INVALID_ARG;
+    a.mass_all = mass_all;
+    a.n_shards = n_shards;
+    a.shard = shard;
+    a.u_final = u_final;
+    a.out_tokens = out_tokens;
+    sv::Tracer tr = make_tracer();
+    return cuda_status(sv::launch_shard_draw(a, (cudaStream_t)stream, tr));
+}
+
 int spec_get_device_status(void *workspace, spec_stream_t stream)
 {
     if (!workspace)

@@ -92,18 +92,22 @@ __device__ __forceinline__ void row_span(const Geometry &g, int64_t rg, int &wf,
     wl = owner_of(ua + g.cpr - 1, g);
 }
 
-// T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
-__device__ __forceinline__ int merge_argmax_row(const Partial *part, const Geometry &g, int64_t rg)
+// T = 0: the maximum of flattened row rg and the lowest index holding it
+// (INT_MAX when every entry is -inf), merged from the row's partials; nan is
+// set when any entry is NaN.  The same result in every lane.
+__device__ __forceinline__ void merge_argmax_pair(const Partial *part, const Geometry &g,
+                                                  int64_t rg, float &best, int &bidx, bool &nan)
 {
     const int lane = threadIdx.x & 31;
     int wf, wl;
     row_span(g, rg, wf, wl);
-    float best = -INFINITY;
-    int bidx = INT_MAX, nan = 0;
+    best = -INFINITY;
+    bidx = INT_MAX;
+    int bad = 0;
     for (int w = wf + lane; w <= wl; w += 32) {
         const Partial q = load_partial(part + rg + w);
         if (q.idx == -2)
-            nan = 1;
+            bad = 1;
         else if (q.idx >= 0 && (q.m > best || (q.m == best && q.idx < bidx))) {
             best = q.m;
             bidx = q.idx;
@@ -118,7 +122,16 @@ __device__ __forceinline__ int merge_argmax_row(const Partial *part, const Geome
             bidx = oi;
         }
     }
-    nan = __any_sync(0xffffffffu, nan);
+    nan = __any_sync(0xffffffffu, bad);
+}
+
+// T = 0: lowest argmax of target row rg; -1 masked row, -2 NaN, -3 +inf.
+__device__ __forceinline__ int merge_argmax_row(const Partial *part, const Geometry &g, int64_t rg)
+{
+    float best;
+    int bidx;
+    bool nan;
+    merge_argmax_pair(part, g, rg, best, bidx, nan);
     return nan ? -2 : (bidx == INT_MAX ? -1 : (best == INFINITY ? -3 : bidx));
 }
 
@@ -443,6 +456,115 @@ struct DrawShared {
     ff *s_total;  // S, the sum of every weight (may be null)
 };
 
+// The search of the CTA whose range [r0, r1) (nsl slices with totals
+// slice_tot, in order) holds the target: base is the running sum before the
+// range; past marks a target at or beyond the end of the whole sum after
+// rounding (then the last element with weight > 0 wins).  The slice, then the
+// thread piece, then the element; `weighed` is the slice already staged (-1
+// none).  Returns the drawn index (or -1 if none has weight), in every thread.
+template <typename T, bool OUTLINE>
+__device__ __forceinline__ int find_in_range(const FinishParams &p, const DrawCtx &d,
+                                             const T *trow, const T *drow, int r0, int r1,
+                                             int nsl, ff base, ff target, bool past, int weighed,
+                                             const ff *slice_tot, const DrawShared<T> &sh,
+                                             uint32_t &phase)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    T *tb = sh.tb, *db = sh.db;
+    float *piece = sh.piece;
+    ff *wred = sh.wred, *s_excl = sh.s_excl;
+    int &s_hit = *sh.s_hit, &s_last = *sh.s_last, &s_expired = *sh.s_expired;
+    uint64_t &bar = *sh.bar;
+    int sl = -1;
+    {
+        ff b2 = base;
+        for (int s2 = 0; s2 < nsl && !past; ++s2) {
+            const ff next = ff_add(b2, slice_tot[s2]);
+            if (ff_gt(next, target)) {
+                sl = s2;
+                break;
+            }
+            b2 = next;
+        }
+        if (sl >= 0) {
+            base = b2;
+        } else {  // the last slice with mass
+            past = true;
+            ff bl = base;
+            b2 = base;
+            sl = nsl - 1;
+            for (int s2 = 0; s2 < nsl; ++s2) {
+                if (slice_tot[s2].hi > 0.f) {
+                    sl = s2;
+                    bl = b2;
+                }
+                b2 = ff_add(b2, slice_tot[s2]);
+            }
+            base = bl;
+        }
+    }
+    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
+    if (sl != weighed) {
+        if (OUTLINE)
+            weigh_slice_outlined<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
+                                    &s_expired, true);
+        else
+            weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
+                           &s_expired);
+    }
+    // scan of the piece sums (float-float, fixed order).  A piece's lower end
+    // is the previous piece's upper end bit for bit, so the pieces tile the
+    // slice with no gap and no overlap.
+    ff incl{piece[tid], 0.f};
+#pragma unroll 1
+    for (int o = 1; o < 32; o <<= 1) {
+        const ff n = ff_shfl_up(incl, o);
+        if (lane >= o)
+            incl = ff_add(n, incl);
+    }
+    ff excl = ff_shfl_up(incl, 1);
+    if (lane == 0)
+        excl = {0.f, 0.f};
+    if (tid == 0) {
+        s_hit = INT_MAX;
+        s_last = -1;
+    }
+    if (lane == 31)
+        s_excl[warp] = incl;
+    __syncthreads();
+    ff wbase = base;
+    for (int q = 0; q < warp; ++q)
+        wbase = ff_add(wbase, s_excl[q]);
+    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
+    if (!past && ff_le(lo, target) && ff_gt(hi, target))
+        atomicMin(&s_hit, tid);
+    __syncthreads();
+    // the piece walk repeats the piece sum's additions, so it meets the same
+    // running sums; rem may round up to the piece total: then the piece's
+    // last element with weight > 0
+    constexpr int E = Elem<T>::kPerVec;
+    const int nv = (len + E - 1) / E;
+    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
+    const int hit = s_hit;
+    if (hit != INT_MAX) {
+        if (warp == hit >> 5) {  // the hit thread's warp walks its piece
+            const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
+            const int hl = hit & 31;
+            const int k = piece_find_warp<T>(d, tb, db, len, __shfl_sync(0xffffffffu, v0, hl),
+                                             __shfl_sync(0xffffffffu, v1, hl),
+                                             __shfl_sync(0xffffffffu, rem, hl), piece);
+            if (lane == 0)
+                s_last = k;
+        }
+    } else {  // past the end after rounding: the last element with mass
+        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
+        if (lp >= 0)
+            atomicMax(&s_last, lp);
+    }
+    __syncthreads();
+    return s_last >= 0 ? c0 + s_last : -1;
+}
+
 // The final draw of one cluster: the CTAs split the vocabulary into ncl
 // ranges, weigh theirs (w = max(0, p - q) with d.resid, else the unnormalised
 // p), exchange the range sums through distributed shared memory, and the CTA
@@ -459,12 +581,12 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
                                           const DrawShared<T> &sh, int staged = -1,
                                           uint32_t *phase_io = nullptr)
 {
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x, lane = tid & 31;
     T *tb = sh.tb, *db = sh.db;
     float *piece = sh.piece;
-    ff *wred = sh.wred, *slice_tot = sh.slice_tot, *s_excl = sh.s_excl;
+    ff *wred = sh.wred, *slice_tot = sh.slice_tot;
     ff(*cl_sum)[kCluster] = sh.cl_sum;
-    int &s_hit = *sh.s_hit, &s_last = *sh.s_last, &s_expired = *sh.s_expired;
+    int &s_expired = *sh.s_expired;
     uint64_t &bar = *sh.bar;
     const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
     const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
@@ -534,97 +656,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     if ((int)rank != cs)
         return cs < 0 ? -1 : -2;  // -1: no mass at all (never with finite rows)
 
-    // ---- owner CTA: the slice, then the thread piece, then the element
-    int sl = -1;
-    {
-        ff b2 = base;
-        for (int s2 = 0; s2 < nsl && !past; ++s2) {
-            const ff next = ff_add(b2, slice_tot[s2]);
-            if (ff_gt(next, target)) {
-                sl = s2;
-                break;
-            }
-            b2 = next;
-        }
-        if (sl >= 0) {
-            base = b2;
-        } else {  // the last slice with mass
-            past = true;
-            ff bl = base;
-            b2 = base;
-            sl = nsl - 1;
-            for (int s2 = 0; s2 < nsl; ++s2) {
-                if (slice_tot[s2].hi > 0.f) {
-                    sl = s2;
-                    bl = b2;
-                }
-                b2 = ff_add(b2, slice_tot[s2]);
-            }
-            base = bl;
-        }
-    }
-    const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-    if (sl != weighed) {
-        if (OUTLINE)
-            weigh_slice_outlined<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
-                                    &s_expired, true);
-        else
-            weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece, wred,
-                           &s_expired);
-        if (phase_io)
-            *phase_io = phase;
-    }
-    // scan of the piece sums (float-float, fixed order).  A piece's lower end
-    // is the previous piece's upper end bit for bit, so the pieces tile the
-    // slice with no gap and no overlap.
-    ff incl{piece[tid], 0.f};
-#pragma unroll 1
-    for (int o = 1; o < 32; o <<= 1) {
-        const ff n = ff_shfl_up(incl, o);
-        if (lane >= o)
-            incl = ff_add(n, incl);
-    }
-    ff excl = ff_shfl_up(incl, 1);
-    if (lane == 0)
-        excl = {0.f, 0.f};
-    if (tid == 0) {
-        s_hit = INT_MAX;
-        s_last = -1;
-    }
-    if (lane == 31)
-        s_excl[warp] = incl;
-    __syncthreads();
-    ff wbase = base;
-    for (int q = 0; q < warp; ++q)
-        wbase = ff_add(wbase, s_excl[q]);
-    const ff lo = ff_add(wbase, excl), hi = ff_add(wbase, incl);
-    if (!past && ff_le(lo, target) && ff_gt(hi, target))
-        atomicMin(&s_hit, tid);
-    __syncthreads();
-    // the piece walk repeats the piece sum's additions, so it meets the same
-    // running sums; rem may round up to the piece total: then the piece's
-    // last element with weight > 0
-    constexpr int E = Elem<T>::kPerVec;
-    const int nv = (len + E - 1) / E;
-    const int v0 = min(nv, tid * p.pv), v1 = min(nv, v0 + p.pv);
-    const int hit = s_hit;
-    if (hit != INT_MAX) {
-        if (warp == hit >> 5) {  // the hit thread's warp walks its piece
-            const float rem = __fadd_rn(__fsub_rn(target.hi, lo.hi), __fsub_rn(target.lo, lo.lo));
-            const int hl = hit & 31;
-            const int k = piece_find_warp<T>(d, tb, db, len, __shfl_sync(0xffffffffu, v0, hl),
-                                             __shfl_sync(0xffffffffu, v1, hl),
-                                             __shfl_sync(0xffffffffu, rem, hl), piece);
-            if (lane == 0)
-                s_last = k;
-        }
-    } else {  // past the end after rounding: the last element with mass
-        const int lp = piece_find<T>(d, tb, db, len, v0, v1, INFINITY);
-        if (lp >= 0)
-            atomicMax(&s_last, lp);
-    }
-    __syncthreads();
-    return s_last >= 0 ? c0 + s_last : -1;
+    const int y = find_in_range<T, OUTLINE>(p, d, trow, drow, r0, r1, nsl, base, target, past,
+                                            weighed, slice_tot, sh, phase);
+    if (phase_io)
+        *phase_io = phase;
+    return y;
 }
 
 template <typename T, bool OUTLINE>
@@ -1323,67 +1359,6 @@ __global__ void __launch_bounds__(kFinishThreads) draft_greedy_kernel(const Fini
         }
         p.out_tokens[r] = y;
         p.out_conf[r] = conf;
-    }
-}
-
-// Acceptance statistics of one verification call, one CTA: per position j
-// the requests that tested it (K_i > j, a_i >= j) and accepted it (a_i > j),
-// and the mean accepted length over requests with a_i >= 0.  Integer counts,
-// so the result does not depend on the order of the atomic adds.
-constexpr int kStatsThreads = 1024;
-
-struct StatsParams {
-    const int32_t *accept_len;
-    const int32_t *cu;
-    int B, Kmax;
-    int32_t *out_reached;
-    int32_t *out_accepted;
-    float *out_mean;
-    uint32_t *status;
-};
-
-__global__ void __launch_bounds__(kStatsThreads) acceptance_stats_kernel(const StatsParams p)
-{
-    __shared__ int reached[kMaxDraft], accepted[kMaxDraft];
-    __shared__ unsigned long long total;
-    __shared__ int n, bad;
-    const int tid = threadIdx.x;
-    if (tid < kMaxDraft)
-        reached[tid] = accepted[tid] = 0;
-    if (tid == 0) {
-        total = 0ull;
-        n = 0;
-        bad = 0;
-    }
-    __syncthreads();
-    for (int i = tid; i < p.B; i += kStatsThreads) {
-        const int a = __ldg(p.accept_len + i);
-        const int k = __ldg(p.cu + i + 1) - __ldg(p.cu + i);
-        if (a < 0)
-            continue;  // a poisoned request
-        if (a > k || k > p.Kmax || k < 0) {
-            bad = 1;
-            continue;
-        }
-        atomicAdd(&total, (unsigned long long)a);
-        atomicAdd(&n, 1);
-        for (int j = 0; j < k; ++j) {
-            if (a >= j)
-                atomicAdd(&reached[j], 1);
-            if (a > j)
-                atomicAdd(&accepted[j], 1);
-        }
-    }
-    __syncthreads();
-    if (tid < p.Kmax) {
-        p.out_reached[tid] = bad ? -1 : reached[tid];
-        p.out_accepted[tid] = bad ? -1 : accepted[tid];
-    }
-    if (tid == 0) {
-        if (bad)
-            set_status(p.status, ST_INVALID);
-        *p.out_mean = bad ? __int_as_float(0x7fc00000)
-                          : (n > 0 ? (float)((double)total / (double)n) : 0.f);
     }
 }
 

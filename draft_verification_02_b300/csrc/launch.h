@@ -117,4 +117,56 @@ struct StatsArgs {
 
 cudaError_t launch_acceptance_stats(const StatsArgs &a, cudaStream_t stream, Tracer &tr);
 
+// Vocabulary-sharded verification (shard.cu): one shard's four steps.
+constexpr int kMaxShards = 32;
+
+struct ShardStatsArgs {
+    VerifyArgs v;  // the shard's logits (v.V = its column count); no outputs
+    int v_begin;   // global token of the shard's column 0
+    void *out_rows;
+};
+
+struct ShardAcceptArgs {
+    const void *rows_all;  // [n_shards][rows]
+    int n_shards;
+    const int32_t *begin;  // host, n_shards + 1
+    const int32_t *tokens;
+    const int32_t *cu;
+    int B;
+    int64_t max_rows;
+    int draft_stride;
+    double temperature;
+    const float *u_accept;
+    int32_t *out_tokens;
+    int32_t *out_len;
+    float *out_p;
+    float *out_q;
+    void *ws;
+};
+
+struct ShardDrawArgs {
+    const void *target;
+    const void *draft;
+    int dtype;
+    int B;
+    int v_begin;
+    int V_shard;
+    int64_t max_rows;
+    int draft_stride;
+    void *out_mass;        // step 3
+    const void *mass_all;  // step 4: [n_shards][B]
+    int n_shards;
+    int shard;
+    const float *u_final;
+    int32_t *out_tokens;
+    void *ws;
+};
+
+size_t shard_ws_bytes(int B, int64_t max_rows);
+bool shard_columns_ok(int V_shard, int dtype);  // the draw's slice table holds V_shard columns
+cudaError_t launch_shard_stats(const ShardStatsArgs &a, cudaStream_t stream, Tracer &tr);
+cudaError_t launch_shard_accept(const ShardAcceptArgs &a, cudaStream_t stream, Tracer &tr);
+cudaError_t launch_shard_mass(const ShardDrawArgs &a, cudaStream_t stream, Tracer &tr);
+cudaError_t launch_shard_draw(const ShardDrawArgs &a, cudaStream_t stream, Tracer &tr);
+
 }  // namespace sv

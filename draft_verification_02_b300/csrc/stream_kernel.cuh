@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
                 if (bad)
                     set_status(p.status, ST_INVALID);
             }
-            if (bad) {
+            if (bad && p.out_tokens) {  // (a shard's row pass has no outputs to poison)
                 for (int64_t k = threadIdx.x; k < g.max_rows; k += kStreamThreads)
                     p.out_tokens[k] = -1;
                 for (int k = threadIdx.x; k < B; k += kStreamThreads)

@@ -54,6 +54,67 @@
 
 namespace sv {
 
+// Acceptance statistics of one verification call, one CTA: per position j
+// the requests that tested it (K_i > j, a_i >= j) and accepted it (a_i > j),
+// and the mean accepted length over requests with a_i >= 0.  Integer counts,
+// so the result does not depend on the order of the atomic adds.
+constexpr int kStatsThreads = 1024;
+
+struct StatsParams {
+    const int32_t *accept_len;
+    const int32_t *cu;
+    int B, Kmax;
+    int32_t *out_reached;
+    int32_t *out_accepted;
+    float *out_mean;
+    uint32_t *status;
+};
+
+__global__ void __launch_bounds__(kStatsThreads) acceptance_stats_kernel(const StatsParams p)
+{
+    __shared__ int reached[kMaxDraft], accepted[kMaxDraft];
+    __shared__ unsigned long long total;
+    __shared__ int n, bad;
+    const int tid = threadIdx.x;
+    if (tid < kMaxDraft)
+        reached[tid] = accepted[tid] = 0;
+    if (tid == 0) {
+        total = 0ull;
+        n = 0;
+        bad = 0;
+    }
+    __syncthreads();
+    for (int i = tid; i < p.B; i += kStatsThreads) {
+        const int a = __ldg(p.accept_len + i);
+        const int k = __ldg(p.cu + i + 1) - __ldg(p.cu + i);
+        if (a < 0)
+            continue;  // a poisoned request
+        if (a > k || k > p.Kmax || k < 0) {
+            bad = 1;
+            continue;
+        }
+        atomicAdd(&total, (unsigned long long)a);
+        atomicAdd(&n, 1);
+        for (int j = 0; j < k; ++j) {
+            if (a >= j)
+                atomicAdd(&reached[j], 1);
+            if (a > j)
+                atomicAdd(&accepted[j], 1);
+        }
+    }
+    __syncthreads();
+    if (tid < p.Kmax) {
+        p.out_reached[tid] = bad ? -1 : reached[tid];
+        p.out_accepted[tid] = bad ? -1 : accepted[tid];
+    }
+    if (tid == 0) {
+        if (bad)
+            set_status(p.status, ST_INVALID);
+        *p.out_mean = bad ? __int_as_float(0x7fc00000)
+                          : (n > 0 ? (float)((double)total / (double)n) : 0.f);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -178,8 +239,10 @@ static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e, int ncl
     return (R + slice - 1) / slice <= kMaxSlices;
 }
 
+// Kernel 1's parameters for a verification call (a.out_tokens / a.out_len
+// may be null: then malformed offsets are only flagged, not poisoned).
 template <typename T, bool GREEDY>
-static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
+static StreamParams stream_params(const VerifyArgs &a)
 {
     const int e = (int)sizeof(T);
     const WsLayout L = ws_layout(a.B, a.max_rows, a.V);
@@ -213,6 +276,46 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     sp.part_cap = (int64_t)((L.total - L.part1) / sizeof(Partial));
     sp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
     sp.debug_unit = a.debug_item;
+    return sp;
+}
+
+template <typename T, bool GREEDY>
+static cudaError_t enqueue_stream(const StreamParams &sp, cudaStream_t s, Tracer &tr)
+{
+    cudaError_t err = prepare_stream<T, GREEDY>();
+    if (err != cudaSuccess)
+        return err;
+    const int grid1 = (sp.g.P + kStreamWarps - 1) / kStreamWarps;
+    const size_t smem1 = (size_t)kStreamWarps * kRing * sp.piece_smem +
+                         (sp.draft_stride > 0 && !GREEDY ? 4 * (size_t)(sp.B + 1) : 0);
+    tr.begin(s);
+    stream_kernel<T, GREEDY><<<grid1, kStreamThreads, smem1, s>>>(sp);
+    if ((err = cudaGetLastError()) != cudaSuccess)
+        return err;
+    tr.after_kernel(s);
+    return cudaSuccess;
+}
+
+cudaError_t launch_stream_pass(const VerifyArgs &a, cudaStream_t s, Tracer &tr, StreamParams &sp)
+{
+    const bool greedy = a.temperature == 0.0;
+    if (a.dtype == 0) {
+        sp = greedy ? stream_params<float, true>(a) : stream_params<float, false>(a);
+        return greedy ? enqueue_stream<float, true>(sp, s, tr)
+                      : enqueue_stream<float, false>(sp, s, tr);
+    }
+    sp = greedy ? stream_params<uint16_t, true>(a) : stream_params<uint16_t, false>(a);
+    return greedy ? enqueue_stream<uint16_t, true>(sp, s, tr)
+                  : enqueue_stream<uint16_t, false>(sp, s, tr);
+}
+
+template <typename T, bool GREEDY>
+static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
+{
+    const int e = (int)sizeof(T);
+    const StreamParams sp = stream_params<T, GREEDY>(a);
+    const Geometry g = sp.g;
+    const bool tma = sp.tma != 0;
 
     FinishParams fp{};
     fp.target = a.target;
@@ -242,7 +345,6 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.part = sp.part;
     fp.part_cap = sp.part_cap;
 
-    cudaError_t err = prepare_stream<T, GREEDY>();
     // The finish kernel with its weighing out of line (more registers, at
     // most two CTAs per SM) when its CTAs can each have an SM and the rows
     // are long, inline otherwise (72 registers, three CTAs per SM).  Measured
@@ -250,18 +352,13 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     // B=4, V=1024 10.4 inline vs 10.9; B=32 and B=64 at V >= 128000 0.7-3.3 us
     // faster inline.
     const bool outline = (int64_t)a.B * fp.ncl <= (int64_t)sm_count() && a.V >= 32768;
-    if (err == cudaSuccess && !GREEDY)
+    cudaError_t err = cudaSuccess;
+    if (!GREEDY)
         err = outline ? prepare_finish_sample<T, true>() : prepare_finish_sample<T, false>();
     if (err != cudaSuccess)
         return err;
-    const int grid1 = (g.P + kStreamWarps - 1) / kStreamWarps;
-    const size_t smem1 = (size_t)kStreamWarps * kRing * sp.piece_smem +
-                         (a.draft_stride > 0 ? 4 * (size_t)(a.B + 1) : 0);
-    tr.begin(s);
-    stream_kernel<T, GREEDY><<<grid1, kStreamThreads, smem1, s>>>(sp);
-    if ((err = cudaGetLastError()) != cudaSuccess)
+    if ((err = enqueue_stream<T, GREEDY>(sp, s, tr)) != cudaSuccess)
         return err;
-    tr.after_kernel(s);
 
     cudaLaunchConfig_t cfg{};
     cfg.blockDim = dim3(kFinishThreads);

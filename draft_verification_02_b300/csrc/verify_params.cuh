@@ -130,4 +130,8 @@ __device__ __forceinline__ int64_t draft_index(int draft_stride, const int32_t *
     return draft_stride > 0 ? (int64_t)i * draft_stride + j : (int64_t)__ldg(cu + i) + j;
 }
 
+// Enqueue kernel 1 alone for a verification call (verify.cu) and return its
+// parameters (where the partials are, the unit geometry).
+cudaError_t launch_stream_pass(const VerifyArgs &a, cudaStream_t s, Tracer &tr, StreamParams &sp);
+
 }  // namespace sv

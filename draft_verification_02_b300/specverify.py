@@ -34,7 +34,11 @@ EXPORTS = ("spec_workspace_size", "spec_workspace_init", "spec_verify_greedy",
            "spec_verify_sample", "dcut_allocate", "spec_get_device_status",
            "spec_status_string", "spec_set_trace", "spec_kernel_launch_count",
            "spec_verify_sample_static", "dcut_allocate_cost", "spec_draft_confidence",
-           "spec_draft_sample", "spec_acceptance_stats", "spec_test_expire_wait")
+           "spec_draft_sample", "spec_acceptance_stats", "spec_test_expire_wait",
+           "spec_shard_workspace_size", "spec_shard_row_count", "spec_shard_row_stats",
+           "spec_shard_accept", "spec_shard_final_mass", "spec_shard_final_draw")
+SPEC_MAX_SHARDS = 32
+SHARD_RECORD_FLOATS = 4  # spec_shard_row and spec_shard_mass: 16 bytes each
 SPEC_STATIC_SCRATCH_BYTES = 1 << 20
 
 
@@ -85,6 +89,21 @@ def _load():
     lib.spec_kernel_launch_count.restype = I64
     lib.spec_test_expire_wait.argtypes = [I64]
     lib.spec_test_expire_wait.restype = INT
+    lib.spec_shard_workspace_size.argtypes = [I32, I64, I32]
+    lib.spec_shard_workspace_size.restype = SZ
+    lib.spec_shard_row_count.argtypes = [I32, I64, I32]
+    lib.spec_shard_row_count.restype = I64
+    lib.spec_shard_row_stats.argtypes = [P, P, INT, P, P, I32, I32, I32, I64, I32, F32, P, P, SZ,
+                                         P]
+    lib.spec_shard_row_stats.restype = INT
+    lib.spec_shard_accept.argtypes = [P, I32, ctypes.POINTER(I32), P, P, I32, I64, I32, F32, P,
+                                      P, P, P, P, P, SZ, P]
+    lib.spec_shard_accept.restype = INT
+    lib.spec_shard_final_mass.argtypes = [P, P, INT, I32, I32, I32, I64, I32, P, P, SZ, P]
+    lib.spec_shard_final_mass.restype = INT
+    lib.spec_shard_final_draw.argtypes = [P, P, INT, P, I32, I32, I32, I32, I32, I64, I32, P, P,
+                                          P, SZ, P]
+    lib.spec_shard_final_draw.restype = INT
     return lib
 
 
@@ -285,6 +304,105 @@ def spec_acceptance_stats(accept_len, cu_draft, B: int, Kmax: int, out_reached, 
         _dev(out_reached, "out_reached", torch.int32, Kmax, allow_none=Kmax == 0),
         _dev(out_accepted, "out_accepted", torch.int32, Kmax, allow_none=Kmax == 0),
         _dev(out_mean, "out_mean", torch.float32, 1),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+# ---- vocabulary-sharded verification (records: float32 tensors of 4 per row / request)
+
+
+def spec_shard_workspace_size(B: int, max_target_rows: int, V_shard: int) -> int:
+    return int(LIB.spec_shard_workspace_size(B, max_target_rows, V_shard))
+
+
+def spec_shard_row_count(B: int, max_target_rows: int, draft_stride: int) -> int:
+    return int(LIB.spec_shard_row_count(B, max_target_rows, draft_stride))
+
+
+def _records(t, name, n):
+    return _dev(t, name, torch.float32, n * SHARD_RECORD_FLOATS)
+
+
+def spec_shard_row_stats(target_shard, draft_shard, draft_tokens, cu_draft, B: int, v_begin: int,
+                         v_end: int, max_target_rows: int, draft_stride: int, temperature: float,
+                         out_rows, workspace, stream=None) -> int:
+    if B == 0:
+        return SPEC_OK
+    Vs = v_end - v_begin
+    nd = _draft_extent(B, max_target_rows, draft_stride)
+    greedy = temperature == 0
+    need_draft = (not greedy) and nd > 0
+    if need_draft and draft_shard is not None and draft_shard.dtype != target_shard.dtype:
+        raise TypeError("target and draft logits must share a dtype")
+    return LIB.spec_shard_row_stats(
+        _dev(target_shard, "target_shard", min_numel=max_target_rows * Vs),
+        _dev(draft_shard, "draft_shard", min_numel=nd * Vs, allow_none=not need_draft),
+        dtype_code(target_shard),
+        _dev(draft_tokens, "draft_tokens", torch.int32, nd, allow_none=nd == 0),
+        _dev(cu_draft, "cu_draft", torch.int32, B + 1), B, v_begin, v_end, max_target_rows,
+        draft_stride, float(temperature),
+        _records(out_rows, "out_rows", spec_shard_row_count(B, max_target_rows, draft_stride)),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_shard_accept(rows_all, n_shards: int, shard_begin, draft_tokens, cu_draft, B: int,
+                      max_target_rows: int, draft_stride: int, temperature: float, u_accept,
+                      out_tokens, out_accept_len, out_p, out_q, workspace, stream=None) -> int:
+    """shard_begin: a host sequence of n_shards + 1 ints."""
+    if B == 0:
+        return SPEC_OK
+    begin = [int(v) for v in shard_begin]
+    if len(begin) != n_shards + 1:
+        raise ValueError("shard_begin must hold n_shards + 1 entries")
+    nd = _draft_extent(B, max_target_rows, draft_stride)
+    greedy = temperature == 0
+    n_rec = spec_shard_row_count(B, max_target_rows, draft_stride)
+    return LIB.spec_shard_accept(
+        _records(rows_all, "rows_all", n_shards * n_rec), n_shards,
+        (ctypes.c_int32 * len(begin))(*begin),
+        _dev(draft_tokens, "draft_tokens", torch.int32, nd, allow_none=nd == 0),
+        _dev(cu_draft, "cu_draft", torch.int32, B + 1), B, max_target_rows, draft_stride,
+        float(temperature),
+        _dev(u_accept, "u_accept", torch.float32, nd, allow_none=greedy or nd == 0),
+        _dev(out_tokens, "out_tokens", torch.int32, max_target_rows),
+        _dev(out_accept_len, "out_accept_len", torch.int32, B),
+        _dev(out_p, "out_p", torch.float32, nd, allow_none=True),
+        _dev(out_q, "out_q", torch.float32, nd, allow_none=True),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_shard_final_mass(target_shard, draft_shard, B: int, v_begin: int, v_end: int,
+                          max_target_rows: int, draft_stride: int, out_mass, workspace,
+                          stream=None) -> int:
+    if B == 0:
+        return SPEC_OK
+    Vs = v_end - v_begin
+    nd = _draft_extent(B, max_target_rows, draft_stride)
+    return LIB.spec_shard_final_mass(
+        _dev(target_shard, "target_shard", min_numel=max_target_rows * Vs),
+        _dev(draft_shard, "draft_shard", min_numel=nd * Vs, allow_none=nd == 0),
+        dtype_code(target_shard), B, v_begin, v_end, max_target_rows, draft_stride,
+        _records(out_mass, "out_mass", B),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+
+
+def spec_shard_final_draw(target_shard, draft_shard, mass_all, n_shards: int, shard: int, B: int,
+                          v_begin: int, v_end: int, max_target_rows: int, draft_stride: int,
+                          u_final, out_tokens, workspace, stream=None) -> int:
+    if B == 0:
+        return SPEC_OK
+    Vs = v_end - v_begin
+    nd = _draft_extent(B, max_target_rows, draft_stride)
+    return LIB.spec_shard_final_draw(
+        _dev(target_shard, "target_shard", min_numel=max_target_rows * Vs),
+        _dev(draft_shard, "draft_shard", min_numel=nd * Vs, allow_none=nd == 0),
+        dtype_code(target_shard), _records(mass_all, "mass_all", n_shards * B), n_shards, shard,
+        B, v_begin, v_end, max_target_rows, draft_stride,
+        _dev(u_final, "u_final", torch.float32, B),
+        _dev(out_tokens, "out_tokens", torch.int32, max_target_rows),
         _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream))
 

@@ -282,6 +282,135 @@ int spec_acceptance_stats(const int32_t *accept_len, const int32_t *cu_draft, in
                           float *out_mean, void *workspace, size_t ws_bytes, spec_stream_t stream);
 
 /*
+ * Vocabulary-sharded verification
+ * -------------------------------
+ * A target served tensor-parallel splits its output projection by vocabulary
+ * (TP = 8 in "Tencent Hunyuan Turns Speculative Decoding Into a Full
+ * Open-Source Stack", section "Key numbers (Hy3-295B-A21B, TP=8)"), so each
+ * rank holds the logits of one contiguous vocabulary range, and so may the
+ * drafter.  These calls verify such a batch without gathering any logit row:
+ * each rank reduces its own columns, and only small per-row and per-request
+ * records cross ranks.  The results are those of spec_verify_sample /
+ * spec_verify_greedy on the whole vocabulary (same layout, same outputs; the
+ * merges round differently, within the same accuracy).
+ *
+ * N shards, shard r holding global tokens [shard_begin[r], shard_begin[r+1])
+ * (shard_begin[0] = 0, strictly increasing, shard_begin[N] = V, N <= 32).
+ * Shard r's logits are target_shard[max_target_rows][V_r] (and draft_shard)
+ * with V_r = shard_begin[r+1] - shard_begin[r]: column c is token
+ * shard_begin[r] + c.  Offsets, drafted tokens and uniforms are the same on
+ * every shard.  One verification is, on every shard, in this order:
+ *   1. spec_shard_row_stats      -> this shard's row records
+ *      (exchange: gather the N shards' records, shard order, on every shard)
+ *   2. spec_shard_accept          -> accepted lengths, accepted tokens, p, q
+ *      T = 0: the verification is complete here.
+ *   3. spec_shard_final_mass      -> this shard's share of the final draw's mass
+ *      (exchange: gather the N shards' masses, shard order)
+ *   4. spec_shard_final_draw      -> the final token where this shard holds it
+ *      (exchange: element-wise max of out_tokens over the shards)
+ * Every shard computes step 2 and the choice of the drawing shard in step 4
+ * from the same gathered bytes with the same code, so all shards agree
+ * bit for bit without further exchange.  The four calls of one
+ * verification use one shard workspace (spec_shard_workspace_size), which
+ * carries the accepted positions and the draw's constants from step 2 to
+ * steps 3 and 4; no other call may use it in between.  Device errors go to
+ * that workspace's status word as for spec_verify_sample (read it with
+ * spec_get_device_status).  Data errors are poisoned identically on every
+ * shard, since they are seen in the gathered records; an expired wait is
+ * seen only by the shard it happened on, so after SPEC_ERR_TIMEOUT on any
+ * shard every output of that verification is unspecified.
+ */
+
+/* One row's record from one shard (16 bytes; exchanged as raw bytes).
+ *   T > 0: m = maximum of the shard's logits in the row, s_hi + s_lo = sum
+ *          over the shard of 2^((l - m) log2(e) / T) (a float-float pair),
+ *          x.gx = the logit at the row's drafted token when this shard holds
+ *          that token (0 otherwise).  NaN or +inf in the row make m or s NaN.
+ *   T = 0: m = maximum, x.arg = global index of its lowest occurrence (-1
+ *          when every entry is -inf, -2 when the row holds a NaN), s = 0. */
+typedef struct {
+    float m;
+    union {
+        float gx;
+        int32_t arg;
+    } x;
+    float s_hi, s_lo;
+} spec_shard_row;
+
+/* One request's share of the final draw's mass on one shard (16 bytes):
+ * w = sum over the shard's columns of the final weights (max(0, p - q) after
+ * a rejection, else the unnormalised p of the bonus row); p = the same sum
+ * of the unnormalised p (kept for the all-zero residual, where the draw
+ * falls back to p).  Float-float pairs. */
+typedef struct {
+    float w_hi, w_lo, p_hi, p_lo;
+} spec_shard_mass;
+
+/* Workspace bytes for one shard of V_shard columns (0 for invalid sizes);
+ * zero-fill it once before first use (spec_workspace_init). */
+size_t spec_shard_workspace_size(int32_t B, int64_t max_target_rows, int32_t V_shard);
+
+/* Records per shard: max_target_rows target rows, then the draft rows
+ * (max_target_rows - B packed, or B * draft_stride padded), by draft index.
+ * Records of rows past cu_draft[B] + B (and of padding rows) are not written. */
+int64_t spec_shard_row_count(int32_t B, int64_t max_target_rows, int32_t draft_stride);
+
+/*
+ * Step 1: this shard's record of every target row and (T > 0) every draft
+ * row.  Reads this shard's logits once (the streaming pass of
+ * spec_verify_sample over V_r columns) and merges each row.  Two launches.
+ *   out_rows  spec_shard_row [spec_shard_row_count(B, max_target_rows, draft_stride)]
+ */
+int spec_shard_row_stats(const void *target_shard, const void *draft_shard, int dtype,
+                         const int32_t *draft_tokens, const int32_t *cu_draft, int32_t B,
+                         int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                         int32_t draft_stride, float temperature, spec_shard_row *out_rows,
+                         void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Step 2: merge the N shards' records of each row (in shard order), run the
+ * accept test and the first-rejection scan, and write out_accept_len,
+ * out_p / out_q (T > 0; may be NULL) and out_tokens except each request's
+ * final position (T > 0: -1 there until step 4).  T = 0 writes the final
+ * token too (the merged argmax).  One launch.
+ *   rows_all     spec_shard_row [N][spec_shard_row_count(...)], shard r's block r
+ *   shard_begin  HOST int32 [N + 1]
+ */
+int spec_shard_accept(const spec_shard_row *rows_all, int32_t n_shards,
+                      const int32_t *shard_begin, const int32_t *draft_tokens,
+                      const int32_t *cu_draft, int32_t B, int64_t max_target_rows,
+                      int32_t draft_stride, float temperature, const float *u_accept,
+                      int32_t *out_tokens, int32_t *out_accept_len, float *out_p, float *out_q,
+                      void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Step 3 (T > 0): this shard's share of each request's final-draw mass, from
+ * the final rows' columns it holds (the target row a_i and, after a
+ * rejection, the draft row a_i).  Requests that step 2 poisoned get zero
+ * mass.  One launch.
+ *   out_mass  spec_shard_mass [B]
+ */
+int spec_shard_final_mass(const void *target_shard, const void *draft_shard, int dtype,
+                          int32_t B, int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                          int32_t draft_stride, spec_shard_mass *out_mass, void *workspace,
+                          size_t ws_bytes, spec_stream_t stream);
+
+/*
+ * Step 4 (T > 0): S = the sum of the N shards' w masses in shard order (the
+ * p masses when every w is zero after a rejection); the shard whose range
+ * holds u_final[i] * S finds the token by the inverse CDF over its columns
+ * and writes it (a global token id) at out_tokens[cu_draft[i] + i + a_i];
+ * every other shard writes -1 there.  One launch.
+ *   mass_all  spec_shard_mass [N][B], shard r's block r
+ *   shard     this shard's index r
+ */
+int spec_shard_final_draw(const void *target_shard, const void *draft_shard, int dtype,
+                          const spec_shard_mass *mass_all, int32_t n_shards, int32_t shard,
+                          int32_t B, int32_t v_begin, int32_t v_end, int64_t max_target_rows,
+                          int32_t draft_stride, const float *u_final, int32_t *out_tokens,
+                          void *workspace, size_t ws_bytes, spec_stream_t stream);
+
+/*
  * spec_verify_sample without a workspace, for callers that cannot allocate
  * device memory: an engine whose memory pool already owns all of HBM (for
  * its KV cache), a plugin whose host runtime forbids allocations outside its

@@ -133,3 +133,40 @@ def test_expiry_hook_arguments():
     assert sv.spec_test_expire_wait(-2) == sv.SPEC_ERR_INVALID_ARG
     assert sv.spec_test_expire_wait(5) == sv.SPEC_OK
     assert sv.spec_test_expire_wait(-1) == sv.SPEC_OK
+
+
+def test_shard_host_checks_reject_before_any_launch():
+    L = sv.LIB
+    I = ctypes.c_int32
+    assert sv.spec_shard_row_count(4, 20, 0) == 20 + 16
+    assert sv.spec_shard_row_count(4, 20, 6) == 20 + 24
+    assert sv.spec_shard_row_count(4, 3, 0) == -1
+    assert sv.spec_shard_workspace_size(4, 20, 1000) > sv.spec_workspace_size(4, 20, 1000)
+    assert sv.spec_shard_workspace_size(4, 20, 0) == 0
+    # an empty shard, no shard, a first bound that is not 0
+    for begin, n in (((0, 10, 10), 2), ((0, 10, 20), 0), ((1, 10, 20), 2)):
+        arr = (I * 3)(*begin)
+        assert L.spec_shard_accept(FAKE, n, arr, FAKE, FAKE, 1, 2, 0, 1.0, FAKE, FAKE, FAKE,
+                                   None, None, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    arr = (I * 3)(0, 10, 20)
+    assert L.spec_shard_accept(FAKE, 2, None, FAKE, FAKE, 1, 2, 0, 1.0, FAKE, FAKE, FAKE, None,
+                               None, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_shard_accept(FAKE, 2, arr, FAKE, FAKE, 1, 2, 0, 1.0, FAKE, FAKE, FAKE, None,
+                               None, FAKE, 16, None) == sv.SPEC_ERR_WORKSPACE
+    assert L.spec_shard_accept(FAKE, 2, arr, FAKE, FAKE, 1, 2, 0, 1.0, None, FAKE, FAKE, None,
+                               None, FAKE, 1 << 20, None) == sv.SPEC_ERR_INVALID_ARG  # no u_accept
+    # the drawing shard's index out of range; an empty column range
+    assert L.spec_shard_final_draw(FAKE, FAKE, 0, FAKE, 2, 2, 1, 0, 10, 2, 0, FAKE, FAKE, FAKE,
+                                   1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_shard_row_stats(FAKE, FAKE, 0, FAKE, FAKE, 1, 10, 10, 2, 0, 1.0, FAKE, FAKE,
+                                  1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_shard_row_stats(FAKE, FAKE, 0, FAKE, FAKE, 1, 0, 10, 2, 0, -1.0, FAKE, FAKE,
+                                  1 << 20, None) == sv.SPEC_ERR_INVALID_ARG
+    # the draw's slice table: 64 slices of 12288 f32 columns at most
+    assert L.spec_shard_final_mass(FAKE, FAKE, 0, 1, 0, 64 * 12288 + 1, 2, 0, FAKE, FAKE,
+                                   1 << 30, None) == sv.SPEC_ERR_INVALID_ARG
+    # B = 0 is a no-op for every step
+    assert L.spec_shard_row_stats(None, None, 0, None, None, 0, 0, 10, 0, 0, 1.0, None, None, 0,
+                                  None) == sv.SPEC_OK
+    assert L.spec_shard_final_mass(None, None, 0, 0, 0, 10, 0, 0, None, None, 0,
+                                   None) == sv.SPEC_OK
