@@ -146,6 +146,49 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t phase)
     }
 }
 
+// Thread-block clusters: this CTA's rank, the split cluster barrier, and
+// stores into another CTA's shared memory (at the address `local` has there).
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_addr(const void *local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ void st_cluster_u32(const void *local, uint32_t rank, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(local, rank)), "r"(v)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_cluster_u64(const void *local, uint32_t rank, uint64_t v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(cluster_addr(local, rank)), "l"(v)
+                 : "memory");
+}
+
 // max that returns NaN when either input is NaN.
 __device__ __forceinline__ float max_nan(float a, float b)
 {

@@ -305,13 +305,15 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 // (ties by request) while the running cost stays within max_cost, skipping
 // those that do not fit.  The page computes in Python floats (fp64); every
 // decision here is taken in fp64 with each operation explicitly rounded, so
-// depths match a sequential fp64 evaluation bit for bit.  One CTA: per-request best depths in parallel,
-// ranks by counting, then one thread walks the ranked requests (the
-// admission is sequential by definition).
+// depths match a sequential fp64 evaluation bit for bit.  One cluster of
+// CTAs: per-request best depths in parallel across its SMs, ranks by
+// counting, then one thread walks the ranked requests (the admission is
+// sequential by definition).
 
 namespace sv {
 
-constexpr int kCostThreads = 1024;
+constexpr int kCostCluster = 8;    // CTAs of the cost kernel's cluster (one per SM)
+constexpr int kCostThreads = 512;  // threads per CTA
 
 struct DcutCostParams {
     const float *conf;
@@ -342,38 +344,58 @@ __device__ __forceinline__ double latency_cost(int d)
     return __dadd_rn(at_pow2[k], __dmul_rn(__dsub_rn(at_pow2[k + 1], at_pow2[k]), frac));
 }
 
+// Bytes of dynamic shared memory per request.
+constexpr int kCostSmemPerReq = 8 + 8 + 4 + 4 + 4;
+
+// One cluster of kCostCluster CTAs (B300's fp64 rate per SM is low, so the
+// fp64 benefits are spread over the cluster's SMs):
+//  1. every (request, depth) pair is one thread somewhere in the cluster:
+//     the prefix product left to right, one multiply by d and one division
+//     by cost(d); a group of Kp lanes keeps its request's first maximum and
+//     stores (benefit, depth) into the shared memory of every CTA;
+//  2. every CTA ranks its share of the requests (larger benefit first, then
+//     lower request) by counting, with the benefits compared as the integer
+//     bits of non-negative doubles, and stores the rank into CTA 0;
+//  3. CTA 0 gathers the costs in rank order, one thread admits in rank order
+//     (sequential by definition, each addition rounded in fp64), and the
+//     CTA writes depths, offsets and benefits.
 __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostParams p)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    double *benefit = reinterpret_cast<double *>(dsm);  // [B]; < 0: no candidate
-    int *best_d = reinterpret_cast<int *>(benefit + p.B);
-    int *order = best_d + p.B;  // request at each rank
-    int *depth = order + p.B;
+    uint64_t *bbits = reinterpret_cast<uint64_t *>(dsm);             // [B] benefit bits
+    double *rank_cost = reinterpret_cast<double *>(bbits + p.B);      // [B] CTA 0
+    int *best_d = reinterpret_cast<int *>(rank_cost + p.B);           // [B] 0: no candidate
+    int *order = best_d + p.B;                                        // [B] CTA 0: request of each rank
+    int *depth = order + p.B;                                         // [B] CTA 0
     __shared__ double cost_tab[kMaxDraft + 1];  // cost(d), d = 1..Kmax
+    __shared__ int s_bad[kCostCluster];         // written by every CTA of the cluster
     __shared__ int s_ncand;
     __shared__ int warp_tot[33];
     const int tid = threadIdx.x, lane = tid & 31;
-    if (tid == 0)
-        s_ncand = 0;
+    const uint32_t rank = cluster_ctarank();
     if (tid >= 1 && tid <= kMaxDraft)
         cost_tab[tid] = latency_cost(tid);
-    for (int r = tid; r < p.B; r += kCostThreads)
-        depth[r] = 0;
+    if (tid < kCostCluster)
+        s_bad[tid] = 0;
+    if (tid == 0)
+        s_ncand = 0;
     __syncthreads();
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (0) every CTA has started: remote stores may begin
 
-    // 1. best depth per request; inputs validated on the way.  With at most
-    // one (request, depth) pair per thread, each pair is its own thread (the
-    // prefix product recomputed left to right, one division), and a group of
-    // Kp lanes keeps the first maximum; otherwise a thread walks a request.
+    // 1. the best depth of every request
     int Kp = 1;
     while (Kp < p.Kmax)
         Kp <<= 1;
-    int bad = 0, ncand = 0;
-    if ((int64_t)p.B * Kp <= kCostThreads) {
-        const int r = tid / Kp, d = tid % Kp + 1;
+    const int64_t npairs = (int64_t)p.B * Kp;
+    const int64_t stride = (int64_t)kCostCluster * kCostThreads;
+    int bad = 0;
+    for (int64_t base = (int64_t)rank * kCostThreads + (tid & ~31); base < npairs; base += stride) {
+        const int64_t t = base + lane;  // groups of Kp lanes never straddle a warp (Kp | 32)
+        const int r = (int)(t / Kp), d = (int)(t % Kp) + 1;
         int km = 0;
         double b = -1.0;
-        if (r < p.B) {
+        if (t < npairs) {
             km = __ldg(p.kmax + r);
             if (km < 0 || km > p.Kmax) {
                 bad = 1;
@@ -401,74 +423,75 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
                 bd = od;
             }
         }
-        if (r < p.B && d == 1) {
-            benefit[r] = km > 0 ? bb : -1.0;
-            best_d[r] = bd;
-            ncand += km > 0;
-        }
-    } else {
-        for (int r = tid; r < p.B; r += kCostThreads) {
-            int km = __ldg(p.kmax + r);
-            if (km < 0 || km > p.Kmax) {
-                bad = 1;
-                km = 0;
+        if (t < npairs && d == 1) {
+            const uint64_t bits = km > 0 ? (uint64_t)__double_as_longlong(bb) : 0ull;
+            const int dd = km > 0 ? bd : 0;
+            for (uint32_t q = 0; q < kCostCluster; ++q) {
+                st_cluster_u64(&bbits[r], q, bits);
+                st_cluster_u32(&best_d[r], q, (uint32_t)dd);
             }
-            double P = 1.0, best = -1.0;
-            int bd = 0;
-            for (int d = 1; d <= km; ++d) {
-                const float c = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
-                if (!(c >= 0.f && c <= 1.f))
-                    bad = 1;
-                P = __dmul_rn(P, (double)c);
-                const double b = __ddiv_rn(__dmul_rn(P, (double)d), cost_tab[d]);
-                if (b > best) {
-                    best = b;
-                    bd = d;
-                }
-            }
-            benefit[r] = km > 0 ? best : -1.0;
-            best_d[r] = bd;
-            ncand += km > 0;
         }
     }
-    bad = __syncthreads_or(bad);
-    if (bad) {
-        if (tid == 0)
-            set_status(p.status, ST_INVALID);
-        for (int r = tid; r < p.B; r += kCostThreads) {
-            p.out_depth[r] = -1;
-            if (p.out_benefit)
-                p.out_benefit[r] = __longlong_as_double(0x7ff8000000000000ll);
+    if (__syncthreads_or(bad) && tid == 0)
+        for (uint32_t q = 0; q < kCostCluster; ++q)
+            st_cluster_u32(&s_bad[rank], q, 1u);
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (1) every CTA holds every request's (benefit, depth)
+    int any_bad = 0;
+    for (int q = 0; q < kCostCluster; ++q)
+        any_bad |= s_bad[q];
+    if (any_bad) {  // the same verdict in every CTA: no barrier follows
+        if (rank == 0) {
+            if (tid == 0)
+                set_status(p.status, ST_INVALID);
+            for (int r = tid; r < p.B; r += kCostThreads) {
+                p.out_depth[r] = -1;
+                if (p.out_benefit)
+                    p.out_benefit[r] = __longlong_as_double(0x7ff8000000000000ll);
+            }
+            for (int r = tid; r <= p.B; r += kCostThreads)
+                p.out_cu[r] = -1;
         }
-        for (int r = tid; r <= p.B; r += kCostThreads)
-            p.out_cu[r] = -1;
         return;
     }
-    if (ncand)
-        atomicAdd(&s_ncand, ncand);
 
-    // 2. rank of every candidate: larger benefit first, then lower request
-    for (int r = tid; r < p.B; r += kCostThreads) {
-        const double b = benefit[r];
-        if (b < 0.0)
+    // 2. rank of every candidate (benefits >= 0: their bits order as integers)
+    for (int r = rank * kCostThreads + tid; r < p.B; r += kCostCluster * kCostThreads) {
+        if (best_d[r] == 0)
             continue;
-        int rank = 0;
+        const uint64_t kb = bbits[r];
+        int rk = 0;
         for (int q = 0; q < p.B; ++q) {
-            const double o = benefit[q];
-            rank += (o > b) || (o == b && q < r);  // no candidate has o < 0 <= b
+            const uint64_t o = bbits[q];
+            rk += best_d[q] != 0 && (o > kb || (o == kb && q < r));
         }
-        order[rank] = r;
+        st_cluster_u32(&order[rk], 0, (uint32_t)r);
     }
-    __syncthreads();
+    cluster_arrive_release();
+    cluster_wait_acquire();  // (2) CTA 0 holds the ranking
+    if (rank != 0)
+        return;  // no CTA touches another's shared memory after (2)
 
-    // 3. admission in rank order (sequential by definition; costs from the table)
+    // 3. admission in rank order
+    int nc = 0;
+    for (int r = tid; r < p.B; r += kCostThreads) {
+        nc += best_d[r] != 0;
+        depth[r] = 0;
+    }
+    if (nc)
+        atomicAdd(&s_ncand, nc);
+    __syncthreads();
+    const int ncand = s_ncand;
+    for (int t = tid; t < ncand; t += kCostThreads)
+        rank_cost[t] = cost_tab[best_d[order[t]]];
+    __syncthreads();
     if (tid == 0) {
         double total = 0.0;
-        for (int t = 0; t < s_ncand; ++t) {
-            const int r = order[t];
-            const double nt = __dadd_rn(total, cost_tab[best_d[r]]);
+        for (int t = 0; t < ncand; ++t) {
+            const double nt = __dadd_rn(total, rank_cost[t]);
             if (nt <= p.max_cost) {
                 total = nt;
+                const int r = order[t];
                 depth[r] = best_d[r];
             }
         }
@@ -488,17 +511,18 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
         off += depth[r];
         p.out_depth[r] = depth[r];
         if (p.out_benefit)
-            p.out_benefit[r] = depth[r] > 0 ? benefit[r] : 0.0;
+            p.out_benefit[r] =
+                depth[r] > 0 ? __longlong_as_double((long long)bbits[r]) : 0.0;
     }
     if (tid == 0)
         p.out_cu[p.B] = total;
-    (void)lane;
 }
 
 cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t s, Tracer &tr)
 {
     static cudaError_t once = cudaFuncSetAttribute(
-        dcut_cost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 20 * kMaxBatch);
+        dcut_cost_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        kCostSmemPerReq * kMaxBatch);
     if (once != cudaSuccess)
         return once;
     DcutCostParams p{};
@@ -512,10 +536,20 @@ cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t s, Tracer &tr)
     p.out_benefit = a.out_benefit;
     const WsLayout L = ws_layout(0, 0, 0);
     p.status = reinterpret_cast<uint32_t *>(static_cast<unsigned char *>(a.ws) + L.status);
-    const size_t smem = 20 * (size_t)(a.B > 0 ? a.B : 1);
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(kCostCluster);
+    cfg.blockDim = dim3(kCostThreads);
+    cfg.dynamicSmemBytes = kCostSmemPerReq * (size_t)(a.B > 0 ? a.B : 1);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCostCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     tr.begin(s);
-    dcut_cost_kernel<<<1, kCostThreads, smem, s>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaLaunchKernelEx(&cfg, dcut_cost_kernel, p);
     if (e != cudaSuccess)
         return e;
     tr.after_kernel(s);

@@ -15,30 +15,11 @@ constexpr int kFinishWarps = kFinishThreads / 32;
 constexpr int kCluster = 16;               // most CTAs per request in the sampling finish kernel
 constexpr int kSampleThreads = 256;        // threads per CTA of the sampling finish kernel
 constexpr int kSampleWarps = kSampleThreads / 32;
-constexpr int kStageRowBytes = 48 * 1024;  // largest slice of one row staged at a time
+#ifndef SV_STAGE_KB
+#define SV_STAGE_KB 48
+#endif
+constexpr int kStageRowBytes = SV_STAGE_KB * 1024;  // largest slice of one row staged at a time
 constexpr int kMaxSlices = 64;             // slices per CTA range (bounds V)
-
-__device__ __forceinline__ uint32_t cluster_ctarank()
-{
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_arrive_relaxed()
-{
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release()
-{
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire()
-{
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 // Store v at the address `local` has in the shared memory of cluster CTA `rank`.
 __device__ __forceinline__ void st_cluster_ff(ff *local, uint32_t rank, ff v)
@@ -174,6 +155,7 @@ __global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const Fin
     // inputs that do not depend on kernel 1 are read before waiting for it
     const int cu_i = __ldg(p.cu + i);
     const int K = __ldg(p.cu + i + 1) - cu_i;
+    const int cu_tot = __ldg(p.cu + p.B);
     const bool shape = request_shape_ok(p, i, cu_i, K);
     const bool act = shape && warp == 0 && lane < K;
     const int64_t dx = act ? draft_index(p.draft_stride, p.cu, i, lane) : 0;
@@ -182,12 +164,13 @@ __global__ void __launch_bounds__(kFinishThreads) finish_greedy_kernel(const Fin
     pdl_wait();  // kernel 1 has completed and its writes are visible
     if (__ldcg(p.cu_flag) == 0u || !shape)
         return;  // malformed offsets: kernel 1 poisoned every output
+    const Geometry g = real_split(p.g, p.B, cu_tot);  // kernel 1's split of the real rows
     const int64_t t0 = (int64_t)cu_i + i;
     for (int rho = warp; rho <= K; rho += kFinishWarps) {
         int wf, wl;
-        row_span(p.g, t0 + rho, wf, wl);
+        row_span(g, t0 + rho, wf, wl);
         const int gj = SV_IN_BOUNDS(t0 + rho + wl, p.part_cap, p.status)
-                           ? merge_argmax_row(p.part, p.g, t0 + rho)
+                           ? merge_argmax_row(p.part, g, t0 + rho)
                            : -2;
         if (lane == 0)
             row_g[rho] = gj;
@@ -695,6 +678,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     }
     const int cu_i = __ldg(p.cu + i);
     const int K = __ldg(p.cu + i + 1) - cu_i;
+    const int cu_tot = __ldg(p.cu + p.B);
     const bool shape = request_shape_ok(p, i, cu_i, K);
     const int64_t t0 = (int64_t)cu_i + i;
     const int nrows = 2 * K + 1;
@@ -743,6 +727,7 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
     if (__ldcg(p.cu_flag) == 0u || !shape)
         return;  // malformed offsets: kernel 1 poisoned every output (same in every CTA)
     cluster_arrive_relaxed();  // (0) this CTA has started
+    const Geometry gs = real_split(p.g, p.B, cu_tot);  // kernel 1's split of the real rows
     // an expired wait of kernel 1 only poisons; its flag is read now, off the
     // critical path
     const bool timeout = warp == 0 && (read_status(p.status) & ST_TIMEOUT);
@@ -756,9 +741,9 @@ __global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const 
         if (my_k[t] < 0)
             continue;
         const int k = my_k[t];
-        const int64_t rg = k <= K ? t0 + k : p.g.max_rows + cu_i + (k - K - 1);
+        const int64_t rg = k <= K ? t0 + k : gs.nt + cu_i + (k - K - 1);
         int wf, wl;
-        row_span(p.g, rg, wf, wl);
+        row_span(gs, rg, wf, wl);
         for (int w = wf + lane; w <= wl; w += 32) {
             if (!SV_IN_BOUNDS(rg + w, p.part_cap, p.status))
                 continue;

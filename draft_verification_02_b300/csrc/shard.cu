@@ -126,6 +126,7 @@ __global__ void __launch_bounds__(kFinishThreads) shard_rows_kernel(const ShardR
     const int i = blockIdx.x;
     const int cu_i = __ldg(p.cu + i);
     const int K = __ldg(p.cu + i + 1) - cu_i;
+    const int cu_tot = __ldg(p.cu + p.B);
     const bool shape = shard_shape_ok(p.max_rows, p.draft_rows, p.draft_stride, i, cu_i, K);
     const T *tbase = reinterpret_cast<const T *>(p.target);
     const T *dbase = reinterpret_cast<const T *>(p.draft);
@@ -133,23 +134,24 @@ __global__ void __launch_bounds__(kFinishThreads) shard_rows_kernel(const ShardR
     pdl_wait();  // the streaming pass has completed and its writes are visible
     if (__ldcg(p.cu_flag) == 0u || !shape)
         return;  // malformed offsets: flagged by the streaming pass, poisoned by step 2
+    const Geometry g = real_split(p.g, p.B, cu_tot);  // the streaming pass's split
     const int64_t t0 = (int64_t)cu_i + i;
     const int nrows = GREEDY ? K + 1 : 2 * K + 1;  // target rows 0..K, then draft rows
     for (int k = warp; k < nrows; k += kFinishWarps) {
         const bool tgt = k <= K;
         const int j = tgt ? k : k - K - 1;
-        const int64_t rg = tgt ? t0 + k : p.g.max_rows + cu_i + j;  // row of the streaming pass
+        const int64_t rg = tgt ? t0 + k : g.nt + cu_i + j;  // row of the streaming pass
         const int64_t dj = k == K ? -1 : draft_index(p.draft_stride, p.cu, i, j);
         const int64_t rec = tgt ? t0 + k : p.max_rows + dj;
         int wf, wl;
-        row_span(p.g, rg, wf, wl);
+        row_span(g, rg, wf, wl);
         ShardRow r{__int_as_float(0x7fc00000), -2, __int_as_float(0x7fc00000), 0.f};
         if (SV_IN_BOUNDS(rg + wl, p.part_cap, p.status)) {
             if (GREEDY) {
                 float best;
                 int bidx;
                 bool nan;
-                merge_argmax_pair(p.part, p.g, rg, best, bidx, nan);
+                merge_argmax_pair(p.part, g, rg, best, bidx, nan);
                 r = {best, nan ? -2 : (bidx == INT_MAX ? -1 : p.v_begin + bidx), 0.f, 0.f};
             } else {
                 float m = -INFINITY;

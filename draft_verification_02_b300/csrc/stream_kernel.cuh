@@ -10,11 +10,18 @@ namespace sv {
 // kernel 1: stream the rows
 // ---------------------------------------------------------------------------
 
+// Units in flight per warp and CTAs per SM: 2 units of 4 KB with 3 CTAs of 8
+// warps per SM (80 registers, 64 KB of ring per CTA).  Measured on B300
+// against 3 units with 2 CTAs per SM (the previous setting), streaming
+// fraction of the measured HBM peak: B=128, V=151936 at T=0.7 0.936 vs
+// 0.894, at T=0 0.874 vs 0.858; B=32, K=16 0.855 vs 0.844, at T=0 0.739 vs
+// 0.716; the padded D-cut rows 0.613 vs 0.580.  2 KB units (rings of 4-6, 2
+// or 3 CTAs) and one CTA with a ring of 4 were all slower (0.60-0.73).
 #ifndef SV_RING
-#define SV_RING 3
+#define SV_RING 2
 #endif
 #ifndef SV_STREAM_CTAS_PER_SM
-#define SV_STREAM_CTAS_PER_SM 2
+#define SV_STREAM_CTAS_PER_SM 3
 #endif
 constexpr int kRing = SV_RING;
 constexpr int kStreamWarps = 8;
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
     __shared__ __align__(8) uint64_t bars[kStreamWarps][kRing];
     const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
     const int w = blockIdx.x * kStreamWarps + wib;
-    const Geometry g = p.g;
+    Geometry g = p.g;  // the host's split until the offsets arrive (real_split)
     const int B = p.B, V = p.V;
     unsigned char *ring = dsm + (size_t)wib * kRing * p.piece_smem;
     int32_t *cu_s = reinterpret_cast<int32_t *>(dsm + (size_t)kStreamWarps * kRing * p.piece_smem);
@@ -331,20 +338,21 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
     }
     __syncwarp();
 
-    const int64_t u0 = w < g.P ? (int64_t)w * g.U / g.P : 0;
-    const int64_t u1 = w < g.P ? (int64_t)(w + 1) * g.U / g.P : 0;
+    int64_t u0 = w < g.P ? (int64_t)w * g.U / g.P : 0;
+    int64_t u1 = w < g.P ? (int64_t)(w + 1) * g.U / g.P : 0;
     const T *tbase = reinterpret_cast<const T *>(p.target);
     const T *dbase = reinterpret_cast<const T *>(p.draft);
     const bool padded = !GREEDY && p.draft_stride > 0;
 
-    // Where the unit at (row rg, column chunk q) comes from; false when the
-    // row lies past the real rows (nt target, nd draft) and `check` is set.
+    // Where the unit at (row rg of the split's index space, column chunk q)
+    // comes from; false when the row lies past the real rows (nt target, nd
+    // draft) and `check` is set.
     int req_hint = 0;  // request of the last slot found (consecutive units share rows)
     auto locate = [&](int64_t rg, int q, const T *&src, int &len, int &col0, int64_t nt,
                       int64_t nd, bool check) -> bool {
         col0 = q * g.Q;
         len = min(g.Q, V - col0);
-        if (rg < g.max_rows) {
+        if (rg < g.nt) {
             if (check && rg >= nt)
                 return false;
             if (!SV_IN_BOUNDS(rg, g.max_rows, p.status))
@@ -352,7 +360,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
             src = tbase + rg * (int64_t)V + col0;
             return true;
         }
-        const int64_t slot = rg - g.max_rows;
+        const int64_t slot = rg - g.nt;
         if (check && slot >= nd)
             return false;
         int64_t row = slot;
@@ -405,7 +413,7 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
     int c_q = (int)(u0 - c_rg * g.cpr);
     int64_t i_rg = c_rg;
     int i_q = c_q;
-    const int64_t n_units = u1 - u0;
+    int64_t n_units = u1 - u0;
     auto advance = [&](int64_t &rg, int &q) {
         if (++q == g.cpr) {
             q = 0;
@@ -469,6 +477,44 @@ __global__ void __launch_bounds__(kStreamThreads, SV_STREAM_CTAS_PER_SM)
         v = __shfl_sync(0xffffffffu, v, 0);
         nd = min(nd, (int64_t)v);
         nt = min(g.max_rows, (int64_t)v + B);
+        const Geometry gr = real_split(g, B, v);
+        if (gr.U != g.U) {
+            // a loose host bound: the real rows are split afresh.  The
+            // speculative first copies are waited for and dropped.
+            bool ok = true;
+            if (p.tma)
+                for (int k = 0; k < kRing; ++k)
+                    if (issued >> k & 1)
+                        ok = mbar_wait_bounded(&bars[wib][k], phase >> k & 1) && ok;
+            if (__any_sync(0xffffffffu, !ok)) {
+                if (lane == 0)
+                    set_status(p.status, ST_TIMEOUT);
+                for (int k = 0; k < kRing; ++k)  // the copies in flight, once more
+                    if (issued >> k & 1)
+                        mbar_wait_bounded(&bars[wib][k], phase >> k & 1);
+                return;
+            }
+            if (p.tma)
+                for (int k = 0; k < kRing; ++k)
+                    if (issued >> k & 1)
+                        phase ^= 1u << k;
+            issued = 0;
+            n_issued = 0;
+            __syncwarp();  // every lane is done with the dropped copies' slots
+            g = gr;
+            u0 = w < g.P ? (int64_t)w * g.U / g.P : 0;
+            u1 = w < g.P ? (int64_t)(w + 1) * g.U / g.P : 0;
+            n_units = u1 - u0;
+            c_rg = u0 / g.cpr;
+            c_q = (int)(u0 - c_rg * g.cpr);
+            i_rg = c_rg;
+            i_q = c_q;
+            if (!padded)  // the first copies of the new split
+                for (; n_issued < kRing && n_issued < n_units; ++n_issued) {
+                    issue(i_rg, i_q, n_issued, nt, nd, true);
+                    advance(i_rg, i_q);
+                }
+        }
     }
     if (padded)
         for (; n_issued < kRing && n_issued < n_units; ++n_issued) {

@@ -162,6 +162,8 @@ static Geometry plan(int64_t rows_total, int64_t max_rows, int V, int elem, int 
     g.cpr = (V + g.Q - 1) / g.Q;
     g.U = rows_total * (int64_t)g.cpr;
     g.P = (int)std::min<int64_t>(P, g.U);
+    g.slots = rows_total - max_rows;
+    g.nt = max_rows;
     return g;
 }
 
@@ -217,17 +219,11 @@ static cudaError_t prepare_draft_sample()
     return once;
 }
 
-// Geometry of a cluster draw over V entries, one cluster per draw: ncl
-// ranges of R entries, weighed in slices.  16 CTAs per draw while the
-// clusters fit the GPU at one CTA per SM (larger clusters are harder to
-// place), else 8.  False when the vocabulary exceeds the slice table.
-static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e, int ncl_force = 0,
-                          int stage_bytes = kStageRowBytes)
+// Slices of at most stage_bytes per row for ncl ranges of a V-entry row;
+// false when a range needs more slices than the slice table holds.
+static bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stage_bytes)
 {
     const int gran = 16 / e;
-    const int ncl = ncl_force > 0 ? ncl_force
-                                  : (draws * kCluster <= (int64_t)sm_count() ? kCluster
-                                                                              : kCluster / 2);
     fp.ncl = ncl;
     const int R = (int)((((int64_t)V + ncl - 1) / ncl + gran - 1) / gran * gran);
     const int slice = std::min(R, stage_bytes / e);
@@ -237,6 +233,27 @@ static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e, int ncl
     fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
     fp.stage_smem = (int)align_up((size_t)slice * e, 128);
     return (R + slice - 1) / slice <= kMaxSlices;
+}
+
+// Geometry of a cluster draw over V entries, one cluster per draw: ncl
+// ranges of R entries, weighed in slices.  16 CTAs per draw while the
+// clusters fit the GPU at two CTAs per SM, else 8; slices of half the
+// largest size once the grid holds more than four CTAs per SM (less shared
+// memory per CTA, so more of them resident).  Measured on B300, ms per step:
+// B = 16, V = 128000: 16 CTAs 0.0206, 8 CTAs 0.0222; B = 32 and 64 at
+// V = 151936: 8 CTAs and 48 KB slices best (0.0703, 0.0930; 16 CTAs 0.0761,
+// 0.1008); B = 128, V = 151936: 24 KB slices 0.1596, 48 KB 0.1652, 16 KB
+// 0.1646, 12 KB 0.1667.  False when the vocabulary exceeds the slice table.
+static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
+{
+    const int64_t sms = sm_count();
+    int ncl = draws * kCluster <= 2 * sms ? kCluster : kCluster / 2;
+#ifdef SV_NCL
+    ncl = SV_NCL;
+#endif
+    if (draws * ncl > 4 * sms && fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
+        return true;
+    return fill_draw_geometry(fp, ncl, V, e, kStageRowBytes);
 }
 
 // Kernel 1's parameters for a verification call (a.out_tokens / a.out_len

@@ -17,12 +17,17 @@ namespace sv {
 // parameters
 // ---------------------------------------------------------------------------
 
-struct Geometry {  // the unit split of kernel 1, needed by kernel 2 to find partials
+// The unit split of kernel 1, needed by kernel 2 to find partials.  Rows
+// are numbered in one index space: target rows [0, nt), then draft slots
+// (draft slot s is row nt + s); units run through it in order.
+struct Geometry {
     int64_t max_rows;  // target rows (host bound)
     int64_t U;         // units
     int cpr;           // units per row
     int Q;             // elements per unit (the last unit of a row may be shorter)
     int P;             // warp workers
+    int64_t slots;     // draft slots of the host bound (max_rows - B at T > 0, else 0)
+    int64_t nt;        // target rows of the index space (max_rows in the host's split)
 };
 
 struct StreamParams {
@@ -108,6 +113,26 @@ __device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b)
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// The split over the rows that exist.  The host splits its bound (every
+// target row up to max_rows, every draft slot); once the real count
+// cu_total = cu_draft[B] is known, a looser bound is re-split over the real
+// rows only (target rows [0, cu_total + B), then the cu_total draft slots),
+// so that no warp is handed rows that do not exist.  Every kernel that reads
+// the partials derives the same split from the same offsets.  (Malformed
+// offsets are clamped here only to keep the split well formed; such a call
+// is poisoned anyway.)
+__device__ __forceinline__ Geometry real_split(Geometry g, int B, int cu_total)
+{
+    const int64_t v = cu_total < 0 ? 0 : cu_total;
+    const int64_t nt = min(g.max_rows, v + B);
+    const int64_t nd = min(g.slots, v);
+    if (nt + nd < g.max_rows + g.slots) {
+        g.nt = nt;
+        g.U = (nt + nd) * (int64_t)g.cpr;
+    }
+    return g;
+}
 
 // Owner warp of unit u when warp w owns units [w*U/P, (w+1)*U/P).
 __device__ __forceinline__ int owner_of(int64_t u, const Geometry &g)

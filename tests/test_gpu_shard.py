@@ -13,7 +13,7 @@ from draft_verification_02_b300 import specverify as sv
 from draft_verification_02_b300 import workloads as W
 from draft_verification_02_b300.sharded import (Shard, shard_bounds, shard_columns,
                                                 verify_sharded_local)
-from test_gpu_verify import MAX_EXEMPT, ragged_batch
+from test_gpu_verify import MAX_EXEMPT, pad_to_loose_bound, ragged_batch
 
 pytestmark = pytest.mark.gpu
 
@@ -197,3 +197,15 @@ def test_repeat_calls_are_bit_identical_sharded():
     _, again, _ = run_sharded(b, bounds)
     for k in ("tokens", "accept_len", "p", "q"):
         torch.testing.assert_close(again[0][k], first[0][k], rtol=0, atol=0, equal_nan=True)
+
+
+@pytest.mark.parametrize("T", [0.0, 0.9])
+def test_sharded_loose_row_bound(T):
+    """A host bound far above the real rows (NaN past them): each shard's
+    streaming pass re-splits the real rows and its row merge follows."""
+    B, V = 10, 9000
+    b = pad_to_loose_bound(ragged_batch(B, V, T, "f32", seed=43, kmax=6), B * 20)
+    batch, outs, status = run_sharded(b, shard_bounds(V, 3), rows=B * 20)
+    assert status == [sv.SPEC_OK] * 3
+    assert_shards_agree(outs)
+    parity.compare_batch(batch, outs[0])

@@ -57,6 +57,22 @@ def ragged_batch(B, V, T, dtype, seed, kmax=16, kmin=0, draft_stride=0, sigma=2.
     return b
 
 
+def pad_to_loose_bound(b, rows):
+    """Grow the row buffers of a packed or padded batch to a host bound of
+    `rows` target rows, the rows past the real ones NaN (a kernel that read
+    one would poison its request)."""
+    V, dt = b.V, b.target_logits.dtype
+    nan = float("nan")
+    b.target_logits = torch.cat(
+        [b.target_logits, torch.full((rows - b.n_target_rows, V), nan, dtype=dt)])
+    if b.draft_stride == 0:
+        extra = rows - b.B - b.draft_logits.shape[0]
+        b.draft_logits = torch.cat([b.draft_logits, torch.full((extra, V), nan, dtype=dt)])
+        b.draft_tokens = torch.cat([b.draft_tokens, torch.zeros(extra, dtype=torch.int32)])
+        b.u_accept = torch.cat([b.u_accept, torch.full((extra,), 0.5)])
+    return b
+
+
 # ---------------------------------------------------------------------------
 # small configurations, every request compared
 # ---------------------------------------------------------------------------
@@ -478,3 +494,20 @@ def test_launch_counts_and_trace():
     assert sv.spec_set_trace(None) == sv.SPEC_OK
     torch.cuda.synchronize()
     assert ev[0].elapsed_time(ev[1]) > 0 and ev[1].elapsed_time(ev[2]) > 0
+
+
+@pytest.mark.parametrize("T,stride", [(0.0, 0), (0.7, 0), (1.0, 8), (0.0, 8)])
+def test_loose_row_bound_reads_only_real_rows(T, stride):
+    """max_target_rows far above the real count, as when the offsets come
+    from the device with only a host bound: the streaming pass splits the
+    real rows afresh once it has read the offsets (dropping its speculative
+    first copies), the finish kernel finds the partials under the same split,
+    and the rows past the real count (NaN here) are never read."""
+    B, V = 12, 20000
+    b = ragged_batch(B, V, T, "bf16", seed=41, kmin=0, kmax=8, draft_stride=stride)
+    loose = B * 33
+    b = pad_to_loose_bound(b, loose)
+    batch, out, v = run_gpu(b, rows=loose)
+    assert v.device_status() == sv.SPEC_OK
+    rep = parity.compare_batch(batch, out)
+    assert rep["exempt_accept"] + rep["exempt_final"] <= MAX_EXEMPT, rep
