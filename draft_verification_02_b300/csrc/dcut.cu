@@ -24,7 +24,10 @@
 #include <climits>
 #include <cstdint>
 
+#include <cstring>
+
 #include "common.cuh"
+#include "fp64_exact.cuh"
 #include "launch.h"
 
 namespace sv {
@@ -303,12 +306,15 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 // ends); each request takes the depth maximising benefit(d) = P_d * d /
 // cost(d) (the first such d); requests are admitted in decreasing benefit
 // (ties by request) while the running cost stays within max_cost, skipping
-// those that do not fit.  The page computes in Python floats (fp64); every
-// decision here is taken in fp64 with each operation explicitly rounded, so
-// depths match a sequential fp64 evaluation bit for bit.  One cluster of
-// CTAs: per-request best depths in parallel across its SMs, ranks by
-// counting, then one thread walks the ranked requests (the admission is
-// sequential by definition).
+// those that do not fit.  The page computes in Python floats (binary64);
+// every value here is the binary64 value of the same operations in the same
+// order, each rounded once, so depths and benefits match a sequential fp64
+// evaluation bit for bit.  The roundings are done exactly on the integer
+// pipes (fp64_exact.cuh; B300's fp64 pipe is slow), the hardware fp64 path
+// only for values outside the normal range.  One cluster of CTAs:
+// per-request best depths in parallel across its SMs, ranks by counting,
+// then one thread walks the ranked requests (the admission is sequential by
+// definition).
 
 namespace sv {
 
@@ -319,7 +325,12 @@ struct DcutCostParams {
     const float *conf;
     const int32_t *kmax;
     int B, Kmax;
+    uint64_t cost_bits[kMaxDraft + 1];   // cost(d) as a double's bits, d = 1..32
+    uint64_t cost_recip[kMaxDraft + 1];  // recip116 of cost(d)'s significand
     double max_cost;
+    uint64_t max_units;  // floor(max_cost * 2^52) when units_path
+    uint64_t half_ulp;   // half a unit in the last place of max_cost + 3, in those units
+    int units_path;      // 0 <= max_cost < 1024: the admission adds in units of 2^-52
     int32_t *out_depth;
     int32_t *out_cu;
     double *out_benefit;
@@ -331,50 +342,114 @@ struct DcutCostParams {
 // [1, 16].  The table's depths are the powers 2^0 .. 2^4, so depth d in
 // (2^k, 2^(k+1)] lies on segment k, whose span is 2^k: the fraction
 // (d - 2^k) / 2^k is exact and the cost is one rounded multiply and one
-// rounded add in fp64.
-__device__ __forceinline__ double latency_cost(int d)
+// rounded add in binary64.  Evaluated on the host (each operation a separate
+// IEEE binary64 operation: `volatile` keeps them from being fused).
+static double latency_cost(int d)
 {
     const double at_pow2[5] = {1.0, 1.2, 1.5, 2.0, 3.0};  // cost(2^k), k = 0..4
     if (d <= 1)
         return at_pow2[0];
     if (d >= 16)
         return at_pow2[4];
-    const int k = 31 - __clz(d - 1);  // floor(log2(d - 1)): 2^k < d <= 2^(k+1)
+    int k = 0;
+    while ((2 << k) < d)  // 2^k < d <= 2^(k+1)
+        ++k;
     const double frac = (double)(d - (1 << k)) / (double)(1 << k);  // exact
-    return __dadd_rn(at_pow2[k], __dmul_rn(__dsub_rn(at_pow2[k + 1], at_pow2[k]), frac));
+    volatile double rise = at_pow2[k + 1] - at_pow2[k];
+    volatile double step = rise * frac;
+    return at_pow2[k] + step;
 }
 
-// Bytes of dynamic shared memory per request.
-constexpr int kCostSmemPerReq = 8 + 8 + 4 + 4 + 4;
+// Bytes of dynamic shared memory per request: benefit bits, the cost of
+// each rank (units of 2^-52, or a double's bits), best depth, rank order,
+// depth, the admission decision of each rank.
+constexpr int kCostSmemPerReq = 8 + 8 + 4 + 4 + 4 + 1;
 
-// One cluster of kCostCluster CTAs (B300's fp64 rate per SM is low, so the
-// fp64 benefits are spread over the cluster's SMs):
-//  1. every (request, depth) pair is one thread somewhere in the cluster:
-//     the prefix product left to right, one multiply by d and one division
-//     by cost(d); a group of Kp lanes keeps its request's first maximum and
+// The benefit P_d * d / cost(d) of one (request, depth) pair as a double's
+// bits, computed the way the scheduler's fp64 arithmetic does (P_d the
+// left-to-right product of the confidences, each operation rounded once):
+// on the integer paths (fp64_exact.cuh), or with the fp64 hardware when a
+// value leaves the normal range (a subnormal product or confidence).  The
+// group of Kp lanes of one request holds its confidences, one per lane
+// (cj of lane j); every lane of the group calls this (it shuffles).
+__device__ __forceinline__ uint64_t pair_benefit(const uint64_t *cost_bits,
+                                                 const uint64_t *cost_recip, float cj, int gbase,
+                                                 int Kp, int d)
+{
+    Dbl P{1ull << 52, -52};  // 1.0
+    bool zero = false, slow = false;
+    for (int j = 0; j < Kp; ++j) {
+        const float c = __shfl_sync(0xffffffffu, cj, gbase + j);
+        if (j >= d || zero || slow)
+            continue;
+        if (c == 0.f) {
+            zero = true;
+            continue;
+        }
+        Dbl cd;
+        if (!flt_unpack(__float_as_uint(c), cd)) {
+            slow = true;
+            continue;
+        }
+        P = mul_round(P, cd);
+        slow = P.e + 1075 < 1;
+    }
+    uint64_t bits = 0;  // +0.0: a zero confidence makes the benefit 0
+    if (!zero && !slow && d >= 1 && d <= kMaxDraft) {
+        const Dbl x = mul_round(P, int_unpack((uint32_t)d));
+        Dbl y;
+        dbl_unpack(cost_bits[d], y);
+        slow = !dbl_pack(div_round(x, y, cost_recip[d]), bits);
+    }
+    // the hardware path, from the start (every lane shuffles; only the
+    // lanes that need it use the result)
+    const bool any_slow = __any_sync(0xffffffffu, slow);
+    if (any_slow) {
+        double Q = 1.0;
+        for (int j = 0; j < Kp; ++j) {
+            const float c = __shfl_sync(0xffffffffu, cj, gbase + j);
+            if (slow && j < d)
+                Q = __dmul_rn(Q, (double)c);
+        }
+        if (slow)
+            bits = (uint64_t)__double_as_longlong(__ddiv_rn(
+                __dmul_rn(Q, (double)d), __longlong_as_double((long long)cost_bits[d])));
+    }
+    return bits;
+}
+
+// One cluster of kCostCluster CTAs:
+//  1. every (request, depth) pair is one thread somewhere in the cluster
+//     (pair_benefit); a group of Kp lanes keeps its request's first maximum
+//     (benefits compared as the integer bits of non-negative doubles) and
 //     stores (benefit, depth) into the shared memory of every CTA;
 //  2. every CTA ranks its share of the requests (larger benefit first, then
-//     lower request) by counting, with the benefits compared as the integer
-//     bits of non-negative doubles, and stores the rank into CTA 0;
-//  3. CTA 0 gathers the costs in rank order, one thread admits in rank order
-//     (sequential by definition, each addition rounded in fp64), and the
-//     CTA writes depths, offsets and benefits.
+//     lower request) by counting, and stores the rank into CTA 0;
+//  3. CTA 0 lays out the costs in rank order, one thread admits in rank
+//     order (sequential by definition: each addition rounded as binary64,
+//     on 128-bit integers in units of 2^-52), and the CTA writes depths,
+//     offsets and benefits.
 __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostParams p)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
-    uint64_t *bbits = reinterpret_cast<uint64_t *>(dsm);             // [B] benefit bits
-    double *rank_cost = reinterpret_cast<double *>(bbits + p.B);      // [B] CTA 0
-    int *best_d = reinterpret_cast<int *>(rank_cost + p.B);           // [B] 0: no candidate
-    int *order = best_d + p.B;                                        // [B] CTA 0: request of each rank
-    int *depth = order + p.B;                                         // [B] CTA 0
-    __shared__ double cost_tab[kMaxDraft + 1];  // cost(d), d = 1..Kmax
+    uint64_t *rank_cost = reinterpret_cast<uint64_t *>(dsm);  // [B] CTA 0: cost of each rank
+    uint64_t *bbits = rank_cost + p.B;                         // [B] benefit bits
+    int *best_d = reinterpret_cast<int *>(bbits + p.B);                // [B] 0: no candidate
+    int *order = best_d + p.B;                                         // [B] CTA 0: request of each rank
+    int *depth = order + p.B;                                          // [B] CTA 0
+    __shared__ uint64_t cost_units[kMaxDraft + 1];  // cost(d) in units of 2^-52
+    __shared__ uint64_t cost_bits[kMaxDraft + 1];   // cost(d) as a double's bits
+    __shared__ uint64_t cost_recip[kMaxDraft + 1];  // recip116 of its significand
     __shared__ int s_bad[kCostCluster];         // written by every CTA of the cluster
     __shared__ int s_ncand;
     __shared__ int warp_tot[33];
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
-    if (tid >= 1 && tid <= kMaxDraft)
-        cost_tab[tid] = latency_cost(tid);
+    if (tid >= 1 && tid <= kMaxDraft) {  // staged: lanes index them by their own depth
+        cost_units[tid] = to_units(p.cost_bits[tid]);
+        cost_bits[tid] = p.cost_bits[tid];
+        cost_recip[tid] = p.cost_recip[tid];
+    }
     if (tid < kCostCluster)
         s_bad[tid] = 0;
     if (tid == 0)
@@ -390,11 +465,14 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     const int64_t npairs = (int64_t)p.B * Kp;
     const int64_t stride = (int64_t)kCostCluster * kCostThreads;
     int bad = 0;
-    for (int64_t base = (int64_t)rank * kCostThreads + (tid & ~31); base < npairs; base += stride) {
+    // warp w of CTA q takes the 32 pairs at (w * kCostCluster + q) * 32 first,
+    // so that a small batch is spread over every SM of the cluster
+    for (int64_t base = ((int64_t)(tid >> 5) * kCostCluster + rank) * 32; base < npairs;
+         base += stride) {
         const int64_t t = base + lane;  // groups of Kp lanes never straddle a warp (Kp | 32)
         const int r = (int)(t / Kp), d = (int)(t % Kp) + 1;
         int km = 0;
-        double b = -1.0;
+        float cj = 0.f;  // this lane's confidence: c[r][d - 1]
         if (t < npairs) {
             km = __ldg(p.kmax + r);
             if (km < 0 || km > p.Kmax) {
@@ -402,21 +480,23 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
                 km = 0;
             }
             if (d <= km) {
-                double P = 1.0;
-                for (int j = 0; j < d; ++j) {
-                    const float c = __ldg(p.conf + (int64_t)r * p.Kmax + j);
-                    if (!(c >= 0.f && c <= 1.f))
-                        bad = 1;
-                    P = __dmul_rn(P, (double)c);
-                }
-                b = __ddiv_rn(__dmul_rn(P, (double)d), cost_tab[d]);
+                cj = __ldg(p.conf + (int64_t)r * p.Kmax + (d - 1));
+                if (!(cj >= 0.f && cj <= 1.f))
+                    bad = 1;
             }
         }
+        // the group's lanes hold its request's confidences; an invalid one
+        // anywhere poisons the whole call, so the values are only used when
+        // the whole warp saw valid ones
+        const bool warp_bad = __any_sync(0xffffffffu, bad);
+        const uint64_t bits =
+            pair_benefit(cost_bits, cost_recip, warp_bad ? 0.f : cj, lane & ~(Kp - 1), Kp, d);
+        const long long b = t < npairs && d <= km && !warp_bad ? (long long)bits : -1;
         // the group's first maximum: larger benefit, then smaller depth
-        double bb = b;
-        int bd = b >= 0.0 ? d : 0;
+        long long bb = b;
+        int bd = b >= 0 ? d : 0;
         for (int o = Kp >> 1; o > 0; o >>= 1) {
-            const double ob = __shfl_xor_sync(0xffffffffu, bb, o);
+            const long long ob = __shfl_xor_sync(0xffffffffu, bb, o);
             const int od = __shfl_xor_sync(0xffffffffu, bd, o);
             if (ob > bb || (ob == bb && od != 0 && (bd == 0 || od < bd))) {
                 bb = ob;
@@ -424,10 +504,10 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
             }
         }
         if (t < npairs && d == 1) {
-            const uint64_t bits = km > 0 ? (uint64_t)__double_as_longlong(bb) : 0ull;
+            const uint64_t best_bits = km > 0 ? (uint64_t)bb + 1 : 0ull;  // the ranking key
             const int dd = km > 0 ? bd : 0;
             for (uint32_t q = 0; q < kCostCluster; ++q) {
-                st_cluster_u64(&bbits[r], q, bits);
+                st_cluster_u64(&bbits[r], q, best_bits);
                 st_cluster_u32(&best_d[r], q, (uint32_t)dd);
             }
         }
@@ -455,17 +535,23 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
         return;
     }
 
-    // 2. rank of every candidate (benefits >= 0: their bits order as integers)
+    // 2. rank of every candidate.  Keys: the benefit's bits + 1 for a
+    // candidate (benefits >= 0: their bits order as integers), 0 for none,
+    // so that no candidate ever counts a non-candidate above it.
     for (int r = rank * kCostThreads + tid; r < p.B; r += kCostCluster * kCostThreads) {
-        if (best_d[r] == 0)
-            continue;
         const uint64_t kb = bbits[r];
-        int rk = 0;
-        for (int q = 0; q < p.B; ++q) {
-            const uint64_t o = bbits[q];
-            rk += best_d[q] != 0 && (o > kb || (o == kb && q < r));
+        if (kb == 0)
+            continue;
+        int rk0 = 0, rk1 = 0;
+        int q = 0;
+        for (; q + 1 < p.B; q += 2) {  // two independent counts
+            const uint64_t o0 = bbits[q], o1 = bbits[q + 1];
+            rk0 += o0 > kb || (o0 == kb && q < r);
+            rk1 += o1 > kb || (o1 == kb && q + 1 < r);
         }
-        st_cluster_u32(&order[rk], 0, (uint32_t)r);
+        if (q < p.B)
+            rk0 += bbits[q] > kb || (bbits[q] == kb && q < r);
+        st_cluster_u32(&order[rk0 + rk1], 0, (uint32_t)r);
     }
     cluster_arrive_release();
     cluster_wait_acquire();  // (2) CTA 0 holds the ranking
@@ -475,27 +561,75 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     // 3. admission in rank order
     int nc = 0;
     for (int r = tid; r < p.B; r += kCostThreads) {
-        nc += best_d[r] != 0;
+        nc += bbits[r] != 0;
         depth[r] = 0;
     }
     if (nc)
         atomicAdd(&s_ncand, nc);
     __syncthreads();
     const int ncand = s_ncand;
-    for (int t = tid; t < ncand; t += kCostThreads)
-        rank_cost[t] = cost_tab[best_d[order[t]]];
+    for (int t = tid; t < ncand; t += kCostThreads) {
+        const int dd = best_d[order[t]];
+        rank_cost[t] = p.units_path ? cost_units[dd] : cost_bits[dd];
+    }
     __syncthreads();
+    // one thread decides in rank order; the decisions (one byte per rank,
+    // kept in the ranks' cost slots) are applied in parallel afterwards
+    uint8_t *admitted = reinterpret_cast<uint8_t *>(depth + p.B);  // [B]
     if (tid == 0) {
-        double total = 0.0;
-        for (int t = 0; t < ncand; ++t) {
-            const double nt = __dadd_rn(total, rank_cost[t]);
-            if (nt <= p.max_cost) {
-                total = nt;
-                const int r = order[t];
-                depth[r] = best_d[r];
+        if (p.units_path) {  // totals below 2^11: 64-bit units of 2^-52
+            // The rounded running total T and the exact sum X of the admitted
+            // costs differ by at most k half-ulps after k admissions (every
+            // rounded sum is below max_cost + 3), so a step whose exact sum
+            // lies farther than (k + 1) half-ulps from max_cost is decided by
+            // X alone, with a two-instruction chain.  A step inside that
+            // margin (a budget on or next to a reachable sum) sends the whole
+            // walk to the rounded chain.
+            const uint64_t M = p.max_units;
+            uint64_t X = 0, margin = p.half_ulp;
+            bool near = false;
+            for (int t0 = 0; t0 < ncand && !near; t0 += 8) {
+                uint64_t c[8];  // the next costs, loaded ahead of the chain
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    c[k] = t0 + k < ncand ? rank_cost[t0 + k] : ~0ull >> 1;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t y = X + c[k];
+                    const bool adm = y + margin <= M;
+                    near |= !adm && y <= M + margin;
+                    X = adm ? y : X;
+                    margin += adm ? p.half_ulp : 0;
+                    if (t0 + k < ncand)
+                        admitted[t0 + k] = adm;
+                }
+            }
+            if (near) {
+                uint64_t total = 0;
+                for (int t = 0; t < ncand; ++t) {
+                    const uint64_t nt = add_units_round(total, rank_cost[t]);
+                    const bool adm = nt <= M;
+                    total = adm ? nt : total;
+                    admitted[t] = adm;
+                }
+            }
+        } else {  // a large budget (or none): the fp64 hardware
+            double total = 0.0;
+            for (int t = 0; t < ncand; ++t) {
+                const double nt =
+                    __dadd_rn(total, __longlong_as_double((long long)rank_cost[t]));
+                const bool adm = p.max_cost >= 0.0 && nt <= p.max_cost;
+                total = adm ? nt : total;
+                admitted[t] = adm;
             }
         }
     }
+    __syncthreads();
+    for (int t = tid; t < ncand; t += kCostThreads)
+        if (admitted[t]) {
+            const int r = order[t];
+            depth[r] = best_d[r];
+        }
     __syncthreads();
 
     // 4. depths, offsets (exclusive scan), benefits of the admitted requests
@@ -512,7 +646,7 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
         p.out_depth[r] = depth[r];
         if (p.out_benefit)
             p.out_benefit[r] =
-                depth[r] > 0 ? __longlong_as_double((long long)bbits[r]) : 0.0;
+                depth[r] > 0 ? __longlong_as_double((long long)(bbits[r] - 1)) : 0.0;
     }
     if (tid == 0)
         p.out_cu[p.B] = total;
@@ -530,7 +664,35 @@ cudaError_t launch_dcut_cost(const DcutCostArgs &a, cudaStream_t s, Tracer &tr)
     p.kmax = a.kmax;
     p.B = a.B;
     p.Kmax = a.Kmax;
+    for (int d = 1; d <= kMaxDraft; ++d) {
+        const double cost = latency_cost(d);
+        std::memcpy(&p.cost_bits[d], &cost, sizeof cost);
+        Dbl y;
+        dbl_unpack(p.cost_bits[d], y);  // cost(d) in [1, 3]: normal
+        p.cost_recip[d] = recip116(y.m);
+    }
+    // floor(max_cost * 2^52): an admitted total is 0 or a double >= 1, a
+    // multiple of 2^-52, so total <= max_cost exactly when its units are <=
+    // this.  Totals stay below max_cost + 3 < 2^11 on this path.
     p.max_cost = a.max_cost;
+    p.units_path = a.max_cost >= 0.0 && a.max_cost < 1024.0;
+    p.max_units = 0;
+    p.half_ulp = 0;
+    if (p.units_path && a.max_cost > 0.0) {
+        uint64_t bits;
+        std::memcpy(&bits, &a.max_cost, sizeof bits);
+        const int be = (int)((bits >> 52) & 0x7ff);
+        const uint64_t m = (bits & ((1ull << 52) - 1)) | (be ? (1ull << 52) : 0ull);
+        const int sh = (be ? be : 1) - 1075 + 52;  // max_cost * 2^52 = m * 2^sh
+        p.max_units = sh >= 0 ? m << sh : (sh > -64 ? m >> -sh : 0);
+    }
+    if (p.units_path) {  // the largest sum ever compared is below max_cost + 3
+        const uint64_t top = p.max_units + (3ull << 52);
+        int L = 64;
+        while (L > 0 && !(top >> (L - 1)))
+            --L;
+        p.half_ulp = L > 53 ? 1ull << (L - 54) : 0;  // no rounding below 2^53 units
+    }
     p.out_depth = a.out_depth;
     p.out_cu = a.out_cu;
     p.out_benefit = a.out_benefit;

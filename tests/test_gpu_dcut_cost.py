@@ -79,3 +79,40 @@ def test_dcut_cost_invalid_confidence():
     assert st == sv.SPEC_OK
     assert v.device_status() == sv.SPEC_ERR_INVALID_ARG
     assert depth.cpu().tolist() == [-1, -1] and cu.cpu().tolist() == [-1, -1, -1]
+
+
+def test_dcut_cost_edge_values_against_oracle():
+    """Values at the edges of the integer forms of the fp64 operations:
+    zero confidences, confidences of 1 and 1 - 2^-24, subnormal confidences
+    and products that underflow the normal range (the hardware path), and
+    budgets equal to an exact running total of the costs and one ulp below
+    it (the admission's <= decided on the rounded sum)."""
+    v = Verifier(8, 8, 1)
+    tiny = np.float32(1e-40)  # a subnormal float
+    cases = []
+    K = 16
+    rows = [np.ones(K), np.zeros(K), np.full(K, np.float32(1 - 2.0 ** -24)),
+            np.full(K, 1e-30), np.r_[np.ones(8), np.full(8, tiny)],
+            np.linspace(1.0, 0.2, K), np.full(K, 0.5), np.r_[0.9, np.zeros(K - 1)]]
+    conf = np.array(rows, np.float32)
+    kmax = np.full(len(rows), K, np.int32)
+    for max_cost in (0.0, 1.0, 3.0, 7.5, 1e9, -1.0, float("inf"), 5e-324):
+        cases.append((conf, kmax, max_cost))
+    # equal benefits everywhere: every request takes depth 2 at cost 1.2, and
+    # the running total is the fp64 sum 1.2 + 1.2 + ...; a budget equal to
+    # that sum admits n requests, one ulp below admits n - 1
+    conf2 = np.ones((12, 2), np.float32)
+    kmax2 = np.full(12, 2, np.int32)
+    t = 0.0
+    for n in range(1, 12):
+        t = t + 1.2
+        for mc in (t, float(np.nextafter(t, 0.0)), float(np.nextafter(t, 10.0))):
+            cases.append((conf2, kmax2, mc))
+    for conf_, kmax_, mc in cases:
+        d, cu, ben = run(v, conf_, kmax_, mc)
+        o = O.dcut_schedule_cost(conf_, kmax_, mc)
+        assert o.status == O.OK
+        assert d.tolist() == o.depth.tolist(), mc
+        assert cu.tolist() == o.cu.tolist(), mc
+        assert ben.tobytes() == o.benefit.tobytes(), mc
+    assert v.device_status() == sv.SPEC_OK
