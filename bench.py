@@ -271,6 +271,13 @@ def workload_of(args):
     return w, T
 
 
+def traffic_key(args, T):
+    """The profiles/ncu_traffic.txt key of a bench line: the workload's name,
+    with _T<temperature> when --temperature changes the workload's own."""
+    T0 = WORKLOADS[args.workload][1]
+    return args.workload if T == T0 else f"{args.workload}_T{T:g}"
+
+
 def workload_desc(w, T, name=None):
     extra = (f", cost-unit D-cut (dcut_allocate_cost, max_cost {DCUT_MAX_COST})"
              if name in COST_WORKLOADS else "")
@@ -380,22 +387,21 @@ def oracle_request(orc, h, i):
 
 
 def oracle_sample_rate(h, seconds, threads, max_requests=None):
-    """Positions/s of the oracle over whole requests, round-robin, on `threads`
-    host threads (the C oracle releases the GIL), for about `seconds`."""
+    """Positions/s of the oracle over whole requests on `threads` host
+    threads (the C oracle releases the GIL), for about `seconds`: rounds of
+    the batch's requests, each round handed to the pool at once so that no
+    thread waits for another's longer request."""
     import oracle as orc
     orc.load()
     B = len(h["k"])
-    order = list(range(B))
     done_pos = 0
     done_req = 0
     t0 = time.perf_counter()
     with ThreadPoolExecutor(threads) as ex:
-        i = 0
         while True:
-            chunk = [order[(i + j) % B] for j in range(threads)]
-            i += threads
-            done_pos += sum(ex.map(lambda r: oracle_request(orc, h, r), chunk))
-            done_req += len(chunk)
+            n = B if not max_requests else max(1, min(B, max_requests - done_req))
+            done_pos += sum(ex.map(lambda r: oracle_request(orc, h, r), range(n)))
+            done_req += n
             el = time.perf_counter() - t0
             if el >= seconds or (max_requests and done_req >= max_requests):
                 break
@@ -624,7 +630,7 @@ def run_ours(args, dist):
                "single_thread": {"value": rate1, "unit": UNIT, "cores": 1,
                                  "sample": f"{nreq1} whole requests, {el1:.1f} s"}}
 
-    traffic = recorded_traffic(args.workload, "stream_kernel")
+    traffic = recorded_traffic(traffic_key(args, T), "stream_kernel")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_dist": step_dist,
@@ -841,7 +847,7 @@ def run_sharded(args, dist):
                "sample": f"{nreq} whole requests of input set 0 ({workload_desc(w, T)}) on the "
                          f"whole vocabulary, one oracle call per request on {threads} host "
                          f"threads, {el:.1f} s"}
-    name = f"{args.workload}_tp{N}"
+    name = f"{traffic_key(args, T)}_tp{N}"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "ms_per_step_dist": step_dist,

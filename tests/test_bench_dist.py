@@ -145,3 +145,13 @@ def test_default_workload_is_the_largest_ragged_pair():
     w0, T0 = bench.workload_of(bench.parse_args(["--workload", "ragged0", "--temperature", "0"]))
     assert (w0.B, w0.V, T0) == (4, 32000, 0.0)
     assert "ragged_B128_V151936" in bench.workload_desc(w, T)
+
+
+def test_traffic_key_names_an_overridden_temperature():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    args = bench.parse_args(["--workload", "ragged17", "--temperature", "0"])
+    assert bench.traffic_key(args, 0.0) == "ragged17_T0"
+    args = bench.parse_args(["--workload", "block"])
+    assert bench.traffic_key(args, bench.WORKLOADS["block"][1]) == "block"
