@@ -582,8 +582,10 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     bool past = true, redo = false;
     ff base{0.f, 0.f}, target{0.f, 0.f};
     for (int pass = 0; pass < 2; ++pass) {
-        ff mine{0.f, 0.f};
-        for (int sl = 0; sl < nsl; ++sl) {
+        // the slices last to first: the first (the largest) stays staged for
+        // the owner's search, which finds the target there most often
+        for (int k = 0; k < nsl; ++k) {
+            const int sl = nsl - 1 - k;
             const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
             const bool cp = !(pass == 0 && sl == 0 && staged == 0);
             const ff ss =
@@ -594,8 +596,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
             weighed = sl;
             if (tid == 0)
                 slice_tot[sl] = ss;
-            mine = ff_add(mine, ss);
         }
+        __syncthreads();  // slice_tot complete
+        ff mine{0.f, 0.f};  // the range's sum, in slice order
+        for (int sl = 0; sl < nsl; ++sl)
+            mine = ff_add(mine, slice_tot[sl]);
         if (tid < ncl)
             st_cluster_ff(&cl_sum[pass][rank], (uint32_t)tid, mine);
         cluster_arrive_release();
@@ -646,8 +651,10 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     return y;
 }
 
-template <typename T, bool OUTLINE>
-__global__ void __launch_bounds__(kSampleThreads, 2) finish_sample_kernel(const FinishParams p)
+// MINB: CTAs per SM the registers must allow (4 caps them at 64, for grids
+// of more than four CTAs per SM; 2 otherwise).
+template <typename T, bool OUTLINE, int MINB>
+__global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(const FinishParams p)
 {
     extern __shared__ __align__(128) unsigned char dsm[];
     T *tb = reinterpret_cast<T *>(dsm);  // staged slice of the target row

@@ -184,15 +184,15 @@ static cudaError_t prepare_stream()
     return once;
 }
 
-template <typename T, bool OUTLINE>
+template <typename T, bool OUTLINE, int MINB>
 static cudaError_t prepare_finish_sample()
 {
     static cudaError_t once = [] {
-        cudaError_t e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE>,
+        cudaError_t e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE, MINB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              2 * kStageRowBytes);
         if (e == cudaSuccess)  // clusters of 16 CTAs
-            e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE>,
+            e = cudaFuncSetAttribute(finish_sample_kernel<T, OUTLINE, MINB>,
                                      cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         return e;
     }();
@@ -369,9 +369,16 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     // B=4, V=1024 10.4 inline vs 10.9; B=32 and B=64 at V >= 128000 0.7-3.3 us
     // faster inline.
     const bool outline = (int64_t)a.B * fp.ncl <= (int64_t)sm_count() && a.V >= 32768;
+    // A grid of more than four CTAs per SM (the half-size slices of
+    // draw_geometry) takes the instance whose registers allow four CTAs per
+    // SM: B=128, V=151936 0.1545 -> 0.1481 ms per step; smaller grids keep
+    // three (mtp 0.0200 vs 0.0208 with four).
+    const bool dense = !outline && (int64_t)a.B * fp.ncl > 4 * (int64_t)sm_count();
     cudaError_t err = cudaSuccess;
     if (!GREEDY)
-        err = outline ? prepare_finish_sample<T, true>() : prepare_finish_sample<T, false>();
+        err = outline ? prepare_finish_sample<T, true, 2>()
+                      : (dense ? prepare_finish_sample<T, false, 4>()
+                               : prepare_finish_sample<T, false, 2>());
     if (err != cudaSuccess)
         return err;
     if ((err = enqueue_stream<T, GREEDY>(sp, s, tr)) != cudaSuccess)
@@ -398,8 +405,9 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
-        err = outline ? cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, true>, fp)
-                      : cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, false>, fp);
+        err = outline ? cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, true, 2>, fp)
+              : dense ? cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, false, 4>, fp)
+                      : cudaLaunchKernelEx(&cfg, finish_sample_kernel<T, false, 2>, fp);
     }
     if (err != cudaSuccess)
         return err;
