@@ -24,3 +24,17 @@ def test_parity_cases_on_the_bounds_checked_build():
         env=env, capture_output=True, text=True, timeout=900, cwd=ROOT)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
     assert " passed" in r.stdout and "failed" not in r.stdout, r.stdout[-2000:]
+
+
+@pytest.mark.gpu
+def test_sharded_parity_cases_on_the_bounds_checked_build():
+    """The vocabulary-sharded kernels on the same build: uneven shard widths
+    (plain-load rows), the padded draft layout and a loose row bound."""
+    env = dict(os.environ, SPECVERIFY_LIB="libspecverify_debug.so")
+    r = subprocess.run(
+        [sys.executable, "-m", "pytest", "-q", "-m", "gpu", "-p", "no:cacheprovider",
+         os.path.join(ROOT, "tests", "test_gpu_shard.py"),
+         "-k", "(matches_oracle and (4099 or 12345)) or padded_draft_layout or loose_row_bound"],
+        env=env, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-2000:]
+    assert " passed" in r.stdout and "failed" not in r.stdout, r.stdout[-2000:]

@@ -209,3 +209,64 @@ def test_sharded_loose_row_bound(T):
     assert status == [sv.SPEC_OK] * 3
     assert_shards_agree(outs)
     parity.compare_batch(batch, outs[0])
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_expired_wait_on_one_shard_flags_it_and_poisons_its_outputs(T):
+    """The forced-expiry hook on shard 0's streaming pass: shard 0's status
+    says TIMEOUT and its accept step poisons every output it holds (the other
+    shards cannot see it, so the verification's outputs are unspecified, as
+    the header states); after its workspace is zeroed the same shards verify
+    correctly."""
+    V, N = 12000, 2
+    bounds = shard_bounds(V, N)
+    b = ragged_batch(6, V, T, "bf16", seed=47, kmin=2, kmax=6).to("cuda")
+    rows = b.n_target_rows
+    shards = [Shard(b.B, rows, bounds, r) for r in range(N)]
+    targets = shard_columns(b.target_logits, bounds)
+    drafts = shard_columns(b.draft_logits if T > 0 else None, bounds)
+    outs = [s.outputs() for s in shards]
+    assert sv.spec_test_expire_wait(3) == sv.SPEC_OK
+    try:
+        recs0 = shards[0].row_stats(targets[0], drafts[0], b.draft_tokens, b.cu_draft, T).clone()
+    finally:
+        assert sv.spec_test_expire_wait(-1) == sv.SPEC_OK
+    recs1 = shards[1].row_stats(targets[1], drafts[1], b.draft_tokens, b.cu_draft, T).clone()
+    rows_all = torch.stack([recs0, recs1])
+    shards[0].accept(rows_all, b.draft_tokens, b.cu_draft, T, b.u_accept, outs[0])
+    torch.cuda.synchronize()
+    assert sv.spec_get_device_status(shards[0].workspace) == sv.SPEC_ERR_TIMEOUT
+    assert bool((outs[0]["accept_len"] == -1).all())
+    assert bool((outs[0]["tokens"] == -1).all())
+    sv.check(sv.spec_workspace_init(shards[0].workspace), "workspace init")
+    sv.check(sv.spec_workspace_init(shards[1].workspace), "workspace init")
+    outs = verify_sharded_local(shards, targets, drafts, b.draft_tokens, b.cu_draft, T,
+                                b.u_accept, b.u_final)
+    torch.cuda.synchronize()
+    assert [sv.spec_get_device_status(s.workspace) for s in shards] == [sv.SPEC_OK] * N
+    parity.compare_batch(b, outs[0])
+
+
+@pytest.mark.parametrize("T", [0.0, 0.8])
+def test_distributed_driver_over_nccl_with_one_rank(T):
+    """verify_sharded with its real exchanges (torch.distributed over NCCL
+    on this GPU) in a group of one rank holding the whole vocabulary: the
+    all-gathers and the max all-reduce run on device tensors, and the
+    result is the oracle's."""
+    import torch.distributed as dist
+    from draft_verification_02_b300.sharded import DistExchange, verify_sharded
+    V = 9000
+    b = ragged_batch(8, V, T, "bf16", seed=53, kmax=8).to("cuda")
+    dist.init_process_group("nccl", store=dist.HashStore(), rank=0, world_size=1,
+                            device_id=torch.device("cuda", 0))
+    try:
+        shard = Shard(b.B, b.n_target_rows, [0, V], 0)
+        out = verify_sharded(shard, DistExchange(), b.target_logits,
+                             b.draft_logits if T > 0 else None, b.draft_tokens, b.cu_draft, T,
+                             b.u_accept, b.u_final)
+        torch.cuda.synchronize()
+    finally:
+        dist.destroy_process_group()
+    assert sv.spec_get_device_status(shard.workspace) == sv.SPEC_OK
+    rep = parity.compare_batch(b, out)
+    assert rep["exempt_accept"] + rep["exempt_final"] <= MAX_EXEMPT, rep
