@@ -237,13 +237,18 @@ static bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stag
 
 // Geometry of a cluster draw over V entries, one cluster per draw: ncl
 // ranges of R entries, weighed in slices.  16 CTAs per draw while the
-// clusters fit the GPU at two CTAs per SM, else 8; slices of half the
-// largest size once the grid holds more than four CTAs per SM (less shared
-// memory per CTA, so more of them resident).  Measured on B300, ms per step:
-// B = 16, V = 128000: 16 CTAs 0.0206, 8 CTAs 0.0222; B = 32 and 64 at
-// V = 151936: 8 CTAs and 48 KB slices best (0.0703, 0.0930; 16 CTAs 0.0761,
-// 0.1008); B = 128, V = 151936: 24 KB slices 0.1596, 48 KB 0.1652, 16 KB
-// 0.1646, 12 KB 0.1667.  False when the vocabulary exceeds the slice table.
+// clusters fit the GPU at two CTAs per SM, else 8; a grid of more than two
+// CTAs per SM (a "dense" grid) takes slices of half the largest size, so
+// that four CTAs fit an SM, with the finish-kernel instance whose registers
+// allow four.  Measured on B300, ms per step: B = 16, V = 128000: 16 CTAs
+// 0.0206, 8 CTAs 0.0222; B = 32 at V = 151936: 8 CTAs, 48 KB slices best
+// (0.0690; dense from one CTA per SM 0.0705, 16 CTAs 0.0755); B = 64 at
+// V = 151936: dense 0.0845, 48 KB slices at three CTAs per SM 0.0915;
+// B = 128: dense 0.1472, 48 KB slices 0.1652.  False when the vocabulary
+// exceeds the slice table.
+#ifndef SV_DENSE_PER_SM
+#define SV_DENSE_PER_SM 2
+#endif
 static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
 {
     const int64_t sms = sm_count();
@@ -251,7 +256,7 @@ static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
 #ifdef SV_NCL
     ncl = SV_NCL;
 #endif
-    if (draws * ncl > 4 * sms && fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
+    if (draws * ncl > SV_DENSE_PER_SM * sms && fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
         return true;
     return fill_draw_geometry(fp, ncl, V, e, kStageRowBytes);
 }
@@ -369,11 +374,12 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     // B=4, V=1024 10.4 inline vs 10.9; B=32 and B=64 at V >= 128000 0.7-3.3 us
     // faster inline.
     const bool outline = (int64_t)a.B * fp.ncl <= (int64_t)sm_count() && a.V >= 32768;
-    // A grid of more than four CTAs per SM (the half-size slices of
-    // draw_geometry) takes the instance whose registers allow four CTAs per
-    // SM: B=128, V=151936 0.1545 -> 0.1481 ms per step; smaller grids keep
-    // three (mtp 0.0200 vs 0.0208 with four).
-    const bool dense = !outline && (int64_t)a.B * fp.ncl > 4 * (int64_t)sm_count();
+    // A dense grid (the half-size slices of draw_geometry) takes the
+    // instance whose registers allow four CTAs per SM: B=128, V=151936
+    // 0.1545 -> 0.1481 ms per step, B=64 0.0915 -> 0.0845; smaller grids
+    // keep three (mtp 0.0200 vs 0.0208 with four).
+    const bool dense =
+        !outline && (int64_t)a.B * fp.ncl > SV_DENSE_PER_SM * (int64_t)sm_count();
     cudaError_t err = cudaSuccess;
     if (!GREEDY)
         err = outline ? prepare_finish_sample<T, true, 2>()
