@@ -443,6 +443,9 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
     __shared__ int s_bad[kCostCluster];         // written by every CTA of the cluster
     __shared__ int s_ncand;
     __shared__ int warp_tot[33];
+    __shared__ uint64_t warp_sum[kCostThreads / 32];  // the admission's scan
+    __shared__ uint64_t s_x;
+    __shared__ int s_first;
     const int tid = threadIdx.x, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();
     if (tid >= 1 && tid <= kMaxDraft) {  // staged: lanes index them by their own depth
@@ -573,55 +576,131 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
         rank_cost[t] = p.units_path ? cost_units[dd] : cost_bits[dd];
     }
     __syncthreads();
-    // one thread decides in rank order; the decisions (one byte per rank,
-    // kept in the ranks' cost slots) are applied in parallel afterwards
-    uint8_t *admitted = reinterpret_cast<uint8_t *>(depth + p.B);  // [B]
-    if (tid == 0) {
-        if (p.units_path) {  // totals below 2^11: 64-bit units of 2^-52
-            // The rounded running total T and the exact sum X of the admitted
-            // costs differ by at most k half-ulps after k admissions (every
-            // rounded sum is below max_cost + 3), so a step whose exact sum
-            // lies farther than (k + 1) half-ulps from max_cost is decided by
-            // X alone, with a two-instruction chain.  A step inside that
-            // margin (a budget on or next to a reachable sum) sends the whole
-            // walk to the rounded chain.
-            const uint64_t M = p.max_units;
-            uint64_t X = 0, margin = p.half_ulp;
-            bool near = false;
-            for (int t0 = 0; t0 < ncand && !near; t0 += 8) {
-                uint64_t c[8];  // the next costs, loaded ahead of the chain
+    uint8_t *admitted = reinterpret_cast<uint8_t *>(depth + p.B);  // [B] per rank
+    if (p.units_path) {
+        // The rounded running total T and the exact sum X of the admitted
+        // costs differ by at most k half-ulps after k admissions (every
+        // rounded sum is below max_cost + 3), so a step whose exact sum lies
+        // farther than (k + 1) half-ulps from max_cost is decided by X alone.
+        //  - Until the first rejection every rank is admitted, so X is the
+        //    prefix sum of the costs: one block-wide scan finds the first
+        //    rank that is not surely admitted.
+        //  - After it the remaining budget is below that rank's cost (at
+        //    most 3) and every cost is at least 1, so at most two more ranks
+        //    fit: each is found by a block-wide search for the next rank
+        //    that is not surely rejected.
+        // A decision inside the margin (a budget on or next to a reachable
+        // sum) sends the whole walk to the rounded chain, one thread.
+        const uint64_t M = p.max_units, hu = p.half_ulp;
+        const uint64_t SAT = ~0ull >> 1;  // above every budget
+        const int per = (ncand + kCostThreads - 1) / kCostThreads;
+        const int t0 = min(ncand, tid * per), t1 = min(ncand, t0 + per);
+        uint64_t seg = 0;
+        for (int t = t0; t < t1; ++t) {
+            admitted[t] = 0;
+            seg = min(SAT, seg + rank_cost[t]);
+        }
+        // exclusive scan of the segment sums (saturating)
+        uint64_t incl = seg;
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    c[k] = t0 + k < ncand ? rank_cost[t0 + k] : ~0ull >> 1;
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t y = X + c[k];
-                    const bool adm = y + margin <= M;
-                    near |= !adm && y <= M + margin;
-                    X = adm ? y : X;
-                    margin += adm ? p.half_ulp : 0;
-                    if (t0 + k < ncand)
-                        admitted[t0 + k] = adm;
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o)
+                incl = min(SAT, incl + n);
+        }
+        if (lane == 31)
+            warp_sum[tid >> 5] = incl;
+        if (tid == 0)
+            s_first = INT_MAX;
+        __syncthreads();
+        uint64_t E = incl - seg;  // this thread's exclusive prefix, then each rank's
+        for (int w = 0; w < (tid >> 5); ++w)
+            E = min(SAT, E + warp_sum[w]);
+        int mine = INT_MAX;  // this thread's first rank that is not surely admitted
+        for (int t = t0; t < t1; ++t) {
+            const uint64_t y = min(SAT, E + rank_cost[t]);
+            if (y + (uint64_t)(t + 1) * hu > M) {
+                mine = t;
+                atomicMin(&s_first, t);
+                break;
+            }
+            E = y;
+        }
+        __syncthreads();
+        const int first = s_first;
+        for (int t = t0; t < t1 && t < first; ++t)
+            admitted[t] = 1;
+        if (first < ncand) {
+            if (mine == first)
+                s_x = E;  // the exact sum of the ranks before `first`, all admitted
+            __syncthreads();
+            // From `first` on, each step takes the next rank that is not
+            // surely rejected.  A surely admitted one is admitted; one inside
+            // the margin is decided on the rounded total T (computed once,
+            // when first needed, from the ranks admitted so far), and a
+            // rejection at T also rejects every later rank whose cost is no
+            // smaller while T stays the same.  The budget left after the first
+            // step that is not sure is below one cost, so few steps follow.
+            uint64_t X = s_x, T = 0, c_rej = ~0ull;
+            bool have_T = false;
+            int k = first, cur = first - 1, n_late = 0;
+            int late[4];  // ranks admitted from `first` on, in order (at most 3)
+            for (;;) {
+                __syncthreads();  // every thread has read s_first
+                if (tid == 0)
+                    s_first = INT_MAX;
+                __syncthreads();
+                const uint64_t lim = M + (uint64_t)(k + 1) * hu;
+                for (int t = max(t0, cur + 1); t < t1; ++t)
+                    if (rank_cost[t] < c_rej && X + rank_cost[t] <= lim) {
+                        atomicMin(&s_first, t);
+                        break;
+                    }
+                __syncthreads();
+                const int nx = s_first;
+                if (nx >= ncand)
+                    break;  // every later rank is rejected
+                const uint64_t c = rank_cost[nx];
+                bool adm;
+                if (X + c + (uint64_t)(k + 1) * hu <= M) {
+                    adm = true;  // surely admitted
+                    if (have_T)
+                        T = add_units_round(T, c);
+                } else {  // inside the margin: the rounded total decides
+                    if (!have_T) {
+                        T = 0;  // the ranks admitted so far, in rank order
+                        for (int t = 0; t < first; ++t)
+                            T = add_units_round(T, rank_cost[t]);
+                        for (int q = 0; q < n_late; ++q)
+                            T = add_units_round(T, rank_cost[late[q]]);
+                        have_T = true;
+                    }
+                    const uint64_t nt = add_units_round(T, c);
+                    adm = nt <= M;
+                    if (adm)
+                        T = nt;
                 }
-            }
-            if (near) {
-                uint64_t total = 0;
-                for (int t = 0; t < ncand; ++t) {
-                    const uint64_t nt = add_units_round(total, rank_cost[t]);
-                    const bool adm = nt <= M;
-                    total = adm ? nt : total;
-                    admitted[t] = adm;
+                if (adm) {
+                    if (tid == 0)
+                        admitted[nx] = 1;
+                    X += c;
+                    ++k;
+                    c_rej = ~0ull;
+                    if (n_late < 4)
+                        late[n_late++] = nx;
+                } else {
+                    c_rej = c;
                 }
+                cur = nx;
             }
-        } else {  // a large budget (or none): the fp64 hardware
-            double total = 0.0;
-            for (int t = 0; t < ncand; ++t) {
-                const double nt =
-                    __dadd_rn(total, __longlong_as_double((long long)rank_cost[t]));
-                const bool adm = p.max_cost >= 0.0 && nt <= p.max_cost;
-                total = adm ? nt : total;
-                admitted[t] = adm;
-            }
+        }
+    } else if (tid == 0) {  // a large budget (or none): the fp64 hardware, one thread
+        double total = 0.0;
+        for (int t = 0; t < ncand; ++t) {
+            const double nt = __dadd_rn(total, __longlong_as_double((long long)rank_cost[t]));
+            const bool adm = p.max_cost >= 0.0 && nt <= p.max_cost;
+            total = adm ? nt : total;
+            admitted[t] = adm;
         }
     }
     __syncthreads();
