@@ -436,7 +436,6 @@ struct DrawShared {
     ff *wred, *slice_tot, *s_excl;
     ff (*cl_sum)[kCluster];  // written by every CTA of the cluster
     int *s_hit, *s_last, *s_expired;
-    ff *s_total;  // S, the sum of every weight (may be null)
 };
 
 // The search of the CTA whose range [r0, r1) (nsl slices with totals
@@ -555,14 +554,11 @@ __device__ __forceinline__ int find_in_range(const FinishParams &p, const DrawCt
 // CTA, the drawn index (or -1 if it found none); -2 in the other CTAs, -1 in
 // all CTAs when no range has mass.  Every CTA of the cluster must call it
 // (it contains cluster barriers); no shared memory of another CTA is touched
-// after it returns.  `staged`: the slice of this CTA's range already in the
-// target buffer (-1 none); phase_io (may be null): the parity of the copy
-// barrier's next phase, updated for the copies made here.
+// after it returns.  The CTA's copy barrier starts at phase parity 0.
 template <typename T, bool OUTLINE>
 __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, const T *trow,
                                           const T *drow, float uf, uint32_t rank, int ncl,
-                                          const DrawShared<T> &sh, int staged = -1,
-                                          uint32_t *phase_io = nullptr)
+                                          const DrawShared<T> &sh)
 {
     const int tid = threadIdx.x, lane = tid & 31;
     T *tb = sh.tb, *db = sh.db;
@@ -574,7 +570,7 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
     const int r0 = min(p.V, (int)rank * p.R), r1 = min(p.V, r0 + p.R);
     const int nsl = r1 > r0 ? (r1 - r0 + p.slice - 1) / p.slice : 0;
     int weighed = -1;  // slice staged in shared memory
-    uint32_t phase = phase_io ? *phase_io : 0u;  // parity of the copy barrier's next phase
+    uint32_t phase = 0u;  // parity of the copy barrier's next phase
 
     // pass 0 sums max(0, p_a - q_a) (or p_K); an all-zero residual makes a
     // second pass over p_a (the same decision in every CTA)
@@ -587,12 +583,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
         for (int k = 0; k < nsl; ++k) {
             const int sl = nsl - 1 - k;
             const int c0 = r0 + sl * p.slice, len = min(p.slice, r1 - c0);
-            const bool cp = !(pass == 0 && sl == 0 && staged == 0);
             const ff ss =
                 OUTLINE ? weigh_slice_outlined<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase,
-                                                  piece, wred, &s_expired, cp)
+                                                  piece, wred, &s_expired, true)
                         : weigh_slice<T>(p, d, trow, drow, c0, len, tb, db, &bar, &phase, piece,
-                                         wred, &s_expired, cp);
+                                         wred, &s_expired);
             weighed = sl;
             if (tid == 0)
                 slice_tot[sl] = ss;
@@ -630,8 +625,6 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
             const int src = cs < 0 ? 0 : cs;
             base = {__shfl_sync(0xffffffffu, excl.hi, src), __shfl_sync(0xffffffffu, excl.lo, src)};
             past = over == 0u;
-            if (sh.s_total && tid == 0)
-                *sh.s_total = S;
             redo = !(S.hi > 0.f);
         }
         if (!(d.resid && redo))
@@ -639,16 +632,11 @@ __device__ __forceinline__ int draw_token(const FinishParams &p, DrawCtx d, cons
         d.resid = false;  // all-zero residual: draw from p_a instead
     }
     // no shared memory of another CTA is touched after this point
-    if (phase_io)
-        *phase_io = phase;
     if ((int)rank != cs)
         return cs < 0 ? -1 : -2;  // -1: no mass at all (never with finite rows)
 
-    const int y = find_in_range<T, OUTLINE>(p, d, trow, drow, r0, r1, nsl, base, target, past,
-                                            weighed, slice_tot, sh, phase);
-    if (phase_io)
-        *phase_io = phase;
-    return y;
+    return find_in_range<T, OUTLINE>(p, d, trow, drow, r0, r1, nsl, base, target, past, weighed,
+                                     slice_tot, sh, phase);
 }
 
 // MINB: CTAs per SM the registers must allow (4 caps them at 64, for grids
@@ -866,7 +854,7 @@ __global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(con
     const T *trow = tbase + trow_i * p.V;
     const T *drow = d.resid ? dbase + drow_i * p.V : nullptr;
     const DrawShared<T> sh{tb,     db,      &bar,    piece,      wred,   slice_tot,
-                           s_excl, cl_sum,  &s_hit,  &s_last,    &s_expired, nullptr};
+                           s_excl, cl_sum,  &s_hit,  &s_last,    &s_expired};
     const int y0 = draw_token<T, OUTLINE>(p, d, trow, drow, uf, rank, ncl, sh);
     if (y0 == -2)
         return;  // another CTA's range holds u*S

@@ -546,7 +546,7 @@ __global__ void __launch_bounds__(kSampleThreads) shard_draw_kernel(const ShardD
     const T *drow =
         d.resid ? reinterpret_cast<const T *>(p.draft) + st.drow * (int64_t)p.V : nullptr;
     const DrawShared<T> sh{tb,     db,      &bar,   piece,  wred,       slice_tot,
-                           s_excl, nullptr, &s_hit, &s_last, &s_expired, nullptr};
+                           s_excl, nullptr, &s_hit, &s_last, &s_expired};
     uint32_t phase = 0;
     const int y = find_in_range<T, false>(p, d, trow, drow, 0, p.V, nsl, base, target, past, -1,
                                           slice_tot, sh, phase);
