@@ -75,13 +75,13 @@ DRAFT_WORKLOADS = ("draft", "draft_greedy", "confidence")
 COST_WORKLOADS = ("dcut_cost",)
 DCUT_MAX_COST = 96.0
 DRAFT_METRIC = "drafted positions/sec and achieved HBM GB/s (fraction of peak) at 1 B300"
-# the sources of each roofline kernel and of its launch geometry: a recorded
-# ncu traffic figure holds only while these hash the same
+# the sources of each roofline kernel and of its split (verify_params.cuh
+# holds the streaming pass's unit planner): a recorded ncu traffic figure
+# holds only while these hash the same
 KERNEL_SOURCES = {
     "stream_kernel": ["draft_verification_02_b300/csrc/stream_kernel.cuh",
                       "draft_verification_02_b300/csrc/verify_params.cuh",
-                      "draft_verification_02_b300/csrc/common.cuh",
-                      "draft_verification_02_b300/csrc/verify.cu"],
+                      "draft_verification_02_b300/csrc/common.cuh"],
     "draft_sample_kernel": ["draft_verification_02_b300/csrc/finish_kernel.cuh",
                             "draft_verification_02_b300/csrc/verify_params.cuh",
                             "draft_verification_02_b300/csrc/common.cuh"],

@@ -692,8 +692,10 @@ __global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(con
     // the rows this warp merges: with at most one row per warp of a CTA,
     // every CTA merges all of them (row k = warp), else the rows are spread
     // over the cluster (k = rank + ncl * (warp + kSampleWarps * t)) and sent
-    // to every CTA.  Target rows 0..K, then draft rows 0..K-1; the logit at
-    // the drafted token of each such row.
+    // to every CTA; rows past the cluster's 2 * kSampleWarps * ncl (with
+    // clusters of 4 and K = 32 only) are merged by every CTA itself after the
+    // exchange.  Target rows 0..K, then draft rows 0..K-1; the logit at the
+    // drafted token of each such row.
     const bool local = nrows <= kSampleWarps;
     int my_k[2];
     float g[2] = {-INFINITY, -INFINITY};
@@ -729,13 +731,8 @@ __global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(con
 
     // ---- (m, s) and p(x) of the request's rows, one or two rows per warp of
     // the cluster, sent to every CTA
-    float mm[2] = {-INFINITY, -INFINITY}, px[2] = {0.f, 0.f};
-    ff sm[2] = {{0.f, 0.f}, {0.f, 0.f}};
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-        if (my_k[t] < 0)
-            continue;
-        const int k = my_k[t];
+    // merge of row k's partials into (m, s) across the warp
+    auto merge_row = [&](int k, float &m, ff &sr) {
         const int64_t rg = k <= K ? t0 + k : gs.nt + cu_i + (k - K - 1);
         int wf, wl;
         row_span(gs, rg, wf, wl);
@@ -743,14 +740,22 @@ __global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(con
             if (!SV_IN_BOUNDS(rg + w, p.part_cap, p.status))
                 continue;
             const Partial pt = load_partial(p.part + rg + w);
-            lse_combine(mm[t], sm[t], pt.m, {pt.s_hi, pt.s_lo}, p.c);
+            lse_combine(m, sr, pt.m, {pt.s_hi, pt.s_lo}, p.c);
         }
 #pragma unroll 1
         for (int o = 16; o > 0; o >>= 1) {
-            const float mo = __shfl_xor_sync(0xffffffffu, mm[t], o);
-            const ff so = ff_shfl_xor(sm[t], o);
-            lse_combine(mm[t], sm[t], mo, so, p.c);
+            const float mo = __shfl_xor_sync(0xffffffffu, m, o);
+            const ff so = ff_shfl_xor(sr, o);
+            lse_combine(m, sr, mo, so, p.c);
         }
+    };
+    float mm[2] = {-INFINITY, -INFINITY}, px[2] = {0.f, 0.f};
+    ff sm[2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (my_k[t] < 0)
+            continue;
+        merge_row(my_k[t], mm[t], sm[t]);
         px[t] = g_ok[t] && row_ok(mm[t], sm[t]) ? softmax_at(g[t], mm[t], sm[t], p.c) : 0.f;
     }
     if (local) {  // every CTA merged every row itself
@@ -769,6 +774,35 @@ __global__ void __launch_bounds__(kSampleThreads, MINB) finish_sample_kernel(con
                 st_cluster_row(row_m, row_s, row_p, my_k[t], (uint32_t)lane, mm[t], sm[t], px[t]);
         cluster_arrive_release();
         cluster_wait_acquire();  // (1) every CTA holds every row's (m, s, p(x))
+        const int spread = 2 * kSampleWarps * ncl;
+        if (nrows > spread) {  // the rows past the cluster's share, in every CTA
+#pragma unroll 1
+            for (int k = spread + warp; k < nrows; k += kSampleWarps) {
+                bool ok = false;
+                float gj = -INFINITY;
+                if (k != K) {  // the logit at the drafted token (the bonus row has none)
+                    const int j = k < K ? k : k - K - 1;
+                    const int64_t dj = draft_index(p.draft_stride, p.cu, i, j);
+                    const int xj =
+                        SV_IN_BOUNDS(dj, p.draft_rows, p.status) ? __ldg(p.tokens + dj) : -1;
+                    ok = xj >= 0 && xj < p.V &&
+                         (k < K ? SV_IN_BOUNDS(t0 + j, p.g.max_rows, p.status)
+                                : SV_IN_BOUNDS(dj, p.draft_rows, p.status));
+                    if (ok)
+                        gj = k < K ? Elem<T>::ld_global(tbase + (t0 + j) * p.V, xj)
+                                   : Elem<T>::ld_global(dbase + dj * p.V, xj);
+                }
+                float m = -INFINITY;
+                ff sr{0.f, 0.f};
+                merge_row(k, m, sr);
+                if (lane == 0) {
+                    row_m[k] = m;
+                    row_s[k] = sr;
+                    row_p[k] = ok && row_ok(m, sr) ? softmax_at(gj, m, sr, p.c) : 0.f;
+                }
+            }
+            __syncthreads();
+        }
     }
 
     // ---- accept test and first rejection: every warp takes the same decision

@@ -131,67 +131,6 @@ static int sm_count()
     return n;
 }
 
-// Unit size for a balanced split: U = rows * ceil(V / Q) units over P warps
-// puts ceil(U / P) units on the busiest warp.  Q is a multiple of the
-// 16-byte granule, at most kPieceBytesMax.  Every unit costs a warp the same
-// instructions whatever its size (the unit loop is unrolled to the largest
-// unit), so:
-//  - a short pass (at most kShortPassUnits on the busiest warp at the best
-//    Q) takes the largest Q with that fewest count: fewest units in all;
-//  - a longer pass is bound by bytes and minimises the busiest warp's
-//    elements plus a fixed cost per unit (SV_UNIT_COST), preferring larger Q.
-// Measured on B300, streaming pass in us (the earlier rule: elements plus
-// 64): 576 rows of V = 128000 at T = 1, padded drafts (11 units a warp)
-// 36.45 -> 33.80; B = 16 at V = 151936 (7 a warp) 21.27 -> 19.40.  The
-// largest Q for longer passes was slower: B = 128 at V = 151936, T = 0.7,
-// 113.8 -> 114.1; B = 32, K = 16 at T = 0 (12 a warp) 33.9 -> 34.5.
-#ifndef SV_UNIT_COST
-#define SV_UNIT_COST 512
-#endif
-#ifndef SV_SHORT_PASS_UNITS
-#define SV_SHORT_PASS_UNITS 11
-#endif
-constexpr int64_t kShortPassUnits = SV_SHORT_PASS_UNITS;
-
-static Geometry plan(int64_t rows_total, int64_t max_rows, int V, int elem, int P_max)
-{
-    Geometry g{};
-    g.max_rows = max_rows;
-    const int gran = 16 / elem;
-    const int qmax = kPieceBytesMax / elem;
-    const int64_t total = rows_total * (int64_t)V;
-    int64_t P = P_max;
-    const int64_t min_work = 2048 / elem;  // at least ~2 KB per warp
-    if (total / min_work < P)
-        P = std::max<int64_t>(1, total / min_work);
-    double best_cost = 1e300;
-    int best_q = qmax, fewest_q = qmax;
-    int64_t fewest = INT64_MAX;
-    for (int q = qmax; q >= gran && q >= qmax / 8; q -= gran) {
-        const int64_t cpr = (V + q - 1) / q;
-        const int64_t U = rows_total * cpr;
-        const int64_t per = (U + P - 1) / P;
-        const double cost = (double)per * (double)(std::min<int64_t>(q, V) + SV_UNIT_COST);
-        if (cost < best_cost * 0.999) {
-            best_cost = cost;
-            best_q = q;
-        }
-        if (per < fewest) {
-            fewest = per;
-            fewest_q = q;
-        }
-    }
-    if (fewest <= kShortPassUnits)
-        best_q = fewest_q;
-    g.Q = std::min(best_q, ((V + gran - 1) / gran) * gran);
-    g.cpr = (V + g.Q - 1) / g.Q;
-    g.U = rows_total * (int64_t)g.cpr;
-    g.P = (int)std::min<int64_t>(P, g.U);
-    g.slots = rows_total - max_rows;
-    g.nt = max_rows;
-    return g;
-}
-
 template <typename T, bool GREEDY>
 static cudaError_t prepare_stream()
 {
@@ -262,14 +201,16 @@ static bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stag
 
 // Geometry of a cluster draw over V entries, one cluster per draw: ncl
 // ranges of R entries, weighed in slices.  16 CTAs per draw while the
-// clusters fit the GPU at two CTAs per SM, else 8; a grid of more than two
-// CTAs per SM (a "dense" grid) takes slices of half the largest size, so
-// that four CTAs fit an SM, with the finish-kernel instance whose registers
-// allow four.  Measured on B300, ms per step: B = 16, V = 128000: 16 CTAs
-// 0.0206, 8 CTAs 0.0222; B = 32 at V = 151936: 8 CTAs, 48 KB slices best
-// (0.0690; dense from one CTA per SM 0.0705, 16 CTAs 0.0755); B = 64 at
-// V = 151936: dense 0.0845, 48 KB slices at three CTAs per SM 0.0915;
-// B = 128: dense 0.1472, 48 KB slices 0.1652.  False when the vocabulary
+// clusters fit the GPU at two CTAs per SM, else 8 while they fit it at four,
+// else 4; a grid of more than two CTAs per SM (a "dense" grid) takes slices
+// of half the largest size, so that four CTAs fit an SM, with the
+// finish-kernel instance whose registers allow four.  Measured on B300, ms
+// per step: B = 16, V = 128000: 16 CTAs 0.0206, 8 CTAs 0.0222, 4 CTAs
+// 0.0278; B = 32 at V = 151936: 8 CTAs, 48 KB slices best (0.0690; dense
+// from one CTA per SM 0.0705, 16 CTAs 0.0755, 4 CTAs 0.0773); B = 64 at
+// V = 151936: 8 CTAs dense 0.0794, 4 CTAs 0.0814, 48 KB slices at three
+// CTAs per SM 0.0915; B = 128: 4 CTAs dense (one wave) 0.1403, 8 CTAs dense
+// (1.73 waves) 0.1473, 48 KB slices 0.1652.  False when the vocabulary
 // exceeds the slice table.
 #ifndef SV_DENSE_PER_SM
 #define SV_DENSE_PER_SM 2
@@ -277,13 +218,22 @@ static bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stag
 static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
 {
     const int64_t sms = sm_count();
-    int ncl = draws * kCluster <= 2 * sms ? kCluster : kCluster / 2;
+    int ncl = draws * kCluster <= 2 * sms              ? kCluster
+              : draws * (kCluster / 2) <= 4 * sms ? kCluster / 2
+                                                       : kCluster / 4;
 #ifdef SV_NCL
     ncl = SV_NCL;
 #endif
-    if (draws * ncl > SV_DENSE_PER_SM * sms && fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
-        return true;
-    return fill_draw_geometry(fp, ncl, V, e, kStageRowBytes);
+    // a vocabulary whose ranges need more slices than the table holds takes
+    // more CTAs per draw
+    for (; ncl <= kCluster; ncl *= 2) {
+        if (draws * ncl > SV_DENSE_PER_SM * sms &&
+            fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
+            return true;
+        if (fill_draw_geometry(fp, ncl, V, e, kStageRowBytes))
+            return true;
+    }
+    return false;
 }
 
 // Kernel 1's parameters for a verification call (a.out_tokens / a.out_len
@@ -382,8 +332,9 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.g = g;
     if (!GREEDY && !draw_geometry(fp, a.B, a.V, e))
         return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
-    // the finish kernel merges up to two rows per warp of the cluster
-    if (!GREEDY && 2 * kMaxDraft + 1 > 2 * kSampleWarps * fp.ncl)
+    // the finish kernel merges up to two rows per warp of the cluster, then
+    // one per warp of each CTA
+    if (!GREEDY && 2 * kMaxDraft + 1 > 2 * kSampleWarps * fp.ncl + kSampleWarps)
         return cudaErrorInvalidValue;
     fp.tma = tma;
     fp.c = sp.c;

@@ -30,6 +30,67 @@ struct Geometry {
     int64_t nt;        // target rows of the index space (max_rows in the host's split)
 };
 
+// Unit size for a balanced split: U = rows * ceil(V / Q) units over P warps
+// puts ceil(U / P) units on the busiest warp.  Q is a multiple of the
+// 16-byte granule, at most kPieceBytesMax.  Every unit costs a warp the same
+// instructions whatever its size (the unit loop is unrolled to the largest
+// unit), so:
+//  - a short pass (at most kShortPassUnits on the busiest warp at the best
+//    Q) takes the largest Q with that fewest count: fewest units in all;
+//  - a longer pass is bound by bytes and minimises the busiest warp's
+//    elements plus a fixed cost per unit (SV_UNIT_COST), preferring larger Q.
+// Measured on B300, streaming pass in us (the earlier rule: elements plus
+// 64): 576 rows of V = 128000 at T = 1, padded drafts (11 units a warp)
+// 36.45 -> 33.80; B = 16 at V = 151936 (7 a warp) 21.27 -> 19.40.  The
+// largest Q for longer passes was slower: B = 128 at V = 151936, T = 0.7,
+// 113.8 -> 114.1; B = 32, K = 16 at T = 0 (12 a warp) 33.9 -> 34.5.
+#ifndef SV_UNIT_COST
+#define SV_UNIT_COST 512
+#endif
+#ifndef SV_SHORT_PASS_UNITS
+#define SV_SHORT_PASS_UNITS 11
+#endif
+constexpr int64_t kShortPassUnits = SV_SHORT_PASS_UNITS;
+
+inline Geometry plan(int64_t rows_total, int64_t max_rows, int V, int elem, int P_max)
+{
+    Geometry g{};
+    g.max_rows = max_rows;
+    const int gran = 16 / elem;
+    const int qmax = kPieceBytesMax / elem;
+    const int64_t total = rows_total * (int64_t)V;
+    int64_t P = P_max;
+    const int64_t min_work = 2048 / elem;  // at least ~2 KB per warp
+    if (total / min_work < P)
+        P = std::max<int64_t>(1, total / min_work);
+    double best_cost = 1e300;
+    int best_q = qmax, fewest_q = qmax;
+    int64_t fewest = INT64_MAX;
+    for (int q = qmax; q >= gran && q >= qmax / 8; q -= gran) {
+        const int64_t cpr = (V + q - 1) / q;
+        const int64_t U = rows_total * cpr;
+        const int64_t per = (U + P - 1) / P;
+        const double cost = (double)per * (double)(std::min<int64_t>(q, V) + SV_UNIT_COST);
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best_q = q;
+        }
+        if (per < fewest) {
+            fewest = per;
+            fewest_q = q;
+        }
+    }
+    if (fewest <= kShortPassUnits)
+        best_q = fewest_q;
+    g.Q = std::min(best_q, ((V + gran - 1) / gran) * gran);
+    g.cpr = (V + g.Q - 1) / g.Q;
+    g.U = rows_total * (int64_t)g.cpr;
+    g.P = (int)std::min<int64_t>(P, g.U);
+    g.slots = rows_total - max_rows;
+    g.nt = max_rows;
+    return g;
+}
+
 struct StreamParams {
     const void *target;
     const void *draft;

@@ -99,6 +99,18 @@ def test_padded_draft_layout(T):
     check_batch(b)
 
 
+@pytest.mark.parametrize("V,dtype", [(5000, "bf16"), (4099, "f32")])
+@pytest.mark.parametrize("T", [0.7, 1.0])
+def test_four_cta_draws_at_full_depth(V, dtype, T):
+    """A batch large enough that each draw takes a cluster of 4 CTAs (more
+    than half a request per SM), with most requests at the largest depth
+    (65 rows: one more than the cluster's share, merged by every CTA)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    b = ragged_batch(sms // 2 + 4, V, T, dtype, seed=V + int(T * 10), kmin=28, kmax=32)
+    assert int(b.k.max()) == 32
+    check_batch(b)
+
+
 @pytest.mark.parametrize("T", [0.0, 0.7, 1.0, 1.3])
 def test_masked_vocabulary(T):
     b = ragged_batch(8, 3000, T, "bf16", seed=4, kmax=6, mask_frac=0.3)
