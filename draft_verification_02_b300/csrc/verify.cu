@@ -33,9 +33,10 @@
 // the logits at the drafted tokens) before waiting for kernel 1 to finish.
 //  - T = 0, finish_greedy_kernel: one CTA per request merges the argmax
 //    partials and runs the first-mismatch ballot.
-//  - T > 0, finish_sample_kernel: one cluster of 8 or 16 CTAs per request.
-//    The request's rows are merged one or two per warp of the cluster (their
-//    (m, s) and p(x) sent to every CTA through distributed shared memory);
+//  - T > 0, finish_sample_kernel: one cluster of 4, 8 or 16 CTAs per
+//    request.  The request's rows are merged one or two per warp of the
+//    cluster (their (m, s) and p(x) sent to every CTA through distributed
+//    shared memory; with 4 CTAs, a 65th row is merged by every CTA itself);
 //    every warp of every CTA runs the accept test and first-rejection ballot
 //    (identical bits everywhere), then each CTA stages its share of the
 //    final-draw rows with TMA and sums the weights.  The range sums are

@@ -127,7 +127,7 @@ struct FinishParams {
     int64_t draft_rows;  // rows the draft side may index
     int draft_stride;
     Geometry g;
-    int ncl;    // CTAs per request (cluster size) in the final draw: 8 or 16
+    int ncl;    // CTAs per request (cluster size) in the final draw: 4, 8 or 16
     int R;      // vocabulary entries per cluster CTA in the final draw
     int slice;  // entries of one row weighed at a time (multiple of 16 bytes)
     int pv;          // 16-byte vectors per thread piece of a slice (odd)
