@@ -526,3 +526,19 @@ def test_loose_row_bound_reads_only_real_rows(T, stride):
     assert v.device_status() == sv.SPEC_OK
     rep = parity.compare_batch(batch, out)
     assert rep["exempt_accept"] + rep["exempt_final"] <= MAX_EXEMPT, rep
+
+
+@pytest.mark.parametrize("T,stride", [(0.0, 0), (0.7, 0), (1.0, 8)])
+def test_loose_bound_over_a_long_host_split(T, stride):
+    """The largest host bound the call accepts, long enough that the host's
+    split balances bytes with units below the largest, over a few real rows:
+    the re-split keeps the host's units over the real rows, and every kernel
+    that reads the partials derives the same split from the offsets."""
+    B, V = 16, 151936
+    b = ragged_batch(B, V, T, "bf16", seed=43, kmin=0, kmax=8, draft_stride=stride)
+    loose = B * 33  # the largest bound the call accepts
+    b = pad_to_loose_bound(b, loose)
+    batch, out, v = run_gpu(b, rows=loose)
+    assert v.device_status() == sv.SPEC_OK
+    rep = parity.compare_batch(batch, out)
+    assert rep["exempt_accept"] + rep["exempt_final"] <= MAX_EXEMPT, rep
