@@ -21,6 +21,58 @@ constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kStageRowBytes = SV_STAGE_KB * 1024;  // largest slice of one row staged at a time
 constexpr int kMaxSlices = 64;             // slices per CTA range (bounds V)
 
+// Slices of at most stage_bytes per row for ncl ranges of a V-entry row;
+// false when a range needs more slices than the slice table holds.
+inline bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stage_bytes)
+{
+    const int gran = 16 / e;
+    fp.ncl = ncl;
+    const int R = (int)((((int64_t)V + ncl - 1) / ncl + gran - 1) / gran * gran);
+    const int slice = std::min(R, stage_bytes / e);
+    const int nv = (slice * e + 15) / 16;
+    fp.R = R;
+    fp.slice = slice;
+    fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
+    fp.stage_smem = (int)align_up((size_t)slice * e, 128);
+    return (R + slice - 1) / slice <= kMaxSlices;
+}
+
+// Geometry of a cluster draw over V entries, one cluster per draw: ncl
+// ranges of R entries, weighed in slices.  16 CTAs per draw while the
+// clusters fit the GPU at two CTAs per SM, else 8 while they fit it at four,
+// else 4; a grid of more than two CTAs per SM (a "dense" grid) takes slices
+// of half the largest size, so that four CTAs fit an SM, with the
+// finish-kernel instance whose registers allow four.  Measured on B300, ms
+// per step: B = 16, V = 128000: 16 CTAs 0.0206, 8 CTAs 0.0222, 4 CTAs
+// 0.0278; B = 32 at V = 151936: 8 CTAs, 48 KB slices best (0.0690; dense
+// from one CTA per SM 0.0705, 16 CTAs 0.0755, 4 CTAs 0.0773); B = 64 at
+// V = 151936: 8 CTAs dense 0.0794, 4 CTAs 0.0814, 48 KB slices at three
+// CTAs per SM 0.0915; B = 128: 4 CTAs dense (one wave) 0.1403, 8 CTAs dense
+// (1.73 waves) 0.1473, 48 KB slices 0.1652.  sms: the GPU's SM count.
+// False when the vocabulary exceeds the slice table.
+#ifndef SV_DENSE_PER_SM
+#define SV_DENSE_PER_SM 2
+#endif
+inline bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e, int64_t sms)
+{
+    int ncl = draws * kCluster <= 2 * sms              ? kCluster
+              : draws * (kCluster / 2) <= 4 * sms ? kCluster / 2
+                                                       : kCluster / 4;
+#ifdef SV_NCL
+    ncl = SV_NCL;
+#endif
+    // a vocabulary whose ranges need more slices than the table holds takes
+    // more CTAs per draw
+    for (; ncl <= kCluster; ncl *= 2) {
+        if (draws * ncl > SV_DENSE_PER_SM * sms &&
+            fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
+            return true;
+        if (fill_draw_geometry(fp, ncl, V, e, kStageRowBytes))
+            return true;
+    }
+    return false;
+}
+
 // Store v at the address `local` has in the shared memory of cluster CTA `rank`.
 __device__ __forceinline__ void st_cluster_ff(ff *local, uint32_t rank, ff v)
 {

@@ -184,59 +184,6 @@ static cudaError_t prepare_draft_sample()
     return once;
 }
 
-// Slices of at most stage_bytes per row for ncl ranges of a V-entry row;
-// false when a range needs more slices than the slice table holds.
-static bool fill_draw_geometry(FinishParams &fp, int ncl, int V, int e, int stage_bytes)
-{
-    const int gran = 16 / e;
-    fp.ncl = ncl;
-    const int R = (int)((((int64_t)V + ncl - 1) / ncl + gran - 1) / gran * gran);
-    const int slice = std::min(R, stage_bytes / e);
-    const int nv = (slice * e + 15) / 16;
-    fp.R = R;
-    fp.slice = slice;
-    fp.pv = ((nv + kSampleThreads - 1) / kSampleThreads) | 1;  // odd: no bank conflicts
-    fp.stage_smem = (int)align_up((size_t)slice * e, 128);
-    return (R + slice - 1) / slice <= kMaxSlices;
-}
-
-// Geometry of a cluster draw over V entries, one cluster per draw: ncl
-// ranges of R entries, weighed in slices.  16 CTAs per draw while the
-// clusters fit the GPU at two CTAs per SM, else 8 while they fit it at four,
-// else 4; a grid of more than two CTAs per SM (a "dense" grid) takes slices
-// of half the largest size, so that four CTAs fit an SM, with the
-// finish-kernel instance whose registers allow four.  Measured on B300, ms
-// per step: B = 16, V = 128000: 16 CTAs 0.0206, 8 CTAs 0.0222, 4 CTAs
-// 0.0278; B = 32 at V = 151936: 8 CTAs, 48 KB slices best (0.0690; dense
-// from one CTA per SM 0.0705, 16 CTAs 0.0755, 4 CTAs 0.0773); B = 64 at
-// V = 151936: 8 CTAs dense 0.0794, 4 CTAs 0.0814, 48 KB slices at three
-// CTAs per SM 0.0915; B = 128: 4 CTAs dense (one wave) 0.1403, 8 CTAs dense
-// (1.73 waves) 0.1473, 48 KB slices 0.1652.  False when the vocabulary
-// exceeds the slice table.
-#ifndef SV_DENSE_PER_SM
-#define SV_DENSE_PER_SM 2
-#endif
-static bool draw_geometry(FinishParams &fp, int64_t draws, int V, int e)
-{
-    const int64_t sms = sm_count();
-    int ncl = draws * kCluster <= 2 * sms              ? kCluster
-              : draws * (kCluster / 2) <= 4 * sms ? kCluster / 2
-                                                       : kCluster / 4;
-#ifdef SV_NCL
-    ncl = SV_NCL;
-#endif
-    // a vocabulary whose ranges need more slices than the table holds takes
-    // more CTAs per draw
-    for (; ncl <= kCluster; ncl *= 2) {
-        if (draws * ncl > SV_DENSE_PER_SM * sms &&
-            fill_draw_geometry(fp, ncl, V, e, kStageRowBytes / 2))
-            return true;
-        if (fill_draw_geometry(fp, ncl, V, e, kStageRowBytes))
-            return true;
-    }
-    return false;
-}
-
 // Kernel 1's parameters for a verification call (a.out_tokens / a.out_len
 // may be null: then malformed offsets are only flagged, not poisoned).
 template <typename T, bool GREEDY>
@@ -331,7 +278,7 @@ static cudaError_t launch_typed(const VerifyArgs &a, cudaStream_t s, Tracer &tr)
     fp.draft_rows = a.draft_stride > 0 ? (int64_t)a.B * a.draft_stride : a.max_rows - a.B;
     fp.draft_stride = a.draft_stride;
     fp.g = g;
-    if (!GREEDY && !draw_geometry(fp, a.B, a.V, e))
+    if (!GREEDY && !draw_geometry(fp, a.B, a.V, e, sm_count()))
         return cudaErrorInvalidValue;  // vocabulary beyond the draw's slice table
     // the finish kernel merges up to two rows per warp of the cluster, then
     // one per warp of each CTA
