@@ -313,8 +313,9 @@ cudaError_t launch_dcut(const DcutArgs &a, cudaStream_t s, Tracer &tr)
 // pipes (fp64_exact.cuh; B300's fp64 pipe is slow), the hardware fp64 path
 // only for values outside the normal range.  One cluster of CTAs:
 // per-request best depths in parallel across its SMs, ranks by counting,
-// then one thread walks the ranked requests (the admission is sequential by
-// definition).
+// then the admission in rank order (sequential by definition), decided
+// block-wide from exact sums of the costs, the rounded running total taken
+// only where the rounding can matter.
 
 namespace sv {
 
@@ -425,10 +426,12 @@ __device__ __forceinline__ uint64_t pair_benefit(const uint64_t *cost_bits,
 //     stores (benefit, depth) into the shared memory of every CTA;
 //  2. every CTA ranks its share of the requests (larger benefit first, then
 //     lower request) by counting, and stores the rank into CTA 0;
-//  3. CTA 0 lays out the costs in rank order, one thread admits in rank
-//     order (sequential by definition: each addition rounded as binary64,
-//     on 128-bit integers in units of 2^-52), and the CTA writes depths,
-//     offsets and benefits.
+//  3. CTA 0 lays out the costs in rank order and admits in rank order: the
+//     exact sums of the costs (64-bit integers in units of 2^-52) decide
+//     every rank farther than the accumulated rounding margin from
+//     max_cost, by a block-wide prefix scan and block-wide searches; a rank
+//     inside the margin is decided on the binary64 running total.  The CTA
+//     then writes depths, offsets and benefits.
 __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostParams p)
 {
     extern __shared__ __align__(16) unsigned char dsm[];
@@ -590,7 +593,8 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
         //    fit: each is found by a block-wide search for the next rank
         //    that is not surely rejected.
         // A decision inside the margin (a budget on or next to a reachable
-        // sum) sends the whole walk to the rounded chain, one thread.
+        // sum) is taken on the rounded running total, as the scheduler's
+        // binary64 additions would.
         const uint64_t M = p.max_units, hu = p.half_ulp;
         const uint64_t SAT = ~0ull >> 1;  // above every budget
         const int per = (ncand + kCostThreads - 1) / kCostThreads;
@@ -644,7 +648,8 @@ __global__ void __launch_bounds__(kCostThreads) dcut_cost_kernel(const DcutCostP
             uint64_t X = s_x, T = 0, c_rej = ~0ull;
             bool have_T = false;
             int k = first, cur = first - 1, n_late = 0;
-            int late[4];  // ranks admitted from `first` on, in order (at most 3)
+            int late[4];  // ranks admitted from `first` on, in order: at most 3, since
+                          // the budget left is below one cost (<= 3) and every cost is >= 1
             for (;;) {
                 __syncthreads();  // every thread has read s_first
                 if (tid == 0)
