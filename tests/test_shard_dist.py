@@ -240,3 +240,30 @@ def test_two_gloo_ranks_exchange_records_and_agree_with_the_oracle(T):
     for r in range(world):
         _check(b, res[r])
     assert res[0]["tokens"].tolist() == res[1]["tokens"].tolist()
+
+
+def test_shard_bounds_and_columns():
+    """The vocabulary split: contiguous ranges in shard order covering [0, V)
+    with widths differing by at most one (the first V % N one wider), every
+    count from 1 to the limit, refused beyond it or beyond V; each shard's
+    columns put side by side give the logits back."""
+    from draft_verification_02_b300 import specverify as sv
+    from draft_verification_02_b300.sharded import shard_columns
+    for V in (1, 2, 7, 1000, 18992, 151936):
+        for n in range(1, min(V, sv.SPEC_MAX_SHARDS) + 1):
+            b = shard_bounds(V, n)
+            w = np.diff(b)
+            assert b[0] == 0 and b[-1] == V and len(b) == n + 1
+            assert w.min() >= 1 and w.max() - w.min() <= 1
+            assert (w[:V % n] == w.max()).all() and (w[V % n:] == V // n).all()
+        for bad in (0, min(V, sv.SPEC_MAX_SHARDS) + 1):
+            with pytest.raises(ValueError):
+                shard_bounds(V, bad)
+    x = torch.randn(5, 1003)
+    for n in (1, 3, 8):
+        b = shard_bounds(1003, n)
+        cols = shard_columns(x, b)
+        assert all(c.is_contiguous() and c.shape == (5, b[r + 1] - b[r])
+                   for r, c in enumerate(cols))
+        assert torch.equal(torch.cat(cols, dim=1), x)
+    assert shard_columns(None, shard_bounds(10, 2)) == [None, None]
