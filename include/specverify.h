@@ -192,7 +192,7 @@ int dcut_allocate(const float *conf, const int32_t *kmax, int32_t B, int32_t Kma
  * Python floats), each operation rounded once, so the depths are those of a
  * plain sequential fp64 evaluation.  Invalid confidences or kmax set
  * SPEC_ERR_INVALID_ARG on the device and write -1 depths and offsets.  One
- * kernel launch (one CTA); B <= SPEC_MAX_BATCH.
+ * kernel launch (one cluster of 8 CTAs); B <= SPEC_MAX_BATCH.
  */
 int dcut_allocate_cost(const float *conf, const int32_t *kmax, int32_t B, int32_t Kmax,
                        double max_cost, int32_t *out_depth, int32_t *out_cu,
